@@ -1,0 +1,502 @@
+"""Benchmark of the KV-cache eviction pass on GB300.
+
+Headline: the LORE-KV eviction pass (reliability weights, attention statistics, projected deletion
+scores, chunked top-B selection and gather-compaction: lorekv_score + lorekv_select_compact) on
+the Llama-3.1-8B-shaped 128K workload (1 sequence, 32 layers, 32/8 heads, d_head 128,
+n = 131072, bf16). A step is one full pass over all 256 (layer, KV head) units; the metric is KV
+tokens scored and compacted per second (a KV token = one (sequence, layer, KV head, position)).
+
+Also reported: the H2O decode mode (OPT-30B shape: batch 64, 48 layers, 56 heads, d_head 128,
+prompt 512, 512 decode steps) as KV tokens attended per second, and the fp64 oracle timed on the
+host cores (cpu_baseline).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--no-h2o]
+Under torchrun each rank runs its own sequence (the units are independent; no data exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KV tokens scored+compacted/sec (eviction pass, 128K ctx); % of HBM roofline"
+UNIT = "tokens/s"
+WORKLOAD = "llama"        # the 128K-context configuration the metric is quoted on
+
+# DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by the sha256 of the
+# kernel's source file at capture time; a changed source reports null until re-captured.
+NCU_TRAFFIC = {}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="native", choices=["native", "reference"])
+    p.add_argument("--no-h2o", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--workload", default=WORKLOAD)
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------------------------
+# distributed plumbing (host-side timing aggregation only)
+# ---------------------------------------------------------------------------------------------
+def dist_init(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return rank, world, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, value: float, device=None) -> float:
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64,
+                     device=device if device is not None and pg.get_backend() == "nccl" else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        rows = []
+        try:
+            with open(self.path) as f:
+                for r in csv.reader(f):
+                    if len(r) >= 9:
+                        rows.append([x.strip() for x in r])
+        finally:
+            if self.path and os.path.exists(self.path):
+                os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------------------------
+# byte / flop accounting (per KV token-unit; a unit = one (sequence, layer, KV head))
+# ---------------------------------------------------------------------------------------------
+def lorekv_algorithmic_bytes(cfg) -> int:
+    """K+V read once + Q_W + Q_look + logits + sampled ids read + compacted K', V' and kept
+    indices written (scores and other intermediates are not counted)."""
+    es = 2 if cfg.dtype == "bf16" else 4
+    kv = 2 * cfg.units * cfg.n * cfg.d * es
+    q = cfg.S * cfg.L * cfg.Hq * (cfg.w + cfg.M * cfg.T) * cfg.d * es
+    logits = cfg.S * cfg.M * cfg.T * cfg.vocab * 4 + cfg.S * cfg.M * cfg.T * 4
+    cap = cfg.n if cfg.n - cfg.sink - cfg.w <= cfg.B else cfg.sink + cfg.B + cfg.w
+    out = 2 * cfg.units * cap * cfg.d * es + cfg.units * cap * 4
+    return kv + q + logits + out
+
+
+def scores_algorithmic_flops_per_token_unit(cfg) -> int:
+    """The scoring kernel's algorithmic work per (token, unit): the cross term v.u_q for every
+    query (2 g Qh d) and the quadratic form ||L_h^T v||^2 per query head (g d (d+1))."""
+    Qh = cfg.w + cfg.M * cfg.T
+    return 2 * cfg.g * Qh * cfg.d + cfg.g * cfg.d * (cfg.d + 1)
+
+
+def attention_algorithmic_flops_per_token_unit(cfg) -> int:
+    """q.k and the a.v accumulation for every query: 4 g Qh d."""
+    Qh = cfg.w + cfg.M * cfg.T
+    return 4 * cfg.g * Qh * cfg.d
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p["bf16_tflops_sustained"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# GB300 FP32 FMA peak from unit counts and the maximum SM clock: 152 SMs x 128 FP32 lanes x 2
+# flop x 2.07 GHz.
+FP32_ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def src_hash(rel):
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+# ---------------------------------------------------------------------------------------------
+# the oracle as the CPU baseline / reference arm
+# ---------------------------------------------------------------------------------------------
+def oracle_sample(cfg, n_units: int, seed_layer: int = 0):
+    """Inputs of a bounded sample of the workload (whole units), generated on the host."""
+    import numpy as np
+    import torch
+    import oracle
+    from kv_cache_eviction_02_gb300 import synth
+    per_layer = cfg.Hkv
+    layers = list(range(seed_layer, seed_layer + max(1, math.ceil(n_units / per_layer))))
+    sub = cfg.replace(L=len(layers))
+    # the sample's layers are generated with the same seeds as the full workload's first layers
+    inp = synth.lorekv_inputs(sub, "cpu")
+    units = [(0, l, kh) for l in range(len(layers)) for kh in range(cfg.Hkv)][:n_units]
+    g, d = cfg.g, cfg.d
+    prep = []
+    for (s, l, kh) in units:
+        u = synth.unit_slice(sub, inp, s, l, kh)
+        Lf = np.stack([oracle.gram_cholesky(u["W_O"], d, kh * g + j)[1] for j in range(g)])
+        prep.append((u, Lf))
+    K = np.stack([oracle._d(u["K"]) for u, _ in prep])
+    V = np.stack([oracle._d(u["V"]) for u, _ in prep])
+    QW = np.stack([oracle._d(u["Q_W"]) for u, _ in prep])
+    QL = np.stack([oracle._d(u["Q_look"]) for u, _ in prep])
+    Lf = np.stack([lf for _, lf in prep])
+    logits = oracle._d(inp["logits"][0])
+    sampled = inp["sampled"][0].numpy()
+    qlook_all = oracle._d(inp["Q_look"][0])
+    del inp
+    torch.set_num_threads(max(1, torch.get_num_threads()))
+    return {"K": K, "V": V, "QW": QW, "QL": QL, "Lf": Lf, "logits": logits, "sampled": sampled,
+            "qlook": qlook_all, "units": len(units)}
+
+
+def oracle_step(cfg, smp):
+    """One bounded oracle pass: reliability, scores of the sampled units (OpenMP over units),
+    chunked top-B selection and gather."""
+    import numpy as np
+    import oracle
+    om = oracle.reliability(smp["logits"], smp["sampled"], smp["qlook"], cfg.M, cfg.T, cfg.beta,
+                            cfg.gamma, cfg.lambda_D)["omega"]
+    S = oracle.lorekv_units(smp["K"], smp["V"], smp["QW"], smp["QL"], smp["Lf"],
+                            np.tile(om, (smp["units"], 1)), M=cfg.M, T=cfg.T, sink=cfg.sink,
+                            lambda_L=cfg.lambda_L, eps=cfg.eps, window_causal=cfg.window_causal)
+    for u in range(smp["units"]):
+        kept = oracle.select(S[u], sink=cfg.sink, w=cfg.w, chunk=cfg.chunk, B=cfg.B)
+        oracle.compact(smp["K"][u], kept)
+        oracle.compact(smp["V"][u], kept)
+    return S
+
+
+def cpu_baseline(cfg, steps=1, warmup=0):
+    import oracle
+    threads = oracle.threads()
+    smp = oracle_sample(cfg, threads)
+    for _ in range(warmup):
+        oracle_step(cfg, smp)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_step(cfg, smp)
+    dt = (time.perf_counter() - t0) / steps
+    tokens = smp["units"] * cfg.n
+    return {"value": tokens / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{smp['units']} whole units (layer, KV head) of the {cfg.name} workload, "
+                      f"{cfg.n} tokens each, reliability + scores + top-B + gather, fp64, "
+                      f"OpenMP over units", "seconds_per_step": dt}
+
+
+def run_reference(args):
+    rank, world, local, pg = dist_init(args)
+    from kv_cache_eviction_02_gb300 import synth
+    cfg = synth.LOREKV_CONFIGS[args.workload]
+    if rank != 0:
+        barrier(pg)
+        return
+    cb = cpu_baseline(cfg, steps=args.steps, warmup=args.warmup)
+    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": cb["seconds_per_step"] * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{cfg.name}: 1 seq x {cfg.L} layers x {cfg.Hq}/{cfg.Hkv} "
+                                   f"heads, d_head {cfg.d}, n {cfg.n}, bf16 inputs",
+                       "sample": cb["sample"]},
+            "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    barrier(pg)
+
+
+# ---------------------------------------------------------------------------------------------
+# native arm
+# ---------------------------------------------------------------------------------------------
+def run_native(args):
+    import torch
+    from kv_cache_eviction_02_gb300 import api, synth
+
+    rank, world, local, pg = dist_init(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = synth.LOREKV_CONFIGS[args.workload]
+    if world > 1:
+        cfg = cfg.replace(seed=cfg.seed + rank)   # each rank scores its own sequence
+    pk = peaks()
+    stream = torch.cuda.current_stream(dev)
+
+    # ---- inputs resident in HBM, per-model preparation (not timed) ----
+    g = synth.lorekv_inputs(cfg, dev)
+    pb = api.LorekvProblem.from_config(cfg)
+    Lf = torch.empty(cfg.L, cfg.Hq, cfg.d, cfg.d, device=dev)
+    G = torch.empty_like(Lf)
+    api.lorekv_prepare_wo(pb, g["W_O"], Lf, G)
+    run = api.LorekvPass(pb, dev)
+    for _ in range(args.warmup):
+        run.run(g, Lf, G)
+    api.kve_check_device()
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region: K passes, inputs (17 GB) larger than L2 ----
+    api.kve_profile_enable(True)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(pg)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            run.run(g, Lf, G)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(pg)
+    api.kve_profile_enable(False)
+    prof = api.kve_profile_report()
+    api.kve_check_device()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = max_over_ranks(pg, ms, dev)
+    tokens_per_step = cfg.units * cfg.n
+    value = tokens_per_step * world / (ms / 1e3)
+    alg_bytes = lorekv_algorithmic_bytes(cfg)
+    gpu_launches = sum(v["kernels"] for v in prof.values())
+
+    # dominant kernel roofline (live CUDA-event timing of the kernel's launches)
+    dom = max(prof, key=lambda k: prof[k]["ms"])
+    dom_ms = prof[dom]["ms"] / prof[dom]["groups"]
+    if dom == "scores":
+        flops = scores_algorithmic_flops_per_token_unit(cfg) * tokens_per_step
+    elif dom == "attention":
+        flops = attention_algorithmic_flops_per_token_unit(cfg) * tokens_per_step
+    else:
+        flops = None
+    kernel_src = {"scores": "kv_cache_eviction_02_gb300/csrc/pass_simt.cu",
+                  "attention": "kv_cache_eviction_02_gb300/csrc/pass_simt.cu"}.get(dom)
+    traffic = None
+    if kernel_src and dom in NCU_TRAFFIC and NCU_TRAFFIC[dom][1] == src_hash(kernel_src):
+        traffic = NCU_TRAFFIC[dom][0]
+    if flops is not None:
+        ach = flops / (dom_ms / 1e3) / 1e12
+        roof = {"kernel": dom, "bound": "alu", "achieved": ach, "peak": FP32_ALU_PEAK_TFLOPS,
+                "unit": "TFLOP/s", "frac": ach / FP32_ALU_PEAK_TFLOPS, "traffic": traffic,
+                "peak_source": "FP32 FMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz",
+                "ms_per_launch": dom_ms}
+    else:
+        ach = alg_bytes / (dom_ms / 1e3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": traffic,
+                "ms_per_launch": dom_ms}
+    hbm_achieved = alg_bytes / (ms / 1e3) / 1e9
+    stages = {k: {"ms_per_step": v["ms"] / args.steps, "kernels": v["kernels"]}
+              for k, v in prof.items()}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": cfg.dtype, "data": "synthetic",
+            "config": {"workload": f"{cfg.name}: {cfg.S} seq x {cfg.L} layers x {cfg.Hq}/{cfg.Hkv} "
+                                   f"heads, d_head {cfg.d}, d_model {cfg.d_model}, n {cfg.n}, "
+                                   f"vocab {cfg.vocab}, w {cfg.w}, M {cfg.M}, T {cfg.T}, "
+                                   f"B {cfg.B}, chunk {cfg.chunk}, sink {cfg.sink}",
+                       "units_per_gpu": cfg.units, "kv_tokens_per_step_per_gpu": tokens_per_step,
+                       "l2": f"inputs larger than L2 ({alg_bytes / 1e9:.1f} GB per pass)",
+                       "parallelism": f"replicas: {world} x independent sequence"},
+            "hbm_roofline": {"algorithmic_bytes": alg_bytes, "achieved_gbs": hbm_achieved,
+                             "peak_gbs": pk["hbm_gbs"], "frac": hbm_achieved / pk["hbm_gbs"],
+                             "peak_source": pk["source"]},
+            "roofline": roof, "stages": stages, "gpu_launches": gpu_launches,
+            "clocks": clk.summary()}
+
+    # ---- end to end through the public API with host buffers ----
+    if not args.no_e2e:
+        line["e2e"] = e2e_lorekv(cfg, g, run, Lf, G, dev, stream, pg, world, args)
+    del g
+    torch.cuda.empty_cache()
+
+    if not args.no_h2o:
+        line["h2o"] = bench_h2o(dev, stream, pg, world, args, pk)
+    if rank == 0 and not args.no_cpu:
+        try:
+            cb = cpu_baseline(cfg)
+            line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind",
+                                                       "sample")}
+        except Exception as e:  # the baseline is reported, never required
+            line["cpu_baseline"] = {"value": None, "error": repr(e)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    barrier(pg)
+
+
+def e2e_lorekv(cfg, g, run, Lf, G, dev, stream, pg, world, args):
+    """Host buffers in, host buffers out: per step the inputs are copied from pinned host memory,
+    the pass runs, and the compressed cache is read back."""
+    import torch
+    names = ["K", "V", "Q_W", "Q_look", "logits", "sampled"]
+    host = {k: torch.empty(g[k].shape, dtype=g[k].dtype, pin_memory=True) for k in names}
+    for k in names:
+        host[k].copy_(g[k])
+    dev_in = {k: torch.empty_like(g[k]) for k in names}
+    outs = [run.kept_idx, run.kept_len, run.K_out, run.V_out, run.omega]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(host[k].numel() * host[k].element_size() for k in names)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    steps = max(1, min(args.steps, 3))
+
+    def one():
+        for k in names:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        run.run(dev_in, Lf, G)
+        for t, h in zip(outs, host_out):
+            h.copy_(t, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize(dev)
+    barrier(pg)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(pg, e0.elapsed_time(e1) / steps, dev)
+    del host, dev_in
+    return {"value": cfg.units * cfg.n * world / (ms / 1e3), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "steps": steps}
+
+
+def bench_h2o(dev, stream, pg, world, args, pk):
+    """H2O decode on the OPT-30B shape: prefill once (timed separately), then the decode steps
+    with the first `warmup` steps untimed."""
+    import torch
+    from kv_cache_eviction_02_gb300 import api, synth
+    cfg = synth.H2O_CONFIGS["opt30b"]
+    hin = synth.h2o_inputs(cfg, dev)
+    st = api.h2o_state_create(cfg.batch, cfg.L, cfg.H, cfg.d, cfg.prompt + cfg.steps,
+                              cfg.budget_frac, torch.float16)
+    api.kve_profile_enable(True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    st.prefill(hin["K"], hin["V"], hin["Q"])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    prefill_ms = e0.elapsed_time(e1)
+    api.kve_profile_report()
+    out = torch.empty(cfg.batch, cfg.L, cfg.H, cfg.d, dtype=torch.float16, device=dev)
+    w = min(max(args.warmup, 3), cfg.steps - 1)
+    for t in range(w):
+        st.decode_step(hin["q"][t], hin["k"][t], hin["v"][t], out)
+    torch.cuda.synchronize(dev)
+    barrier(pg)
+    e0.record(stream)
+    for t in range(w, cfg.steps):
+        st.decode_step(hin["q"][t], hin["k"][t], hin["v"][t], out)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    api.kve_profile_enable(False)
+    prof = api.kve_profile_report()
+    steps = cfg.steps - w
+    ms = max_over_ranks(pg, e0.elapsed_time(e1) / steps, dev)
+    # tokens attended per step: after appending at length t the unit holds floor(0.2 (t-1)) + 1
+    held = [math.floor(cfg.budget_frac * (cfg.prompt + s)) + 1 for s in range(w, cfg.steps)]
+    tokens = cfg.units * sum(held) / steps
+    row = 2 * cfg.d * 2            # K and V row bytes
+    per_step_bytes = cfg.units * (sum(held) / steps * (row + 8) + 4 * cfg.d * 2 + 16)
+    step_ms = prof["h2o_step"]["ms"] / prof["h2o_step"]["groups"]
+    ach = per_step_bytes / (step_ms / 1e3) / 1e9
+    st.close()
+    del hin
+    torch.cuda.empty_cache()
+    return {"metric": "KV tokens attended+scored/sec (H2O decode step)",
+            "value": tokens * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+            "steps": steps, "warmup": w, "prefill_ms": prefill_ms,
+            "config": f"opt30b: batch {cfg.batch}, {cfg.L} layers, {cfg.H} heads, d_head {cfg.d}, "
+                      f"prompt {cfg.prompt}, {cfg.steps} decode steps, budget 20%, fp16",
+            "roofline": {"kernel": "h2o_step", "bound": "hbm", "achieved": ach,
+                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
+                         "traffic": None, "bytes_per_launch": per_step_bytes}}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+/*
+ * kvevict — C-ABI of the GB300 (sm_103a) KV-cache eviction library.
+ *
+ * Two eviction modes:
+ *   LORE-KV  (project page "LORE-KV: Monte Carlo Estimation for KV-Cache Eviction"): score every
+ *            cached token of every KV head by its projected deletion score under the window and
+ *            lookahead queries, then keep the protected sink/window plus the top-B tokens in
+ *            chunks of 4 and gather them into a dense compressed cache.
+ *   H2O      (paper summary "H2O: Heavy-Hitter Oracle for Efficient Generative Inference of Large
+ *            Language Models"): per-step decode eviction by accumulated attention, with half of
+ *            the budget reserved for the most recent tokens.
+ *
+ * Conventions, for every call below:
+ *   - Tensor arguments are DEVICE pointers (unless a comment says otherwise), row-major, densely
+ *     packed, and owned by the caller. The library never frees them and keeps no reference after
+ *     the call returns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Calls enqueue
+ *     kernels on that stream and return without synchronising, except where stated.
+ *   - Every call returns a status (KVE_OK = 0). On failure nothing is enqueued, unless the status
+ *     is KVE_ECUDA (a CUDA launch failed); kve_last_error() then gives a message for the calling
+ *     thread. No exception crosses this interface and nothing falls back to the CPU.
+ *   - The scoring and selection calls allocate no device memory: their scratch lives in a
+ *     caller-provided workspace of at least the size the matching *_workspace_size() call returns.
+ *   - Kernels that wait on an on-chip barrier give up after a bounded number of polls and record
+ *     the failure in a device error word; kve_check_device(stream) synchronises the stream and
+ *     turns a recorded failure into KVE_ETIMEOUT.
+ *
+ * Notation follows the pages: K, V cached keys/values; Q_W the w window queries (last prompt
+ * tokens); Q_look the M x T lookahead queries; W_O the attention output projection; logits and
+ * sampled ids of the lookahead tokens; B the budget; chunk the adjacent-token group size.
+ */
+#ifndef KVEVICT_H
+#define KVEVICT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------------------------- */
+#define KVE_OK 0
+#define KVE_EINVAL 1     /* a size, shape rule or pointer is invalid                             */
+#define KVE_EDTYPE 2     /* dtype not supported by this call                                      */
+#define KVE_EWORKSPACE 3 /* workspace missing or smaller than *_workspace_size()                  */
+#define KVE_ENOTPD 4     /* W_O^h^T W_O^h is not positive definite (Cholesky pivot <= 0)         */
+#define KVE_ECUDA 5      /* a CUDA runtime call failed                                            */
+#define KVE_ETIMEOUT 6   /* a bounded on-device wait gave up (see kve_check_device)               */
+
+/* ---- element types ------------------------------------------------------------------------ */
+#define KVE_F32 0
+#define KVE_BF16 1
+#define KVE_F16 2
+
+/* Problem shape of one LORE-KV pass. A "unit" is one (sequence, layer, KV head); there are
+ * n_seq * n_layers * n_kv_heads units. Query head h belongs to KV head h / (n_q_heads/n_kv_heads)
+ * (grouped-query attention). dtype is the element type of K, V, Q_W, Q_look and W_O. */
+typedef struct {
+    int n_seq, n_layers, n_q_heads, n_kv_heads, d_head, d_model, n_tokens, vocab;
+    int dtype;
+} KveShape;
+
+/* Method parameters (LORE-KV page, "Hyperparameters" table; defaults w=32, M=4, T=8,
+ * lambda_L=1, (beta, gamma, lambda_D) = (1, 1.3, 0) for /E or (1, 1, 0.3) for /D, eps=1e-6,
+ * chunk=4). sink = number of leading tokens always kept (attention sink). budget_B = number of
+ * non-protected tokens kept per KV head (a multiple of chunk). window_causal = 1: window query r
+ * (0-based, at position n-w+r) attends only to tokens i <= n-w+r; lookahead queries see all n. */
+typedef struct {
+    int w, M, T, chunk, sink, budget_B, window_causal;
+    float lambda_L, beta, gamma, lambda_D, eps;
+} KveLorekvParams;
+
+/* ---- LORE-KV -------------------------------------------------------------------------------- */
+
+/* Per-model preparation of e = ||W_O^h x|| (LORE-KV page, Method, Eqs. 5-7): for every layer l
+ * and query head h, G = W_O^h^T W_O^h and its Cholesky factor L (G = L L^T, L lower triangular),
+ * so that ||W_O^h x|| = ||L^T x||. W_O^h is columns h*d .. h*d+d-1 of the o_proj weight.
+ *   W_O   [n_layers][d_model][n_q_heads*d_head]   shape->dtype
+ *   L_out [n_layers][n_q_heads][d_head][d_head]   fp32 (upper triangle written as 0)
+ *   G_out [n_layers][n_q_heads][d_head][d_head]   fp32
+ * Synchronises `stream` before returning (it must read the positive-definiteness flag).
+ * Returns KVE_ENOTPD if any G is not positive definite. */
+int lorekv_prepare_wo(const KveShape *shape, const void *W_O, float *L_out, float *G_out,
+                      void *stream);
+
+/* Bytes of workspace lorekv_score() needs for this shape and parameters. 0 on invalid input. */
+size_t lorekv_workspace_size(const KveShape *shape, const KveLorekvParams *params);
+
+/* Scores every cached token (LORE-KV page, Method, Eqs. 2-7).
+ *   K, V      [n_seq][n_layers][n_kv_heads][n_tokens][d_head]   shape->dtype
+ *   Q_W       [n_seq][n_layers][n_q_heads][w][d_head]           shape->dtype
+ *   Q_look    [n_seq][n_layers][n_q_heads][M*T][d_head]         shape->dtype, row m*T+t
+ *   L, G      from lorekv_prepare_wo                            fp32
+ *   logits    [n_seq][M*T][vocab] fp32, row m*T+t is the next-token logits at lookahead token t
+ *             of trajectory m; sampled [n_seq][M*T] int32 is the token drawn there.
+ *   scores_out [n_seq][n_layers][n_kv_heads][n_tokens] fp32: S_i = mean_W e + lambda_L *
+ *             sum_m omega_m mean_m e, with e = a/(1-a+eps) ||L_h^T (v_i - o_q)|| and the means over
+ *             all g query heads of the KV head; 0 for protected tokens (i < sink or i >= n-w).
+ *   omega_out [n_seq][M] fp32: omega = softmax(beta*cbar - gamma*Hbar - lambda_D*Dhat) (Eq. 10).
+ * Requirements: n_tokens >= sink + w; n_q_heads % n_kv_heads == 0; dtype KVE_F32 or KVE_BF16;
+ * d_head a multiple of 32 (KVE_F32) or 128 (KVE_BF16); sampled ids in [0, vocab). */
+int lorekv_score(const KveShape *shape, const KveLorekvParams *params, const void *K,
+                 const void *V, const void *Q_W, const void *Q_look, const float *L,
+                 const float *G, const float *logits, const int32_t *sampled, float *scores_out,
+                 float *omega_out, void *workspace, size_t ws_bytes, void *stream);
+
+/* Attention statistics only (the first half of lorekv_score, exposed for testing): for each unit
+ * and each of its g*(w+M*T) queries (query head major, then window rows, then lookahead rows):
+ *   lse_out [units][g*(w+M*T)] fp32 natural-log log-sum-exp of q.k/sqrt(d) over visible tokens,
+ *   o_out   [units][g*(w+M*T)][d_head] fp32 attention output o_q.
+ * Uses the same workspace as lorekv_score. */
+int lorekv_attention_stats(const KveShape *shape, const KveLorekvParams *params, const void *K,
+                           const void *V, const void *Q_W, const void *Q_look, float *lse_out,
+                           float *o_out, void *workspace, size_t ws_bytes, void *stream);
+
+/* Kept-row capacity per unit: n_tokens if n - sink - w <= budget_B, else sink + budget_B + w. */
+int lorekv_kept_capacity(const KveShape *shape, const KveLorekvParams *params);
+
+/* Chunked top-B selection and gather-compaction (LORE-KV page, "Evict and decode", Eq. 8;
+ * "Hyperparameters": adjacent-token chunks of `chunk`).
+ *   scores   [units][n_tokens] fp32 from lorekv_score
+ *   K, V     as in lorekv_score
+ *   kept_idx [units][cap] int32, cap = lorekv_kept_capacity(): kept positions, ascending
+ *   kept_len [units] int32
+ *   K_out, V_out [units][cap][d_head] shape->dtype: K_out[u][j] = K[u][kept_idx[u][j]]
+ * Chunk c covers tokens [sink + c*chunk, sink + (c+1)*chunk); its score is the mean of S over
+ * the chunk; the budget_B/chunk chunks with the highest score are kept (equal scores: lower c).
+ * (n_tokens - sink - w) and budget_B must be multiples of chunk. Needs no workspace: pass NULL, 0
+ * (a non-NULL workspace is accepted and ignored). */
+int lorekv_select_compact(const KveShape *shape, const KveLorekvParams *params,
+                          const float *scores, const void *K, const void *V, int32_t *kept_idx,
+                          int32_t *kept_len, void *K_out, void *V_out, void *workspace,
+                          size_t ws_bytes, void *stream);
+
+/* ---- H2O ------------------------------------------------------------------------------------ */
+
+/* Opaque decode state. It owns preallocated device slots for K, V, accumulated scores and
+ * positions of every (batch, layer, head) unit (H2O summary, Appendix A: preallocated memory,
+ * evicted slots are overwritten in place). */
+typedef struct KveH2O KveH2O;
+
+/* Allocates the state for batch x n_layers x n_heads units of head size d_head, for sequences of
+ * up to max_len tokens (prompt + decode steps), budget_frac in (0, 1]. Slot capacity per unit is
+ * floor(budget_frac*max_len) + 1. dtype KVE_F16 or KVE_BF16. *out receives the handle. */
+int h2o_state_create(KveH2O **out, int batch, int n_layers, int n_heads, int d_head, int max_len,
+                     float budget_frac, int dtype);
+
+/* Prefill (H2O summary, Section 4.1; prompt handled as one block): accumulated scores of the
+ * prompt tokens are the causal-attention column sums acc_j = sum_{i>=j} softmax_i(q_i.K_{<=i}/
+ * sqrt d)_j; then the cache is compressed to k_t = floor(budget_frac*t) tokens (t = prompt_len):
+ * the r_t = floor(k_t/2) most recent are kept, and among the rest the highest accumulated scores
+ * (equal scores: the newer token stays).
+ *   K, V, Q [batch][n_layers][n_heads][prompt_len][d_head] state dtype. */
+int h2o_prefill(KveH2O *st, const void *K, const void *V, const void *Q, int prompt_len,
+                void *stream);
+
+/* One decode step for every unit (H2O summary, Section 4.1, Algorithm 1 with linear h; Section
+ * 2.1 and Definition 2.2 for attention over the retained set; Definition 2.1: at most one
+ * eviction per step): append (k_new, v_new) into a free slot; attend with q over the retained
+ * tokens including the new one; add the softmax row to the accumulated scores; with t the new
+ * length, k_t = floor(budget_frac*t) and r_t = floor(k_t/2), while more than k_t tokens are held
+ * evict the lowest accumulated score among positions < t - r_t (equal scores: the oldest).
+ *   q, k_new, v_new, attn_out [batch][n_layers][n_heads][d_head] state dtype;
+ *   attn_out = softmax(q.K/sqrt d) V over the retained tokens. */
+int h2o_decode_step(KveH2O *st, const void *q, const void *k_new, const void *v_new,
+                    void *attn_out, void *stream);
+
+/* Copies the state out (device pointers, any may be NULL):
+ *   K, V [units][cap][d_head] state dtype; pos [units][cap] int32 (-1 for an empty slot);
+ *   acc [units][cap] fp32; count [units] int32 (retained tokens). */
+int h2o_export(const KveH2O *st, void *K, void *V, int32_t *pos, float *acc, int32_t *count,
+               void *stream);
+
+/* Slot capacity per unit and the current sequence length t (tokens seen so far). */
+int h2o_capacity(const KveH2O *st);
+int h2o_length(const KveH2O *st);
+
+void h2o_state_destroy(KveH2O *st);
+
+/* ---- diagnostics ---------------------------------------------------------------------------- */
+
+/* Message of the last failing call on this thread ("" if none). Valid until the next call. */
+const char *kve_last_error(void);
+
+/* Synchronises `stream`, then reads and clears the device error word that bounded on-device
+ * waits set. Returns KVE_OK, KVE_ETIMEOUT (a wait gave up) or KVE_ECUDA. */
+int kve_check_device(void *stream);
+
+/* Host-side fault injection for tests: the next `count` calls of the API (excluding the
+ * diagnostics) fail with `status` before touching the GPU. count = 0 clears it. */
+int kve_inject_failure(int status, int count);
+
+/* Kernel timing for measurement: while enabled, every launch group of the library (one
+ * pipeline stage, e.g. "scores" or "select_compact") is bracketed by CUDA events recorded on the
+ * stream it runs on. Disabled by default; enabling costs two event records per stage. */
+int kve_profile_enable(int on);
+
+/* Synchronises on the recorded events and writes one line per stage into buf (host memory,
+ * NUL-terminated, truncated to len): "<stage> <launch groups> <kernels> <total ms>\n". Clears the
+ * record. Returns the number of stages, or -KVE_EINVAL if buf is NULL. */
+int kve_profile_report(char *buf, size_t len);
+
+/* Library version (major*10000 + minor*100 + patch). */
+int kve_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVEVICT_H */

@@ -1,0 +1,116 @@
+// Internal declarations shared by the library's translation units (not part of the C-ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvevict.h"
+
+namespace kve {
+
+// ---- element conversion ------------------------------------------------------------------------
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f(__half x) { return __half2float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+template <> __device__ __forceinline__ __half from_f<__half>(float x) { return __float2half_rn(x); }
+
+inline size_t dtype_size(int dt) { return dt == KVE_F32 ? 4 : 2; }
+
+// ---- device error word -------------------------------------------------------------------------
+// Bit 0: a bounded wait on an mbarrier gave up. The host reads and clears it in kve_check_device.
+enum : unsigned { KVE_DEVERR_TIMEOUT = 1u };
+unsigned *device_error_word();  // device address of the word (per device, set up lazily)
+
+// ---- warp helpers ------------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ---- LORE-KV launch description ----------------------------------------------------------------
+struct LorekvDims {
+    int S, L, Hq, Hkv, g, d, d_model, n, vocab, dtype;
+    int w, M, T, MT, nq;       // nq = w + M*T queries per query head
+    int Qu;                    // g * nq queries per unit
+    int units;                 // S * L * Hkv
+    int chunk, sink, B, window_causal;
+    float lambda_L, beta, gamma, lambda_D, eps;
+    int nsplit;                // token splits of the attention-statistics pass
+    int split_len;             // tokens per split (multiple of 128)
+    int rel_splits;            // CTAs per logits row in the reliability pass
+};
+
+// Workspace carve-up of lorekv_score (byte offsets, 256-aligned).
+struct LorekvWorkspace {
+    size_t part_ml, part_o;    // split partials: [units][nsplit][Qu] float2 (m2, l), [..][d] f32
+    size_t lse2, o;            // combined: [units][Qu] f32 (log2 domain), [units][Qu][d] f32
+    size_t u32, cq, wq;        // u = G o [units][Qu][d] f32; c = o^T G o, weight [units][Qu]
+    size_t u16, lt16;          // bf16 operands: U [units][Qu][d]; L^T packed [L][Hq][d][d]
+    size_t q16;                // bf16 queries packed [units][Qu][d]
+    size_t part_s;             // per-query-head partial scores [units][g][n] f32
+    size_t rel_part;           // reliability partials [S][MT][rel_splits] float4
+    size_t cosm;               // cosine sums [S][L*Hq][M][M] f32
+    size_t total;
+};
+
+bool lorekv_dims(const KveShape *sh, const KveLorekvParams *p, LorekvDims *D, const char **why);
+LorekvWorkspace lorekv_ws_layout(const LorekvDims &D);
+
+// ---- launchers (each returns cudaGetLastError() of its launches) -------------------------------
+cudaError_t launch_reliability(const LorekvDims &D, const void *Q_look, const float *logits,
+                               const int32_t *sampled, float *omega_out, void *ws,
+                               const LorekvWorkspace &W, cudaStream_t st);
+cudaError_t launch_prepare_wo(int L, int Hq, int d, int d_model, int dtype, const void *W_O,
+                              float *L_out, float *G_out, int *notpd_flag, cudaStream_t st);
+cudaError_t launch_attention_simt(const LorekvDims &D, const void *K, const void *V,
+                                  const void *QW, const void *QL, void *ws,
+                                  const LorekvWorkspace &W, cudaStream_t st);
+cudaError_t launch_combine(const LorekvDims &D, void *ws, const LorekvWorkspace &W,
+                           float *lse_out, float *o_out, cudaStream_t st);
+cudaError_t launch_prep_u(const LorekvDims &D, const float *G, const float *omega, void *ws,
+                          const LorekvWorkspace &W, cudaStream_t st);
+cudaError_t launch_scores_simt(const LorekvDims &D, const void *K, const void *V,
+                               const void *QW, const void *QL, const float *Lf, void *ws,
+                               const LorekvWorkspace &W, float *scores, cudaStream_t st);
+cudaError_t launch_select_compact(const LorekvDims &D, const float *scores, const void *K,
+                                  const void *V, int32_t *kept_idx, int32_t *kept_len,
+                                  void *K_out, void *V_out, int cap, cudaStream_t st);
+
+// H2O
+struct H2OState {
+    int batch, L, H, d, max_len, cap, dtype;
+    float frac;
+    int units;
+    int t;             // tokens seen so far
+    int prefilled;
+    void *K, *V;       // [units][cap][d]
+    float *acc;        // [units][cap]
+    int32_t *pos;      // [units][cap], -1 = empty
+    int32_t *nslots;   // [units] slots in use (including a hole)
+    int32_t *hole;     // [units] free slot left by the last eviction, -1 if none
+};
+cudaError_t launch_h2o_prefill(H2OState &s, const void *K, const void *V, const void *Q, int P,
+                               cudaStream_t st);
+cudaError_t launch_h2o_step(H2OState &s, const void *q, const void *k, const void *v, void *out,
+                            cudaStream_t st);
+cudaError_t launch_h2o_export(const H2OState &s, void *K, void *V, int32_t *pos, float *acc,
+                              int32_t *count, cudaStream_t st);
+
+}  // namespace kve

@@ -1,0 +1,415 @@
+// LORE-KV scoring on CUDA cores (FP32 FMA). This is the path for fp32 inputs and for shapes the
+// tensor-core kernels do not cover; it computes exactly what the tensor-core path computes.
+//
+// Attention statistics (LORE-KV page, Method: a_{q,i} = softmax_i(q.k_i/sqrt d), o_q =
+// sum_i a_{q,i} v_i): each CTA takes 32 queries of one unit and one split of the tokens, with an
+// online softmax in the log2 domain; a combine kernel merges the splits.
+//
+// Per-query prep: u_q = G_h o_q and c_q = o_q^T G_h o_q, so that
+//   ||L_h^T (v_i - o_q)||^2 = ||L_h^T v_i||^2 - 2 v_i.u_q + c_q,
+// plus the weight of the query in S_i (1/(g w) for window queries, lambda_L omega_m/(g T) for
+// the lookahead queries of trajectory m; psi = mean).
+//
+// Scores (Eqs. 5-7): e_{q,i} = a_{q,i}/(1-a_{q,i}+eps) * sqrt(x_{q,i}), S_i = sum_q weight_q e_{q,i}.
+#include "kve_internal.cuh"
+
+namespace kve {
+
+namespace {
+
+constexpr int kQB = 32;  // queries per CTA in the statistics pass
+constexpr int kTT = 32;  // tokens per shared-memory tile
+
+template <typename T>
+__device__ __forceinline__ const T *query_ptr(const T *QW, const T *QL, const LorekvDims &D,
+                                              int unit, int qi) {
+    const int kh = unit % D.Hkv;
+    const int sl = unit / D.Hkv;  // s*L + l
+    const int j = qi / D.nq, r = qi % D.nq;
+    const int h = kh * D.g + j;
+    if (r < D.w) return QW + (((size_t)sl * D.Hq + h) * D.w + r) * D.d;
+    return QL + (((size_t)sl * D.Hq + h) * D.MT + (r - D.w)) * D.d;
+}
+
+__device__ __forceinline__ int visible_tokens(const LorekvDims &D, int qi) {
+    const int r = qi % D.nq;
+    return (r < D.w && D.window_causal) ? D.n - D.w + r + 1 : D.n;
+}
+
+// grid (ceil(Qu/32), nsplit, units), block 256 (8 warps x 4 queries). DPL = d/32 dims per lane.
+template <typename T, int DPL>
+__global__ void __launch_bounds__(256) attn_partial_kernel(const T *__restrict__ K,
+                                                           const T *__restrict__ V,
+                                                           const T *__restrict__ QW,
+                                                           const T *__restrict__ QL, LorekvDims D,
+                                                           float2 *__restrict__ part_ml,
+                                                           float *__restrict__ part_o) {
+    constexpr int d = DPL * 32;
+    extern __shared__ float sm[];
+    float *qs = sm;                       // [kQB][d]
+    float *ks = qs + kQB * d;             // [kTT][d+1]
+    float *vs = ks + kTT * (d + 1);       // [kTT][d+1]
+    const int qb = blockIdx.x, sp = blockIdx.y, unit = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float qscale = kLog2e * rsqrtf((float)d);
+    for (int idx = threadIdx.x; idx < kQB * d; idx += blockDim.x) {
+        const int qq = idx / d, k = idx % d;
+        const int qi = qb * kQB + qq;
+        qs[idx] = (qi < D.Qu) ? to_f(query_ptr(QW, QL, D, unit, qi)[k]) * qscale : 0.f;
+    }
+    const int t0 = sp * D.split_len, t1 = min(D.n, t0 + D.split_len);
+    const T *Ku = K + (size_t)unit * D.n * d;
+    const T *Vu = V + (size_t)unit * D.n * d;
+    float m[4], l[4], o[4][DPL];
+    int nvis[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        m[a] = -INFINITY;
+        l[a] = 0.f;
+        const int qi = qb * kQB + warp * 4 + a;
+        nvis[a] = (qi < D.Qu) ? visible_tokens(D, qi) : 0;
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) o[a][c] = 0.f;
+    }
+    for (int base = t0; base < t1; base += kTT) {
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < kTT * d; idx += blockDim.x) {
+            const int tt = idx / d, k = idx % d;
+            const int tok = base + tt;
+            ks[tt * (d + 1) + k] = (tok < t1) ? to_f(Ku[(size_t)tok * d + k]) : 0.f;
+            vs[tt * (d + 1) + k] = (tok < t1) ? to_f(Vu[(size_t)tok * d + k]) : 0.f;
+        }
+        __syncthreads();
+        const int tok = base + lane;
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        const float *kr = ks + lane * (d + 1);
+        const float *qr = qs + (warp * 4) * d;
+        for (int k = 0; k < d; ++k) {
+            const float kv = kr[k];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) s[a] = fmaf(qr[a * d + k], kv, s[a]);
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const bool valid = tok < t1 && tok < nvis[a];
+            const float sv = valid ? s[a] : -INFINITY;
+            const float mt = warp_max(sv);
+            const float mn = fmaxf(m[a], mt);
+            if (mn == -INFINITY) continue;  // nothing visible yet
+            const float corr = (m[a] == -INFINITY) ? 0.f : exp2f(m[a] - mn);
+            const float p = valid ? exp2f(sv - mn) : 0.f;
+            l[a] = l[a] * corr + warp_sum(p);
+            m[a] = mn;
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) o[a][c] *= corr;
+            for (int t2 = 0; t2 < kTT; ++t2) {
+                const float pt = __shfl_sync(0xffffffffu, p, t2);
+                const float *vr = vs + t2 * (d + 1);
+#pragma unroll
+                for (int c = 0; c < DPL; ++c) o[a][c] = fmaf(pt, vr[lane + 32 * c], o[a][c]);
+            }
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int qi = qb * kQB + warp * 4 + a;
+        if (qi >= D.Qu) continue;
+        const size_t row = ((size_t)unit * D.nsplit + sp) * D.Qu + qi;
+        if (lane == 0) part_ml[row] = make_float2(m[a], l[a]);
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) part_o[row * d + lane + 32 * c] = o[a][c];
+    }
+}
+
+// grid (Qu, units), block d. Merges the token splits of one query.
+__global__ void combine_kernel(LorekvDims D, const float2 *__restrict__ part_ml,
+                               const float *__restrict__ part_o, float *__restrict__ lse2,
+                               float *__restrict__ o, float *__restrict__ lse_out,
+                               float *__restrict__ o_out) {
+    const int qi = blockIdx.x, unit = blockIdx.y, k = threadIdx.x;
+    const size_t base = (size_t)unit * D.nsplit * D.Qu + qi;
+    float mx = -INFINITY;
+    for (int sp = 0; sp < D.nsplit; ++sp) mx = fmaxf(mx, part_ml[base + (size_t)sp * D.Qu].x);
+    float l = 0.f, acc = 0.f;
+    for (int sp = 0; sp < D.nsplit; ++sp) {
+        const float2 ml = part_ml[base + (size_t)sp * D.Qu];
+        if (ml.x == -INFINITY) continue;
+        const float sc = exp2f(ml.x - mx);
+        l = fmaf(ml.y, sc, l);
+        acc = fmaf(part_o[(base + (size_t)sp * D.Qu) * D.d + k], sc, acc);
+    }
+    const size_t row = (size_t)unit * D.Qu + qi;
+    const float ov = acc / l;
+    o[row * D.d + k] = ov;
+    if (o_out) o_out[row * D.d + k] = ov;
+    if (k == 0) {
+        const float v = mx + log2f(l);
+        lse2[row] = v;
+        if (lse_out) lse_out[row] = v * kLn2;
+    }
+}
+
+// grid (g, units), block 256. u_q = G_h o_q, c_q = o_q^T G_h o_q, weight_q; bf16 copies of u and
+// of the pre-scaled query for the tensor-core path.
+template <typename T>
+__global__ void __launch_bounds__(256) prep_u_kernel(LorekvDims D, const float *__restrict__ G,
+                                                     const float *__restrict__ omega,
+                                                     const T *__restrict__ QW,
+                                                     const T *__restrict__ QL,
+                                                     const float *__restrict__ o,
+                                                     float *__restrict__ u32,
+                                                     float *__restrict__ cq,
+                                                     float *__restrict__ wq,
+                                                     __nv_bfloat16 *__restrict__ u16,
+                                                     __nv_bfloat16 *__restrict__ q16) {
+    extern __shared__ float Gs[];  // [d][d]
+    const int j = blockIdx.x, unit = blockIdx.y;
+    const int d = D.d;
+    const int kh = unit % D.Hkv, l = (unit / D.Hkv) % D.L, s = unit / (D.Hkv * D.L);
+    const int h = kh * D.g + j;
+    const float *Gh = G + ((size_t)l * D.Hq + h) * d * d;
+    for (int idx = threadIdx.x; idx < d * d; idx += blockDim.x) Gs[idx] = Gh[idx];
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int r = warp; r < D.nq; r += blockDim.x >> 5) {
+        const int qi = j * D.nq + r;
+        const size_t row = (size_t)unit * D.Qu + qi;
+        const float *orow = o + row * d;
+        float cpart = 0.f;
+        for (int jj = lane; jj < d; jj += 32) {
+            float acc = 0.f;
+            for (int k = 0; k < d; ++k) acc = fmaf(Gs[k * d + jj], orow[k], acc);  // G symmetric
+            u32[row * d + jj] = acc;
+            if (u16) u16[row * d + jj] = __float2bfloat16_rn(acc);
+            cpart = fmaf(orow[jj], acc, cpart);
+        }
+        cpart = warp_sum(cpart);
+        if (q16) {
+            const T *qp = query_ptr(QW, QL, D, unit, qi);
+            for (int k = lane; k < d; k += 32) q16[row * d + k] = __float2bfloat16_rn(to_f(qp[k]));
+        }
+        if (lane == 0) {
+            cq[row] = cpart;
+            float wt;
+            if (r < D.w)
+                wt = 1.f / (float)(D.g * D.w);
+            else
+                wt = D.lambda_L * omega[(size_t)s * D.M + (r - D.w) / D.T] / (float)(D.g * D.T);
+            wq[row] = wt;
+        }
+    }
+}
+
+// grid (ceil(n/32), units), block 256. Lane = token of the tile, warp = a subset of the queries.
+template <typename T, int DPL>
+__global__ void __launch_bounds__(256) scores_simt_kernel(
+    const T *__restrict__ K, const T *__restrict__ V, const T *__restrict__ QW,
+    const T *__restrict__ QL, const float *__restrict__ Lf, LorekvDims D,
+    const float *__restrict__ lse2, const float *__restrict__ u32, const float *__restrict__ cq,
+    const float *__restrict__ wq, float *__restrict__ scores) {
+    constexpr int d = DPL * 32;
+    extern __shared__ float sm[];
+    float *ks = sm;                        // [kTT][d+1]
+    float *vs = ks + kTT * (d + 1);        // [kTT][d+1]
+    float *qs = vs + kTT * (d + 1);        // [nq][d] pre-scaled by log2e/sqrt(d)
+    float *us = qs + D.nq * d;             // [nq][d]
+    float *ls = us + D.nq * d;             // [d][d]
+    float *qc = ls + d * d;                // [3][nq]: lse2, c, weight
+    float *red = qc + 3 * D.nq;            // [8][32]
+    const int tile = blockIdx.x, unit = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i0 = tile * kTT;
+    const int tok = i0 + lane;
+    const bool scored = tok >= D.sink && tok < D.n - D.w;
+    float *Su = scores + (size_t)unit * D.n;
+    if (i0 + kTT <= D.sink || i0 >= D.n - D.w) {  // the whole tile is protected
+        if (threadIdx.x < kTT && tok < D.n) Su[tok] = 0.f;
+        return;
+    }
+    const T *Ku = K + (size_t)unit * D.n * d;
+    const T *Vu = V + (size_t)unit * D.n * d;
+    for (int idx = threadIdx.x; idx < kTT * d; idx += blockDim.x) {
+        const int tt = idx / d, k = idx % d;
+        const int t = i0 + tt;
+        ks[tt * (d + 1) + k] = (t < D.n) ? to_f(Ku[(size_t)t * d + k]) : 0.f;
+        vs[tt * (d + 1) + k] = (t < D.n) ? to_f(Vu[(size_t)t * d + k]) : 0.f;
+    }
+    const int kh = unit % D.Hkv, l = (unit / D.Hkv) % D.L;
+    const float qscale = kLog2e * rsqrtf((float)d);
+    float Sacc = 0.f;
+    for (int j = 0; j < D.g; ++j) {
+        __syncthreads();
+        const int h = kh * D.g + j;
+        for (int idx = threadIdx.x; idx < D.nq * d; idx += blockDim.x) {
+            const int r = idx / d, k = idx % d;
+            const int qi = j * D.nq + r;
+            qs[idx] = to_f(query_ptr(QW, QL, D, unit, qi)[k]) * qscale;
+            us[idx] = u32[((size_t)unit * D.Qu + qi) * d + k];
+        }
+        const float *Lh = Lf + ((size_t)l * D.Hq + h) * d * d;
+        for (int idx = threadIdx.x; idx < d * d; idx += blockDim.x) ls[idx] = Lh[idx];
+        for (int r = threadIdx.x; r < D.nq; r += blockDim.x) {
+            const size_t row = (size_t)unit * D.Qu + j * D.nq + r;
+            qc[r] = lse2[row];
+            qc[D.nq + r] = cq[row];
+            qc[2 * D.nq + r] = wq[row];
+        }
+        __syncthreads();
+        // ||L_h^T v||^2: warp w owns output dims jj = w, w+8, ...
+        const float *vr = vs + lane * (d + 1);
+        const float *kr = ks + lane * (d + 1);
+        float nvp = 0.f;
+        for (int jj = warp; jj < d; jj += 8) {
+            float y = 0.f;
+            for (int k = jj; k < d; ++k) y = fmaf(ls[k * d + jj], vr[k], y);  // L lower triangular
+            nvp = fmaf(y, y, nvp);
+        }
+        red[warp * 32 + lane] = nvp;
+        __syncthreads();
+        float nv = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) nv += red[w * 32 + lane];
+        for (int r = warp; r < D.nq; r += 8) {
+            const float *qr = qs + r * d;
+            const float *ur = us + r * d;
+            float s = 0.f, vu = 0.f;
+            for (int k = 0; k < d; ++k) {
+                s = fmaf(qr[k], kr[k], s);
+                vu = fmaf(ur[k], vr[k], vu);
+            }
+            const float a = exp2f(s - qc[r]);
+            const float x = fmaxf(fmaf(-2.f, vu, nv + qc[D.nq + r]), 0.f);
+            const float e = a / (1.f - a + D.eps) * sqrtf(x);
+            Sacc = fmaf(qc[2 * D.nq + r], e, Sacc);
+        }
+    }
+    __syncthreads();
+    red[warp * 32 + lane] = Sacc;
+    __syncthreads();
+    if (threadIdx.x < kTT && tok < D.n) {
+        float S = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) S += red[w * 32 + threadIdx.x];
+        Su[tok] = scored ? S : 0.f;
+    }
+}
+
+template <typename T>
+cudaError_t attn_dispatch(const LorekvDims &D, const void *K, const void *V, const void *QW,
+                          const void *QL, float2 *ml, float *po, cudaStream_t st) {
+    const dim3 grid((D.Qu + kQB - 1) / kQB, D.nsplit, D.units);
+    const size_t smem = sizeof(float) * (kQB * D.d + 2 * kTT * (D.d + 1));
+#define KVE_ATTN_CASE(DPL)                                                                     \
+    case DPL: {                                                                                \
+        auto kern = attn_partial_kernel<T, DPL>;                                               \
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);    \
+        kern<<<grid, 256, smem, st>>>((const T *)K, (const T *)V, (const T *)QW, (const T *)QL, \
+                                      D, ml, po);                                              \
+        break;                                                                                 \
+    }
+    switch (D.d / 32) {
+        KVE_ATTN_CASE(1)
+        KVE_ATTN_CASE(2)
+        KVE_ATTN_CASE(4)
+        default: return cudaErrorInvalidValue;
+    }
+#undef KVE_ATTN_CASE
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t scores_dispatch(const LorekvDims &D, const void *K, const void *V, const void *QW,
+                            const void *QL, const float *Lf, const float *lse2, const float *u32,
+                            const float *cq, const float *wq, float *scores, cudaStream_t st) {
+    const dim3 grid((D.n + kTT - 1) / kTT, D.units);
+    const size_t smem = sizeof(float) * (2 * kTT * (D.d + 1) + 2 * D.nq * D.d + D.d * D.d +
+                                         3 * D.nq + 8 * 32);
+#define KVE_SC_CASE(DPL)                                                                        \
+    case DPL: {                                                                                 \
+        auto kern = scores_simt_kernel<T, DPL>;                                                 \
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);     \
+        kern<<<grid, 256, smem, st>>>((const T *)K, (const T *)V, (const T *)QW, (const T *)QL, \
+                                      Lf, D, lse2, u32, cq, wq, scores);                        \
+        break;                                                                                  \
+    }
+    switch (D.d / 32) {
+        KVE_SC_CASE(1)
+        KVE_SC_CASE(2)
+        KVE_SC_CASE(4)
+        default: return cudaErrorInvalidValue;
+    }
+#undef KVE_SC_CASE
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention_simt(const LorekvDims &D, const void *K, const void *V,
+                                  const void *QW, const void *QL, void *ws,
+                                  const LorekvWorkspace &W, cudaStream_t st) {
+    char *b = static_cast<char *>(ws);
+    float2 *ml = reinterpret_cast<float2 *>(b + W.part_ml);
+    float *po = reinterpret_cast<float *>(b + W.part_o);
+    if (D.dtype == KVE_F32) return attn_dispatch<float>(D, K, V, QW, QL, ml, po, st);
+    return attn_dispatch<__nv_bfloat16>(D, K, V, QW, QL, ml, po, st);
+}
+
+cudaError_t launch_combine(const LorekvDims &D, void *ws, const LorekvWorkspace &W,
+                           float *lse_out, float *o_out, cudaStream_t st) {
+    char *b = static_cast<char *>(ws);
+    combine_kernel<<<dim3(D.Qu, D.units), D.d, 0, st>>>(
+        D, reinterpret_cast<const float2 *>(b + W.part_ml),
+        reinterpret_cast<const float *>(b + W.part_o), reinterpret_cast<float *>(b + W.lse2),
+        reinterpret_cast<float *>(b + W.o), lse_out, o_out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prep_u(const LorekvDims &D, const float *G, const float *omega, void *ws,
+                          const LorekvWorkspace &W, cudaStream_t st, const void *QW,
+                          const void *QL, bool want_bf16);
+
+cudaError_t launch_prep_u(const LorekvDims &D, const float *G, const float *omega, void *ws,
+                          const LorekvWorkspace &W, cudaStream_t st) {
+    return launch_prep_u(D, G, omega, ws, W, st, nullptr, nullptr, false);
+}
+
+cudaError_t launch_prep_u(const LorekvDims &D, const float *G, const float *omega, void *ws,
+                          const LorekvWorkspace &W, cudaStream_t st, const void *QW,
+                          const void *QL, bool want_bf16) {
+    char *b = static_cast<char *>(ws);
+    const size_t smem = sizeof(float) * D.d * D.d;
+    __nv_bfloat16 *u16 = want_bf16 ? reinterpret_cast<__nv_bfloat16 *>(b + W.u16) : nullptr;
+    __nv_bfloat16 *q16 = want_bf16 ? reinterpret_cast<__nv_bfloat16 *>(b + W.q16) : nullptr;
+    const float *o = reinterpret_cast<const float *>(b + W.o);
+    float *u32 = reinterpret_cast<float *>(b + W.u32);
+    float *cq = reinterpret_cast<float *>(b + W.cq);
+    float *wq = reinterpret_cast<float *>(b + W.wq);
+    if (D.dtype == KVE_F32) {
+        auto kern = prep_u_kernel<float>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        kern<<<dim3(D.g, D.units), 256, smem, st>>>(D, G, omega, (const float *)QW,
+                                                    (const float *)QL, o, u32, cq, wq, u16, q16);
+    } else {
+        auto kern = prep_u_kernel<__nv_bfloat16>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        kern<<<dim3(D.g, D.units), 256, smem, st>>>(D, G, omega, (const __nv_bfloat16 *)QW,
+                                                    (const __nv_bfloat16 *)QL, o, u32, cq, wq,
+                                                    u16, q16);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scores_simt(const LorekvDims &D, const void *K, const void *V,
+                               const void *QW, const void *QL, const float *Lf, void *ws,
+                               const LorekvWorkspace &W, float *scores, cudaStream_t st) {
+    char *b = static_cast<char *>(ws);
+    const float *lse2 = reinterpret_cast<const float *>(b + W.lse2);
+    const float *u32 = reinterpret_cast<const float *>(b + W.u32);
+    const float *cq = reinterpret_cast<const float *>(b + W.cq);
+    const float *wq = reinterpret_cast<const float *>(b + W.wq);
+    if (D.dtype == KVE_F32)
+        return scores_dispatch<float>(D, K, V, QW, QL, Lf, lse2, u32, cq, wq, scores, st);
+    return scores_dispatch<__nv_bfloat16>(D, K, V, QW, QL, Lf, lse2, u32, cq, wq, scores, st);
+}
+
+}  // namespace kve

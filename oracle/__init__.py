@@ -197,32 +197,45 @@ def compact(X, kept):
 def lorekv_config_units(cfg, inputs, units, *, want_kept=True):
     """Oracle outputs for selected units of a full config.
 
-    ``units`` is a list of (s, l, kh). Returns {unit: {"S", "kept", "omega"}} plus "omega" per
-    sequence. omega uses every layer and head of the sequence (Eq. 10 with the disagreement
-    term), the Cholesky factors come from the layer's W_O."""
+    ``units`` is a list of (s, l, kh). Returns {unit: {"S", "kept", "omega"}}. omega uses every
+    layer and head of the sequence (Eq. 10 with the disagreement term); the Cholesky factors come
+    from the layer's W_O. The units are scored in parallel (OpenMP over units)."""
     from kv_cache_eviction_02_gb300.synth import unit_slice  # input slicing only
 
     g, d = cfg.g, cfg.d
     omegas = {}
-    res = {}
-    for (s, l, kh) in units:
+    for (s, _, _) in units:
         if s not in omegas:
             omegas[s] = reliability(inputs["logits"][s], inputs["sampled"][s],
                                     inputs["Q_look"][s], cfg.M, cfg.T, cfg.beta, cfg.gamma,
                                     cfg.lambda_D)["omega"]
+    Ks, Vs, QWs, QLs, Lfs, oms = [], [], [], [], [], []
+    chol = {}
+    for (s, l, kh) in units:
         u = unit_slice(cfg, inputs, s, l, kh)
         Lf = np.zeros((g, d, d))
         for j in range(g):
-            _, Lj, st = gram_cholesky(u["W_O"], d, kh * g + j)
-            if st != OK:
-                raise ValueError("W_O^T W_O not positive definite")
-            Lf[j] = Lj
-        S = lorekv_unit(u["K"], u["V"], u["Q_W"], u["Q_look"], Lf, omegas[s], M=cfg.M, T=cfg.T,
-                        sink=cfg.sink, lambda_L=cfg.lambda_L, eps=cfg.eps,
-                        window_causal=cfg.window_causal)
-        r = {"S": S, "omega": omegas[s]}
+            key = (l, kh * g + j)
+            if key not in chol:
+                _, Lj, st = gram_cholesky(u["W_O"], d, kh * g + j)
+                if st != OK:
+                    raise ValueError("W_O^T W_O not positive definite")
+                chol[key] = Lj
+            Lf[j] = chol[key]
+        Ks.append(_d(u["K"]))
+        Vs.append(_d(u["V"]))
+        QWs.append(_d(u["Q_W"]))
+        QLs.append(_d(u["Q_look"]))
+        Lfs.append(Lf)
+        oms.append(omegas[s])
+    S_all = lorekv_units(np.stack(Ks), np.stack(Vs), np.stack(QWs), np.stack(QLs),
+                         np.stack(Lfs), np.stack(oms), M=cfg.M, T=cfg.T, sink=cfg.sink,
+                         lambda_L=cfg.lambda_L, eps=cfg.eps, window_causal=cfg.window_causal)
+    res = {}
+    for i, (s, l, kh) in enumerate(units):
+        r = {"S": S_all[i], "omega": omegas[s]}
         if want_kept:
-            r["kept"] = select(S, sink=cfg.sink, w=cfg.w, chunk=cfg.chunk, B=cfg.B)
+            r["kept"] = select(S_all[i], sink=cfg.sink, w=cfg.w, chunk=cfg.chunk, B=cfg.B)
         res[(s, l, kh)] = r
     return res
 
@@ -278,8 +291,17 @@ class H2OUnit:
         self.t = P
         self.pos = np.arange(P, dtype=np.int32)
         self.K, self.V, self.acc = K.copy(), V.copy(), acc.copy()
+        self.prefill_acc = acc.copy()
         self.queries = P
         self._evict_now()
+
+    def adopt_prefill(self, keep_positions, K, V):
+        """Teacher forcing after the prefill compression: retain exactly ``keep_positions`` of the
+        prompt (K, V are the prompt rows) with their prefill accumulated scores."""
+        keep = np.asarray(sorted(keep_positions), dtype=np.int32)
+        K, V = _d(K), _d(V)
+        self.pos, self.K, self.V = keep, K[keep], V[keep]
+        self.acc = self.prefill_acc[keep].copy()
 
     def _evict_now(self):
         ev = h2o_evict(self.pos, self.acc, self.t, self.frac)
@@ -288,8 +310,11 @@ class H2OUnit:
         self.pos, self.K, self.V, self.acc = self.pos[keep], self.K[keep], self.V[keep], self.acc[keep]
         return evicted
 
-    def step(self, q, k, v):
-        """append -> attend (the new token attends to itself) -> accumulate -> evict."""
+    def step(self, q, k, v, evict: bool = True):
+        """append -> attend (the new token attends to itself) -> accumulate -> evict.
+
+        With evict=False the step stops before the eviction (teacher forcing: the caller then
+        adopts a retained set with :meth:`adopt`)."""
         q, k, v = _d(q), _d(k), _d(v)
         self.pos = np.append(self.pos, np.int32(self.t))
         self.K = np.vstack([self.K, k[None]])
@@ -301,7 +326,7 @@ class H2OUnit:
         self.full_acc[self.pos] += p
         self.queries += 1
         pre = {"pos": self.pos.copy(), "acc": self.acc.copy()}
-        evicted = self._evict_now()
+        evicted = self._evict_now() if evict else []
         return out, evicted, pre
 
     def adopt(self, keep_positions):

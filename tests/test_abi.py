@@ -1,0 +1,124 @@
+"""C-ABI checks that need no GPU: the library builds, loads and exports every function that
+include/kvevict.h declares; argument validation and the host-side fault hook work before any
+CUDA call is made."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def api():
+    from kv_cache_eviction_02_gb300 import _build, api as a
+    _build.build()
+    a.lib()
+    return a
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "kvevict.h")) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w]*\s*\**\s*([a-z_][a-z0-9_]*)\s*\(", src,
+                       flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_exported_api(api):
+    names = _declared_functions()
+    assert "lorekv_score" in names and "h2o_decode_step" in names
+    assert set(names) == set(api.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(api):
+    out = subprocess.run(["nm", "-D", "--defined-only", api.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    for name in _declared_functions():
+        assert name in exported, name
+        assert getattr(api.lib(), name) is not None
+
+
+def _pb(api, **kw):
+    base = dict(n_seq=1, n_layers=2, n_q_heads=8, n_kv_heads=2, d_head=128, d_model=256,
+                n_tokens=1000, vocab=500, dtype=api.KVE_BF16, budget_B=128)
+    base.update(kw)
+    return api.LorekvProblem(**base)
+
+
+def test_workspace_size_and_capacity(api):
+    pb = _pb(api)
+    ws = api.lorekv_workspace_size(pb)
+    assert ws > 0 and ws % 256 == 0
+    assert api.lorekv_kept_capacity(pb) == 4 + 128 + 32
+    assert api.lorekv_kept_capacity(_pb(api, n_tokens=36 + 128)) == 36 + 128   # all kept
+    # more tokens -> more workspace
+    assert api.lorekv_workspace_size(_pb(api, n_tokens=2000)) > ws
+
+
+@pytest.mark.parametrize("bad", [
+    dict(n_tokens=1001),            # (n - sink - w) not a multiple of chunk
+    dict(budget_B=130),             # B not a multiple of chunk
+    dict(n_q_heads=7),              # not a multiple of n_kv_heads
+    dict(d_head=96),                # unsupported head size
+    dict(n_tokens=20),              # fewer tokens than sink + w
+    dict(M=40),                     # too many trajectories
+])
+def test_invalid_shapes_are_rejected_without_a_gpu(api, bad):
+    pb = _pb(api, **bad)
+    assert api.lorekv_workspace_size(pb) == 0
+    with pytest.raises(api.KveError) as e:
+        api.lorekv_kept_capacity(pb)
+    assert e.value.status == api.KVE_EINVAL
+
+
+def test_score_rejects_bad_arguments_before_touching_the_gpu(api):
+    L = api.lib()
+    pb = _pb(api)
+    sh, pr = pb.shape(), pb.params()
+    fake = ctypes.c_void_p(256)
+    # missing workspace
+    st = L.lorekv_score(ctypes.byref(sh), ctypes.byref(pr), fake, fake, fake, fake, fake, fake,
+                        fake, fake, fake, fake, None, 0, None)
+    assert st == api.KVE_EWORKSPACE
+    assert "workspace" in L.kve_last_error().decode()
+    # wrong dtype
+    sh.dtype = api.KVE_F16
+    st = L.lorekv_score(ctypes.byref(sh), ctypes.byref(pr), fake, fake, fake, fake, fake, fake,
+                        fake, fake, fake, fake, fake, 1 << 40, None)
+    assert st == api.KVE_EDTYPE
+    # null tensors
+    sh.dtype = api.KVE_BF16
+    st = L.lorekv_score(ctypes.byref(sh), ctypes.byref(pr), None, fake, fake, fake, fake, fake,
+                        fake, fake, fake, fake, fake, 1 << 40, None)
+    assert st == api.KVE_EINVAL
+
+
+def test_h2o_create_validates_arguments(api):
+    L = api.lib()
+    h = ctypes.c_void_p()
+    assert L.h2o_state_create(ctypes.byref(h), 1, 1, 2, 96, 100, 0.2, api.KVE_F16) == api.KVE_EINVAL
+    assert L.h2o_state_create(ctypes.byref(h), 1, 1, 2, 64, 100, 1.5, api.KVE_F16) == api.KVE_EINVAL
+    assert L.h2o_state_create(ctypes.byref(h), 1, 1, 2, 64, 100, 0.2, api.KVE_F32) == api.KVE_EDTYPE
+    assert L.h2o_state_create(ctypes.byref(h), 1, 1, 2, 64, 100000, 0.2, api.KVE_F16) == api.KVE_EINVAL
+    assert not h.value
+    assert L.h2o_decode_step(None, None, None, None, None, None) == api.KVE_EINVAL
+
+
+def test_injected_failure_is_reported_then_cleared(api):
+    pb = _pb(api)
+    api.kve_inject_failure(api.KVE_ECUDA, 2)
+    for _ in range(2):
+        with pytest.raises(api.KveError) as e:
+            api.lorekv_prepare_wo(pb, 1, 1, 1, 0)
+        assert e.value.status == api.KVE_ECUDA
+        assert "injected" in str(e.value)
+    # the hook is used up: the next call validates normally (null pointers -> EINVAL)
+    with pytest.raises(api.KveError) as e:
+        api.lorekv_prepare_wo(pb, None, None, None, 0)
+    assert e.value.status == api.KVE_EINVAL
+    api.kve_inject_failure(0, 0)

@@ -1,0 +1,184 @@
+"""GPU parity of the LORE-KV eviction pass against the fp64 oracle (called through the C-ABI).
+
+Small configurations compare every unit element by element; they span several token tiles with a
+ragged tail, GQA groups of 1, 4 and 5, both coefficient presets, causal and non-causal window
+queries, and the all-kept edge case. The full-size workloads (Mistral-7B-, Llama-3.1-8B- and
+Qwen2.5-14B-shaped) run in the benchmark's launch configuration and compare sampled units with
+the oracle, plus properties checked on every unit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kv_cache_eviction_02_gb300 import api, synth
+from parity import (OMEGA_RTOL, SCORE_RTOL, assert_kept_matches,
+                    assert_kept_valid_for_own_scores, assert_scores_close)
+
+pytestmark = pytest.mark.gpu
+
+CFG = synth.LorekvConfig
+SMALL = {
+    "tiny": synth.LOREKV_CONFIGS["tiny"],
+    "bf16_gqa4_D": CFG("bf16_gqa4_D", "bf16", S=2, L=2, Hq=8, Hkv=2, d=128, d_model=256, n=1000,
+                       vocab=5000, beta=1.0, gamma=1.0, lambda_D=0.3),
+    "bf16_gqa5_E": CFG("bf16_gqa5_E", "bf16", S=1, L=1, Hq=10, Hkv=2, d=128, d_model=640,
+                       n=2084, vocab=3000, B=512, outlier_frac=0.01),
+    "f32_ragged_d32": CFG("f32_ragged_d32", "f32", S=1, L=2, Hq=4, Hkv=2, d=32, d_model=64,
+                          n=300, vocab=300, B=64, keys="normal"),
+    "bf16_noncausal": CFG("bf16_noncausal", "bf16", S=1, L=1, Hq=4, Hkv=1, d=128, d_model=512,
+                          n=516, vocab=1000, window_causal=0, M=2, T=4, w=16),
+    "f32_all_kept": CFG("f32_all_kept", "f32", S=1, L=1, Hq=2, Hkv=1, d=64, d_model=64,
+                        n=36 + 96, vocab=64, keys="normal"),
+}
+
+
+def _dev():
+    return torch.device("cuda:0")
+
+
+def _prepare(cfg, g):
+    pb = api.LorekvProblem.from_config(cfg)
+    Lf = torch.empty(cfg.L, cfg.Hq, cfg.d, cfg.d, device=_dev())
+    G = torch.empty_like(Lf)
+    api.lorekv_prepare_wo(pb, g["W_O"], Lf, G)
+    return pb, Lf, G
+
+
+def _all_units(cfg):
+    return [(s, l, kh) for s in range(cfg.S) for l in range(cfg.L) for kh in range(cfg.Hkv)]
+
+
+def _unit_index(cfg, s, l, kh):
+    return (s * cfg.L + l) * cfg.Hkv + kh
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_prepare_wo_matches_oracle(name):
+    cfg = SMALL[name]
+    inp = synth.lorekv_inputs(cfg, "cpu")
+    g = {k: v.to(_dev()) for k, v in inp.items()}
+    _, Lf, G = _prepare(cfg, g)
+    Lc, Gc = Lf.double().cpu().numpy(), G.double().cpu().numpy()
+    for l in range(cfg.L):
+        for h in range(cfg.Hq):
+            Gr, Lr, st = oracle.gram_cholesky(inp["W_O"][l], cfg.d, h)
+            assert st == oracle.OK
+            assert np.allclose(Gc[l, h], Gr, rtol=1e-6, atol=1e-7 * np.abs(Gr).max())
+            assert np.allclose(Lc[l, h], Lr, rtol=1e-6, atol=1e-7 * np.abs(Lr).max())
+
+
+def test_prepare_wo_reports_not_positive_definite():
+    # d_model < d_head: every Gram matrix is rank deficient
+    pb = api.LorekvProblem(1, 1, 2, 1, 64, 16, 100, 10, api.KVE_F32)
+    W = torch.randn(1, 16, 128, device=_dev())
+    Lf = torch.empty(1, 2, 64, 64, device=_dev())
+    with pytest.raises(api.KveError) as e:
+        api.lorekv_prepare_wo(pb, W, Lf, torch.empty_like(Lf))
+    assert e.value.status == api.KVE_ENOTPD
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_attention_statistics_match_oracle(name):
+    cfg = SMALL[name]
+    inp = synth.lorekv_inputs(cfg, "cpu")
+    g = {k: v.to(_dev()) for k, v in inp.items()}
+    pb = api.LorekvProblem.from_config(cfg)
+    ws = torch.empty(api.lorekv_workspace_size(pb), dtype=torch.uint8, device=_dev())
+    Qu = cfg.g * cfg.queries_per_head
+    lse = torch.empty(cfg.units, Qu, device=_dev())
+    o = torch.empty(cfg.units, Qu, cfg.d, device=_dev())
+    api.lorekv_attention_stats(pb, g["K"], g["V"], g["Q_W"], g["Q_look"], lse, o, ws)
+    api.kve_check_device()
+    lse, o = lse.double().cpu().numpy(), o.double().cpu().numpy()
+    tol = 1e-5 if cfg.dtype == "f32" else 2e-3
+    for (s, l, kh) in _all_units(cfg):
+        u = synth.unit_slice(cfg, inp, s, l, kh)
+        eye = np.stack([np.eye(cfg.d)] * cfg.g)
+        r = oracle.lorekv_unit(u["K"], u["V"], u["Q_W"], u["Q_look"], eye, np.ones(cfg.M) / cfg.M,
+                               M=cfg.M, T=cfg.T, sink=cfg.sink, lambda_L=1.0, eps=cfg.eps,
+                               window_causal=cfg.window_causal, want=("lse", "o"))
+        ui = _unit_index(cfg, s, l, kh)
+        lse_ref = r["lse"].reshape(-1)
+        o_ref = r["o"].reshape(-1, cfg.d)
+        assert np.allclose(lse[ui], lse_ref, rtol=0, atol=tol * np.maximum(1, np.abs(lse_ref)).max())
+        err = np.linalg.norm(o[ui] - o_ref, axis=1)
+        assert np.all(err <= tol * np.linalg.norm(o_ref, axis=1) + 1e-6), (name, err.max())
+
+
+def _run_pass(cfg, g):
+    pb, Lf, G = _prepare(cfg, g)
+    run = api.LorekvPass(pb, _dev())
+    run.run(g, Lf, G)
+    api.kve_check_device()
+    return run
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_eviction_pass_matches_oracle(name):
+    cfg = SMALL[name]
+    inp = synth.lorekv_inputs(cfg, "cpu")
+    g = {k: v.to(_dev()) for k, v in inp.items()}
+    run = _run_pass(cfg, g)
+    ref = oracle.lorekv_config_units(cfg, inp, _all_units(cfg))
+    S = run.scores.double().cpu().numpy()
+    om = run.omega.double().cpu().numpy()
+    kept = run.kept_idx.cpu().numpy()
+    klen = run.kept_len.cpu().numpy()
+    for (s, l, kh), r in ref.items():
+        ui = _unit_index(cfg, s, l, kh)
+        assert np.allclose(om[s], r["omega"], rtol=OMEGA_RTOL, atol=0), (name, s)
+        assert_scores_close(S[ui], r["S"], cfg.dtype, f"{name} unit {ui}")
+        assert klen[ui] == run.cap
+        assert_kept_matches(kept[ui, :klen[ui]], r["S"], sink=cfg.sink, w=cfg.w, chunk=cfg.chunk,
+                            B=cfg.B, rtol=SCORE_RTOL[cfg.dtype], what=f"{name} unit {ui}")
+    # compaction is bit-exact given the GPU's own index set
+    Kf = g["K"].reshape(cfg.units, cfg.n, cfg.d)
+    Vf = g["V"].reshape(cfg.units, cfg.n, cfg.d)
+    idx = run.kept_idx.long()
+    assert torch.equal(run.K_out, torch.gather(Kf, 1, idx[..., None].expand(-1, -1, cfg.d)))
+    assert torch.equal(run.V_out, torch.gather(Vf, 1, idx[..., None].expand(-1, -1, cfg.d)))
+
+
+def test_scores_are_deterministic():
+    cfg = SMALL["bf16_gqa4_D"]
+    g = {k: v.to(_dev()) for k, v in synth.lorekv_inputs(cfg, "cpu").items()}
+    a = _run_pass(cfg, g)
+    S1, k1 = a.scores.clone(), a.kept_idx.clone()
+    b = _run_pass(cfg, g)
+    assert torch.equal(S1, b.scores) and torch.equal(k1, b.kept_idx)
+
+
+FULL = ["mistral", "llama", "qwen"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload_sampled_units(name):
+    cfg = synth.LOREKV_CONFIGS[name]
+    torch.cuda.empty_cache()
+    g = synth.lorekv_inputs(cfg, _dev())
+    run = _run_pass(cfg, g)
+    S = run.scores
+    # every unit: protected tokens score 0, scores finite and non-negative, kept sets valid
+    assert torch.isfinite(S).all() and (S >= 0).all()
+    assert (S[:, :cfg.sink] == 0).all() and (S[:, cfg.n - cfg.w:] == 0).all()
+    kept = run.kept_idx.cpu().numpy()
+    Sc = S.cpu().numpy()
+    for ui in range(cfg.units):
+        assert_kept_valid_for_own_scores(kept[ui], Sc[ui], sink=cfg.sink, w=cfg.w,
+                                         chunk=cfg.chunk, B=cfg.B, what=f"{name} unit {ui}")
+    # sampled units against the oracle
+    units = [(0, 0, 0), (cfg.S - 1, cfg.L // 2, cfg.Hkv - 1), (cfg.S - 1, cfg.L - 1, cfg.Hkv // 2)]
+    ref = oracle.lorekv_config_units(cfg, g, units)
+    om = run.omega.double().cpu().numpy()
+    for (s, l, kh), r in ref.items():
+        ui = _unit_index(cfg, s, l, kh)
+        assert np.allclose(om[s], r["omega"], rtol=OMEGA_RTOL, atol=0)
+        assert_scores_close(Sc[ui].astype(np.float64), r["S"], cfg.dtype, f"{name} unit {ui}")
+        assert_kept_matches(kept[ui], r["S"], sink=cfg.sink, w=cfg.w, chunk=cfg.chunk, B=cfg.B,
+                            rtol=SCORE_RTOL[cfg.dtype], what=f"{name} unit {ui}")
+    idx = run.kept_idx.long()
+    Kf = g["K"].reshape(cfg.units, cfg.n, cfg.d)
+    assert torch.equal(run.K_out, torch.gather(Kf, 1, idx[..., None].expand(-1, -1, cfg.d)))
+    del g, run
+    torch.cuda.empty_cache()
