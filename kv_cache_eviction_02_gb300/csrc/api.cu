@@ -17,7 +17,6 @@ cudaError_t launch_prep_u(const LorekvDims &D, const float *G, const float *omeg
                           const LorekvWorkspace &W, cudaStream_t st, const void *QW,
                           const void *QL, bool want_bf16);
 size_t h2o_prefill_smem(int d, int P, int dtype);
-bool tc_supported(const LorekvDims &D);
 cudaError_t launch_scores_tc(const LorekvDims &D, const void *K, const void *V, const float *Lf,
                              void *ws, const LorekvWorkspace &W, float *scores,
                              unsigned *err_word, cudaStream_t st);
@@ -171,6 +170,7 @@ bool lorekv_dims(const KveShape *sh, const KveLorekvParams *p, LorekvDims *D, co
     split_len = (split_len + 127) / 128 * 128;
     D->split_len = (int)split_len;
     D->nsplit = (int)((D->n + split_len - 1) / split_len);
+    if (tc_supported(*D)) tc_plan(D);
     long rs = (304 + (long)D->S * D->MT - 1) / ((long)D->S * D->MT);
     const long rs_max = (D->vocab + 2047) / 2048;
     if (rs > rs_max) rs = rs_max;
@@ -200,6 +200,7 @@ LorekvWorkspace lorekv_ws_layout(const LorekvDims &D) {
     W.q16 = take(bf ? 2 * uq * D.d : 0);
     W.lt16 = take(bf ? 2 * (size_t)D.L * D.Hq * D.d * D.d : 0);
     W.part_s = take(bf ? sizeof(float) * (size_t)D.units * D.g * D.n : 0);
+    W.qconst = take(bf ? sizeof(float4) * uq : 0);
     W.rel_part = take(sizeof(float4) * (size_t)D.S * D.MT * D.rel_splits);
     W.cosm = take(sizeof(float) * (size_t)D.S * D.L * D.Hq * D.M * D.M);
     W.total = off;
@@ -418,7 +419,7 @@ int lorekv_score(const KveShape *shape, const KveLorekvParams *params, const voi
         e = launch_prep_u(D, G, omega_out, workspace, W, st, Q_W, Q_look, tc);
     }
     if (e == cudaSuccess) {
-        ProfScope ps("scores", 1, st);
+        ProfScope ps("scores", tc ? 4 : 1, st);
         if (tc)
             e = launch_scores_tc(D, K, V, L, workspace, W, scores_out, device_error_word(), st);
         else

@@ -65,12 +65,15 @@ struct LorekvWorkspace {
     size_t u16, lt16;          // bf16 operands: U [units][Qu][d]; L^T packed [L][Hq][d][d]
     size_t q16;                // bf16 queries packed [units][Qu][d]
     size_t part_s;             // per-query-head partial scores [units][g][n] f32
+    size_t qconst;             // per-query {-lse2, c, weight, 0} [units][Qu] float4
     size_t rel_part;           // reliability partials [S][MT][rel_splits] float4
     size_t cosm;               // cosine sums [S][L*Hq][M][M] f32
     size_t total;
 };
 
 bool lorekv_dims(const KveShape *sh, const KveLorekvParams *p, LorekvDims *D, const char **why);
+bool tc_supported(const LorekvDims &D);  // tensor-core kernels cover this shape
+void tc_plan(LorekvDims *D);             // token splits of the tensor-core attention pass
 LorekvWorkspace lorekv_ws_layout(const LorekvDims &D);
 
 // ---- launchers (each returns cudaGetLastError() of its launches) -------------------------------

@@ -379,7 +379,7 @@ cudaError_t launch_prep_u(const LorekvDims &D, const float *G, const float *omeg
     char *b = static_cast<char *>(ws);
     const size_t smem = sizeof(float) * D.d * D.d;
     __nv_bfloat16 *u16 = want_bf16 ? reinterpret_cast<__nv_bfloat16 *>(b + W.u16) : nullptr;
-    __nv_bfloat16 *q16 = want_bf16 ? reinterpret_cast<__nv_bfloat16 *>(b + W.q16) : nullptr;
+    __nv_bfloat16 *q16 = nullptr;  // the tensor-core path packs the queries itself
     const float *o = reinterpret_cast<const float *>(b + W.o);
     float *u32 = reinterpret_cast<float *>(b + W.u32);
     float *cq = reinterpret_cast<float *>(b + W.cq);

@@ -1,24 +1,670 @@
-// Tensor-core (tcgen05) kernels of the LORE-KV scoring pass. Not enabled yet: tc_supported()
-// reports false and the CUDA-core kernels run for every shape.
-#include "kve_internal.cuh"
+// LORE-KV scoring on the 5th-generation tensor cores (tcgen05, sm_103a), bf16 inputs, fp32 TMEM
+// accumulators, TMA-staged 128-byte-swizzled operand tiles.
+//
+// Attention statistics (LORE-KV page, Method: a_{q,i} = softmax_i(q.k_i/sqrt d), o_q =
+// sum_i a_{q,i} v_i), one CTA per (unit, 256 queries, token split):
+//   S_t = Q_t K^T (M = 128 queries, N = 128 tokens) for the two query tiles t = 0, 1 of the CTA,
+//   an online softmax per query row in a 4-warp group per tile (rows = TMEM lanes), P written as
+//   bf16 into shared memory, O_t += P_t V (V as the MN-major B operand). O stays in TMEM; it is
+//   rescaled only when a row's running maximum grows by more than 2^8, so the common step needs no
+//   TMEM round trip. The MMA issuer ping-pongs the two tiles so the tensor pipe computes one tile's
+//   S while the other tile's softmax runs.
+//
+// Projected deletion scores (Eqs. 5-7), one CTA per (unit, query head, token range), tokens on M:
+//   S^T = K Q_h^T, X = V U_h^T (u_q = G_h o_q) and Y = V L_h (||L_h^T v||^2 = ||row of Y||^2,
+//   the upper-right 64x64 block of L_h^T is zero and skipped) for 128 tokens per tile, into one of
+//   two 256-column TMEM buffers; two 4-warp epilogue groups take alternate tiles and evaluate
+//   e = a/(1-a+eps) sqrt(||L^T v||^2 - 2 v.u + c) with a = exp2(s log2e/sqrt(d) - lse2) for the
+//   head's 64 queries, weighted by psi = mean per set. Per-head partial sums go to the workspace and
+//   a small kernel adds the g heads in a fixed order.
+#include <cudaTypedefs.h>
+
+#include "tc_common.cuh"
 
 namespace kve {
 
-bool tc_supported(const LorekvDims &) { return false; }
+constexpr int kSms = 152;  // GB300
 
-cudaError_t launch_pack_queries(const LorekvDims &, const void *, const void *, void *,
-                                const LorekvWorkspace &, cudaStream_t) {
-    return cudaErrorNotSupported;
+bool tc_supported(const LorekvDims &D) {
+    return D.dtype == KVE_BF16 && D.d == 128 && D.nq >= 1 && D.nq <= 64;
 }
 
-cudaError_t launch_attention_tc(const LorekvDims &, const void *, const void *, void *,
-                                const LorekvWorkspace &, unsigned *, cudaStream_t) {
-    return cudaErrorNotSupported;
+// ---- host: tensor maps ---------------------------------------------------------------------------
+bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                       uint32_t box_inner, uint32_t box_rows) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !p)
+            return false;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    if (reinterpret_cast<uintptr_t>(base) % 16 != 0) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t launch_scores_tc(const LorekvDims &, const void *, const void *, const float *,
-                             void *, const LorekvWorkspace &, float *, unsigned *, cudaStream_t) {
-    return cudaErrorNotSupported;
+// Token splits (attention) or ranges (scores) that spread `items * parts` CTAs evenly over the
+// SMs: minimise ceil(items*parts / SMs) * ceil(tiles / parts).
+static int balance_parts(long items, long tiles, int max_parts) {
+    int best = 1;
+    long best_cost = -1;
+    for (int p = 1; p <= max_parts && p <= tiles; ++p) {
+        const long waves = (items * p + kSms - 1) / kSms;
+        const long per = (tiles + p - 1) / p;
+        const long cost = waves * per;
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = p;
+        }
+    }
+    return best;
+}
+
+void tc_plan(LorekvDims *D) {
+    const long ntiles = (D->n + 127) / 128;
+    const long nqp = (D->Qu + 255) / 256;
+    const int ns = balance_parts((long)D->units * nqp, ntiles, 64);
+    const long per = (ntiles + ns - 1) / ns;
+    D->split_len = (int)(per * 128);
+    D->nsplit = (int)((D->n + D->split_len - 1) / D->split_len);
+}
+
+namespace {
+
+// ---- small packing kernels -------------------------------------------------------------------------
+// lt16[lh][j][k] = bf16(L[lh][k][j]): the B operand (N = j, K = k, K-major) of Y = V L.
+__global__ void pack_lt_kernel(const float *__restrict__ L, __nv_bfloat16 *__restrict__ lt,
+                               int d) {
+    const size_t base = (size_t)blockIdx.x * d * d;
+    for (int e = threadIdx.x; e < d * d; e += blockDim.x) {
+        const int j = e / d, k = e % d;
+        lt[base + e] = __float2bfloat16_rn(L[base + (size_t)k * d + j]);
+    }
+}
+
+// q16[unit][qi][:] = the query of row qi (head-major, window rows then lookahead rows).
+__global__ void pack_queries_kernel(const __nv_bfloat16 *__restrict__ QW,
+                                    const __nv_bfloat16 *__restrict__ QL, LorekvDims D,
+                                    __nv_bfloat16 *__restrict__ q16) {
+    const int qi = blockIdx.x, unit = blockIdx.y;
+    const int kh = unit % D.Hkv, sl = unit / D.Hkv;
+    const int j = qi / D.nq, r = qi % D.nq, h = kh * D.g + j;
+    const __nv_bfloat16 *src = (r < D.w) ? QW + (((size_t)sl * D.Hq + h) * D.w + r) * D.d
+                                         : QL + (((size_t)sl * D.Hq + h) * D.MT + (r - D.w)) * D.d;
+    __nv_bfloat16 *dst = q16 + ((size_t)unit * D.Qu + qi) * D.d;
+    for (int k = threadIdx.x; k < D.d; k += blockDim.x) dst[k] = src[k];
+}
+
+// Per-query constants of the scoring epilogue: {-lse2, c, weight, 0}.
+__global__ void pack_qconst_kernel(const float *__restrict__ lse2, const float *__restrict__ cq,
+                                   const float *__restrict__ wq, long rows,
+                                   float4 *__restrict__ qconst) {
+    const long r = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (r < rows) qconst[r] = make_float4(-lse2[r], cq[r], wq[r], 0.f);
+}
+
+// S_i = sum over query heads of the partial scores (fixed order); 0 for protected tokens.
+__global__ void reduce_heads_kernel(const float *__restrict__ part, int g, int n, int sink, int w,
+                                    float *__restrict__ S) {
+    const int unit = blockIdx.y;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float acc = 0.f;
+    for (int j = 0; j < g; ++j) acc += part[((size_t)unit * g + j) * n + i];
+    S[(size_t)unit * n + i] = (i >= sink && i < n - w) ? acc : 0.f;
+}
+
+// ---- scores kernel -----------------------------------------------------------------------------------
+struct ScoresArgs {
+    int n, g, Hkv, L, Hq, nq, Qu, sink, w;
+    int ntiles, tpr, nranges;
+    float eps, k1;
+    const float4 *qconst;
+    float *part_s;
+    unsigned *err;
+};
+
+constexpr int kScThreads = 320;
+constexpr uint32_t SC_Q = 0, SC_U = 16384, SC_LT = 32768, SC_ST = 65536;  // stage: K 32K + V 32K
+constexpr uint32_t SC_QC = SC_ST + 2 * 65536;
+constexpr uint32_t SC_BAR = SC_QC + 64 * 16;
+constexpr size_t SC_SMEM = SC_BAR + 256 + 1024;
+
+__global__ void __launch_bounds__(kScThreads, 1)
+    scores_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_u,
+                     const __grid_constant__ CUtensorMap tm_lt, ScoresArgs A) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.x;
+    const int j = b % A.g;
+    const int range = (b / A.g) % A.nranges;
+    const int unit = b / (A.g * A.nranges);
+    const int t_begin = range * A.tpr;
+    const int ntl = min(A.ntiles, t_begin + A.tpr) - t_begin;
+    if (ntl <= 0) return;
+    const int kh = unit % A.Hkv, l = (unit / A.Hkv) % A.L, h = kh * A.g + j;
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SC_BAR);
+    uint64_t *ops_full = bars + 0, *full = bars + 1, *empty = bars + 3, *tfull = bars + 5,
+             *tempty = bars + 7;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 9);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 10);
+    float4 *qc = reinterpret_cast<float4 *>(sm + SC_QC);
+
+    if (threadIdx.x == 0) {
+        tc::mbar_init(ops_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+            tc::mbar_init(&tfull[s], 1);
+            tc::mbar_init(&tempty[s], 128);
+        }
+        *abort_flag = 0;
+        tc::mbar_fence_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::fence_before_sync();
+    }
+    if (threadIdx.x >= 64 && threadIdx.x < 128) {
+        const int t = threadIdx.x - 64;
+        qc[t] = (t < A.nq) ? A.qconst[(size_t)unit * A.Qu + j * A.nq + t]
+                           : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {  // ---- TMA producer ----
+            const int qrow = unit * A.Qu + j * A.nq;
+            const int lrow = (l * A.Hq + h) * 128;
+            tc::mbar_expect_tx(ops_full, 65536);
+            tc::tma_load_2d(sm + SC_Q, &tm_q, 0, qrow, ops_full);
+            tc::tma_load_2d(sm + SC_Q + 8192, &tm_q, 64, qrow, ops_full);
+            tc::tma_load_2d(sm + SC_U, &tm_u, 0, qrow, ops_full);
+            tc::tma_load_2d(sm + SC_U + 8192, &tm_u, 64, qrow, ops_full);
+            tc::tma_load_2d(sm + SC_LT, &tm_lt, 0, lrow, ops_full);
+            tc::tma_load_2d(sm + SC_LT + 16384, &tm_lt, 64, lrow, ops_full);
+            for (int i = 0; i < ntl; ++i) {
+                const int s = i & 1;
+                const uint32_t ph = (i >> 1) & 1;
+                if (!tc::mbar_wait(&empty[s], ph ^ 1, abort_flag, A.err)) break;
+                tc::mbar_expect_tx(&full[s], 65536);
+                const int row = unit * A.n + (t_begin + i) * 128;
+                uint8_t *st = sm + SC_ST + s * 65536;
+                tc::tma_load_2d(st, &tm_k, 0, row, &full[s]);
+                tc::tma_load_2d(st + 16384, &tm_k, 64, row, &full[s]);
+                tc::tma_load_2d(st + 32768, &tm_v, 0, row, &full[s]);
+                tc::tma_load_2d(st + 49152, &tm_v, 64, row, &full[s]);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && tc::mbar_wait(ops_full, 0, abort_flag, A.err)) {  // ---- MMA issuer ----
+            tc::fence_after_sync();
+            const uint32_t q_addr = tc::smem_u32(sm + SC_Q), u_addr = tc::smem_u32(sm + SC_U);
+            const uint32_t lt_addr = tc::smem_u32(sm + SC_LT);
+            constexpr uint32_t id64 = tc::idesc_bf16(128, 64, 0);
+            for (int i = 0; i < ntl; ++i) {
+                const int s = i & 1, bb = i & 1;
+                const uint32_t ph = (i >> 1) & 1;
+                if (!tc::mbar_wait(&full[s], ph, abort_flag, A.err)) break;
+                if (!tc::mbar_wait(&tempty[bb], ph ^ 1, abort_flag, A.err)) break;
+                tc::fence_after_sync();
+                const uint32_t k_addr = tc::smem_u32(sm + SC_ST + s * 65536);
+                const uint32_t v_addr = k_addr + 32768;
+                const uint32_t d0 = tmem + bb * 256;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;  // 128-row operand
+                    const uint32_t bo = (k >> 2) * 8192 + (k & 3) * 32;   // 64-row operand
+                    tc::mma_bf16(d0 + 0, tc::sdesc_sw128(k_addr + ao, 16, 1024),
+                                 tc::sdesc_sw128(q_addr + bo, 16, 1024), id64, k > 0);
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;
+                    const uint32_t bo = (k >> 2) * 8192 + (k & 3) * 32;
+                    tc::mma_bf16(d0 + 64, tc::sdesc_sw128(v_addr + ao, 16, 1024),
+                                 tc::sdesc_sw128(u_addr + bo, 16, 1024), id64, k > 0);
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {  // columns j < 64 of L^T v: all of k
+                    const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;
+                    const uint32_t bo = (k >> 2) * 16384 + (k & 3) * 32;
+                    tc::mma_bf16(d0 + 128, tc::sdesc_sw128(v_addr + ao, 16, 1024),
+                                 tc::sdesc_sw128(lt_addr + bo, 16, 1024), id64, k > 0);
+                }
+#pragma unroll
+                for (int k = 4; k < 8; ++k) {  // columns j >= 64: L[k][j] = 0 for k < 64
+                    const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;
+                    const uint32_t bo = (k >> 2) * 16384 + 8192 + (k & 3) * 32;
+                    tc::mma_bf16(d0 + 192, tc::sdesc_sw128(v_addr + ao, 16, 1024),
+                                 tc::sdesc_sw128(lt_addr + bo, 16, 1024), id64, k > 4);
+                }
+                tc::mma_commit(&empty[s]);
+                tc::mma_commit(&tfull[bb]);
+            }
+        }
+    } else {  // ---- epilogue: two 4-warp groups, alternate tiles ----
+        const int wg = (warp - 2) >> 2, lg = warp & 3;
+        const int row = lg * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
+        float *out = A.part_s + ((size_t)unit * A.g + j) * A.n;
+        const float one_eps = 1.f + A.eps;
+        for (int i = wg; i < ntl; i += 2) {
+            const uint32_t ph = (i >> 1) & 1;
+            if (!tc::mbar_wait(&tfull[wg], ph, abort_flag, A.err)) break;
+            tc::fence_after_sync();
+            const uint32_t tb = tmem + lane_off + wg * 256;
+            float nv = 0.f;
+            {
+                float y0[32], y1[32];
+                tc::tmem_ld32(tb + 128, y0);
+                tc::tmem_ld32(tb + 160, y1);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) nv = fmaf(y0[c], y0[c], fmaf(y1[c], y1[c], nv));
+                tc::tmem_ld32(tb + 192, y0);
+                tc::tmem_ld32(tb + 224, y1);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) nv = fmaf(y0[c], y0[c], fmaf(y1[c], y1[c], nv));
+            }
+            float s0[32], s1[32], x0[32], x1[32];
+            tc::tmem_ld32(tb + 0, s0);
+            tc::tmem_ld32(tb + 32, s1);
+            tc::tmem_ld32(tb + 64, x0);
+            tc::tmem_ld32(tb + 96, x1);
+            tc::tmem_wait_ld();
+            tc::fence_before_sync();
+            tc::mbar_arrive(&tempty[wg]);
+            float acc = 0.f;
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                const float4 c = qc[q];
+                const float a = tc::ex2_approx(fmaf(s0[q], A.k1, c.x));
+                const float x = fmaxf(fmaf(-2.f, x0[q], nv + c.y), 1e-30f);
+                const float dd = one_eps - a;
+                acc = fmaf(c.z, a * x * tc::rsqrt_approx(x * dd * dd), acc);
+            }
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                const float4 c = qc[32 + q];
+                const float a = tc::ex2_approx(fmaf(s1[q], A.k1, c.x));
+                const float x = fmaxf(fmaf(-2.f, x1[q], nv + c.y), 1e-30f);
+                const float dd = one_eps - a;
+                acc = fmaf(c.z, a * x * tc::rsqrt_approx(x * dd * dd), acc);
+            }
+            const int tok = (t_begin + i) * 128 + row;
+            if (tok < A.n) out[tok] = (tok >= A.sink && tok < A.n - A.w) ? acc : 0.f;
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---- attention-statistics kernel ------------------------------------------------------------------
+struct AttnArgs {
+    int n, Qu, nq, w, window_causal, nsplit, split_len, nqp;
+    float k1;
+    float2 *part_ml;
+    float *part_o;
+    unsigned *err;
+};
+
+constexpr int kAtThreads = 320;
+constexpr uint32_t AT_Q = 0, AT_P = 65536, AT_RING = 131072;  // Q0,Q1 | P0,P1 | 3 x 32 KB ring
+constexpr uint32_t AT_BAR = AT_RING + 3 * 32768;
+constexpr size_t AT_SMEM = AT_BAR + 256 + 1024;
+constexpr float kRescaleLog2 = 8.f;  // rescale O only when a row maximum grows by > 2^8
+
+// S_t = Q_t K_i^T for query tile t (K_i = ring item 2i).
+__device__ __forceinline__ bool attn_issue_s(uint32_t base, uint32_t tmem, int t, int i,
+                                             uint64_t *rfull, uint64_t *rempty, uint64_t *s_full,
+                                             uint64_t *s_free, volatile int *abort_flag,
+                                             unsigned *err) {
+    constexpr uint32_t id_s = tc::idesc_bf16(128, 128, 0);
+    const int c = 2 * i, slot = c % 3;
+    if (t == 0 && !tc::mbar_wait(&rfull[slot], (c / 3) & 1, abort_flag, err)) return false;
+    if (!tc::mbar_wait(&s_free[t], (i & 1) ^ 1, abort_flag, err)) return false;
+    tc::fence_after_sync();
+    const uint32_t q_addr = base + AT_Q + t * 32768;
+    const uint32_t k_addr = base + AT_RING + slot * 32768;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
+        tc::mma_bf16(tmem + t * 128, tc::sdesc_sw128(q_addr + o, 16, 1024),
+                     tc::sdesc_sw128(k_addr + o, 16, 1024), id_s, k > 0);
+    }
+    tc::mma_commit(&s_full[t]);
+    if (t == 1) tc::mma_commit(&rempty[slot]);
+    return true;
+}
+
+// O_t += P_t V_i for query tile t (V_i = ring item 2i+1, the MN-major B operand).
+__device__ __forceinline__ bool attn_issue_pv(uint32_t base, uint32_t tmem, int t, int i,
+                                              uint64_t *rfull, uint64_t *rempty, uint64_t *p_full,
+                                              uint64_t *o_done, volatile int *abort_flag,
+                                              unsigned *err) {
+    constexpr uint32_t id_pv = tc::idesc_bf16(128, 128, 1);
+    const int c = 2 * i + 1, slot = c % 3;
+    if (t == 0 && !tc::mbar_wait(&rfull[slot], (c / 3) & 1, abort_flag, err)) return false;
+    if (!tc::mbar_wait(&p_full[t], i & 1, abort_flag, err)) return false;
+    tc::fence_after_sync();
+    const uint32_t p_addr = base + AT_P + t * 32768;
+    const uint32_t v_addr = base + AT_RING + slot * 32768;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {  // K = 16 tokens per step
+        const uint32_t po = (k >> 2) * 16384 + (k & 3) * 32;
+        const uint32_t vo = k * 2048;  // 16 tokens x 128 bytes
+        tc::mma_bf16(tmem + 256 + t * 128, tc::sdesc_sw128(p_addr + po, 16, 1024),
+                     tc::sdesc_sw128(v_addr + vo, 16384, 1024), id_pv,
+                     (i > 0 || k > 0) ? 1u : 0u);
+    }
+    tc::mma_commit(&o_done[t]);
+    if (t == 1) tc::mma_commit(&rempty[slot]);
+    return true;
+}
+
+// 320 threads x 200 registers fit the 64K-register file with one CTA per SM.
+__global__ void __maxnreg__(200)
+    attention_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_q, AttnArgs A) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sp = blockIdx.x % A.nsplit;
+    const int qp = (blockIdx.x / A.nsplit) % A.nqp;
+    const int unit = blockIdx.x / (A.nsplit * A.nqp);
+    const int t0 = sp * A.split_len, t1 = min(A.n, t0 + A.split_len);
+    const int ntl = (t1 - t0 + 127) / 128;
+    if (ntl <= 0) return;
+    const int qbase = qp * 256;
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + AT_BAR);
+    uint64_t *q_full = bars + 0, *rfull = bars + 1, *rempty = bars + 4, *s_full = bars + 7,
+             *s_free = bars + 9, *p_full = bars + 11, *o_done = bars + 13;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 16);
+
+    if (threadIdx.x == 0) {
+        tc::mbar_init(q_full, 1);
+        for (int s = 0; s < 3; ++s) {
+            tc::mbar_init(&rfull[s], 1);
+            tc::mbar_init(&rempty[s], 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            tc::mbar_init(&s_full[t], 1);
+            tc::mbar_init(&s_free[t], 128);
+            tc::mbar_init(&p_full[t], 128);
+            tc::mbar_init(&o_done[t], 1);
+        }
+        *abort_flag = 0;
+        tc::mbar_fence_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::fence_before_sync();
+    }
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {  // ---- TMA producer: Q once, then K_i, V_i through a 3-slot ring ----
+            const int qrow = unit * A.Qu + qbase;
+            tc::mbar_expect_tx(q_full, 65536);
+            for (int t = 0; t < 2; ++t) {
+                tc::tma_load_2d(sm + AT_Q + t * 32768, &tm_q, 0, qrow + 128 * t, q_full);
+                tc::tma_load_2d(sm + AT_Q + t * 32768 + 16384, &tm_q, 64, qrow + 128 * t, q_full);
+            }
+            for (int c = 0; c < 2 * ntl; ++c) {
+                const int slot = c % 3;
+                const uint32_t ph = (c / 3) & 1;
+                if (!tc::mbar_wait(&rempty[slot], ph ^ 1, abort_flag, A.err)) break;
+                tc::mbar_expect_tx(&rfull[slot], 32768);
+                const int row = unit * A.n + t0 + (c >> 1) * 128;
+                const CUtensorMap *map = (c & 1) ? &tm_v : &tm_k;
+                uint8_t *dst = sm + AT_RING + slot * 32768;
+                tc::tma_load_2d(dst, map, 0, row, &rfull[slot]);
+                tc::tma_load_2d(dst + 16384, map, 64, row, &rfull[slot]);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && tc::mbar_wait(q_full, 0, abort_flag, A.err)) {  // ---- MMA issuer ----
+            const uint32_t base = tc::smem_u32(sm);
+            bool ok = attn_issue_s(base, tmem, 0, 0, rfull, rempty, s_full, s_free, abort_flag,
+                                   A.err) &&
+                      attn_issue_s(base, tmem, 1, 0, rfull, rempty, s_full, s_free, abort_flag,
+                                   A.err);
+            for (int i = 0; ok && i < ntl; ++i) {
+                ok = attn_issue_pv(base, tmem, 0, i, rfull, rempty, p_full, o_done, abort_flag,
+                                   A.err);
+                if (ok && i + 1 < ntl)
+                    ok = attn_issue_s(base, tmem, 0, i + 1, rfull, rempty, s_full, s_free,
+                                      abort_flag, A.err);
+                if (ok)
+                    ok = attn_issue_pv(base, tmem, 1, i, rfull, rempty, p_full, o_done,
+                                       abort_flag, A.err);
+                if (ok && i + 1 < ntl)
+                    ok = attn_issue_s(base, tmem, 1, i + 1, rfull, rempty, s_full, s_free,
+                                      abort_flag, A.err);
+            }
+        }
+    } else {  // ---- softmax groups: warps 2-5 own query tile 0, warps 6-9 tile 1 ----
+        const int t = (warp - 2) >> 2, lg = warp & 3;
+        const int r = lg * 32 + lane;
+        const int qi = qbase + 128 * t + r;
+        const bool valid_row = qi < A.Qu;
+        const int rr = qi % A.nq;
+        const int nvis = (valid_row && rr < A.w && A.window_causal) ? A.n - A.w + rr + 1 : A.n;
+        const int vend = min(t1, nvis);
+        const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
+        const uint32_t s_col = tmem + lane_off + t * 128;
+        const uint32_t o_col = tmem + lane_off + 256 + t * 128;
+        uint8_t *P = sm + AT_P + t * 32768;
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int i = 0; i < ntl; ++i) {
+            if (!tc::mbar_wait(&s_full[t], i & 1, abort_flag, A.err)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            float s[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_col + c * 32, s[c]);
+            tc::tmem_wait_ld();
+            tc::fence_before_sync();
+            tc::mbar_arrive(&s_free[t]);
+            const int nv_tile = vend - (t0 + i * 128);  // valid columns of this row in the tile
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float x = (c * 32 + e < nv_tile) ? s[c][e] * A.k1 : -INFINITY;
+                    s[c][e] = x;
+                    mt = fmaxf(mt, x);
+                }
+            const float m_new = fmaxf(m_used, mt);
+            // O is rescaled only when the row maximum grew by more than 2^8 (and O holds data)
+            const bool rescale = m_new > m_used + kRescaleLog2;
+            const float f = (rescale && i > 0) ? tc::ex2_approx(m_used - m_new) : 1.f;
+            if (rescale) m_used = m_new;
+            float lsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float p = (m_used == -INFINITY) ? 0.f : tc::ex2_approx(s[c][e] - m_used);
+                    s[c][e] = p;
+                    lsum += p;
+                }
+            l = fmaf(l, f, lsum);
+            // P_t and O_t are free once the previous P V product has completed
+            if (i > 0 && !tc::mbar_wait(&o_done[t], (i - 1) & 1, abort_flag, A.err)) {
+                ok = false;
+                break;
+            }
+            // P row -> shared memory, 128-byte-swizzled K-major (tokens 0-63 | 64-127 blocks)
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch) {
+                const int c = ch >> 2, e0 = (ch & 3) * 8;
+                uint4 pk;
+                __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    h2[u] = __floats2bfloat162_rn(s[c][e0 + 2 * u], s[c][e0 + 2 * u + 1]);
+                *reinterpret_cast<uint4 *>(P + (ch >> 3) * 16384 + tc::sw128_offset(r, ch & 7)) = pk;
+            }
+            if (f != 1.f) {
+                tc::fence_after_sync();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float o[32];
+                    tc::tmem_ld32(o_col + c * 32, o);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] *= f;
+                    tc::tmem_st32(o_col + c * 32, o);
+                }
+                tc::tmem_wait_st();
+            }
+            tc::fence_proxy_async_smem();
+            tc::fence_before_sync();
+            tc::mbar_arrive(&p_full[t]);
+        }
+        if (ok && tc::mbar_wait(&o_done[t], (ntl - 1) & 1, abort_flag, A.err)) {
+            tc::fence_after_sync();
+            const size_t rowi = ((size_t)unit * A.nsplit + sp) * A.Qu + qi;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float o[32];
+                tc::tmem_ld32(o_col + c * 32, o);
+                tc::tmem_wait_ld();
+                if (valid_row) {
+                    float4 *dst = reinterpret_cast<float4 *>(A.part_o + rowi * 128 + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+                }
+            }
+            if (valid_row) A.part_ml[rowi] = make_float2(m_used, l);
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_pack_queries(const LorekvDims &D, const void *QW, const void *QL, void *ws,
+                                const LorekvWorkspace &W, cudaStream_t st) {
+    __nv_bfloat16 *q16 = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) + W.q16);
+    pack_queries_kernel<<<dim3(D.Qu, D.units), 128, 0, st>>>(
+        static_cast<const __nv_bfloat16 *>(QW), static_cast<const __nv_bfloat16 *>(QL), D, q16);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attention_tc(const LorekvDims &D, const void *K, const void *V, void *ws,
+                                const LorekvWorkspace &W, unsigned *err, cudaStream_t st) {
+    char *b = static_cast<char *>(ws);
+    CUtensorMap tk, tv, tq;
+    const uint64_t rows = (uint64_t)D.units * D.n;
+    if (!make_tmap_bf16_2d(&tk, K, 128, rows, 64, 128) ||
+        !make_tmap_bf16_2d(&tv, V, 128, rows, 64, 128) ||
+        !make_tmap_bf16_2d(&tq, b + W.q16, 128, (uint64_t)D.units * D.Qu, 64, 128))
+        return cudaErrorInvalidValue;
+    AttnArgs A;
+    A.n = D.n;
+    A.Qu = D.Qu;
+    A.nq = D.nq;
+    A.w = D.w;
+    A.window_causal = D.window_causal;
+    A.nsplit = D.nsplit;
+    A.split_len = D.split_len;
+    A.nqp = (D.Qu + 255) / 256;
+    A.k1 = kLog2e / sqrtf((float)D.d);
+    A.part_ml = reinterpret_cast<float2 *>(b + W.part_ml);
+    A.part_o = reinterpret_cast<float *>(b + W.part_o);
+    A.err = err;
+    cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AT_SMEM);
+    if (e != cudaSuccess) return e;
+    attention_tc_kernel<<<D.units * A.nqp * D.nsplit, kAtThreads, AT_SMEM, st>>>(tk, tv, tq, A);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scores_tc(const LorekvDims &D, const void *K, const void *V, const float *Lf,
+                             void *ws, const LorekvWorkspace &W, float *scores, unsigned *err,
+                             cudaStream_t st) {
+    char *b = static_cast<char *>(ws);
+    __nv_bfloat16 *lt16 = reinterpret_cast<__nv_bfloat16 *>(b + W.lt16);
+    pack_lt_kernel<<<D.L * D.Hq, 256, 0, st>>>(Lf, lt16, D.d);
+    const long rows_q = (long)D.units * D.Qu;
+    pack_qconst_kernel<<<(unsigned)((rows_q + 255) / 256), 256, 0, st>>>(
+        reinterpret_cast<const float *>(b + W.lse2), reinterpret_cast<const float *>(b + W.cq),
+        reinterpret_cast<const float *>(b + W.wq), rows_q,
+        reinterpret_cast<float4 *>(b + W.qconst));
+    CUtensorMap tk, tv, tq, tu, tl;
+    const uint64_t rows = (uint64_t)D.units * D.n;
+    if (!make_tmap_bf16_2d(&tk, K, 128, rows, 64, 128) ||
+        !make_tmap_bf16_2d(&tv, V, 128, rows, 64, 128) ||
+        !make_tmap_bf16_2d(&tq, b + W.q16, 128, (uint64_t)rows_q, 64, 64) ||
+        !make_tmap_bf16_2d(&tu, b + W.u16, 128, (uint64_t)rows_q, 64, 64) ||
+        !make_tmap_bf16_2d(&tl, lt16, 128, (uint64_t)D.L * D.Hq * 128, 64, 128))
+        return cudaErrorInvalidValue;
+    ScoresArgs A;
+    A.n = D.n;
+    A.g = D.g;
+    A.Hkv = D.Hkv;
+    A.L = D.L;
+    A.Hq = D.Hq;
+    A.nq = D.nq;
+    A.Qu = D.Qu;
+    A.sink = D.sink;
+    A.w = D.w;
+    A.ntiles = (D.n + 127) / 128;
+    A.nranges = balance_parts((long)D.units * D.g, A.ntiles, 64);
+    A.tpr = (A.ntiles + A.nranges - 1) / A.nranges;
+    A.nranges = (A.ntiles + A.tpr - 1) / A.tpr;
+    A.eps = D.eps;
+    A.k1 = kLog2e / sqrtf((float)D.d);
+    A.qconst = reinterpret_cast<const float4 *>(b + W.qconst);
+    A.part_s = reinterpret_cast<float *>(b + W.part_s);
+    A.err = err;
+    cudaError_t e = cudaFuncSetAttribute(scores_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SC_SMEM);
+    if (e != cudaSuccess) return e;
+    scores_tc_kernel<<<D.units * A.nranges * D.g, kScThreads, SC_SMEM, st>>>(tk, tv, tq, tu, tl, A);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    reduce_heads_kernel<<<dim3((D.n + 255) / 256, D.units), 256, 0, st>>>(
+        A.part_s, D.g, D.n, D.sink, D.w, scores);
+    return cudaGetLastError();
 }
 
 }  // namespace kve
