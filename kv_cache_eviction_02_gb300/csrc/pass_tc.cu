@@ -383,8 +383,8 @@ __device__ __forceinline__ bool attn_issue_pv(uint32_t base, uint32_t tmem, int 
     return true;
 }
 
-// 320 threads x 200 registers fit the 64K-register file with one CTA per SM.
-__global__ void __maxnreg__(200)
+// 10 warps: three share a sub-partition's 16K registers, so at most 168 registers a thread.
+__global__ void __launch_bounds__(kAtThreads, 1)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_q, AttnArgs A) {
