@@ -44,7 +44,7 @@ NCU_TRAFFIC = {}
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--steps", type=int, default=30)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--no-h2o", action="store_true")
@@ -105,7 +105,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                 "--format=csv,noheader,nounits", "-lms", "50", "-f", self.path],
                 stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
         except FileNotFoundError:
             self.proc = None
@@ -341,12 +341,20 @@ def run_native(args):
         flops = attention_algorithmic_flops_per_token_unit(cfg) * tokens_per_step
     else:
         flops = None
-    kernel_src = {"scores": "kv_cache_eviction_02_gb300/csrc/pass_simt.cu",
-                  "attention": "kv_cache_eviction_02_gb300/csrc/pass_simt.cu"}.get(dom)
+    tensor = cfg.dtype == "bf16" and cfg.d == 128 and cfg.w + cfg.M * cfg.T <= 64
+    src = ("kv_cache_eviction_02_gb300/csrc/pass_tc.cu" if tensor
+           else "kv_cache_eviction_02_gb300/csrc/pass_simt.cu")
     traffic = None
-    if kernel_src and dom in NCU_TRAFFIC and NCU_TRAFFIC[dom][1] == src_hash(kernel_src):
+    if dom in NCU_TRAFFIC and NCU_TRAFFIC[dom][1] == src_hash(src):
         traffic = NCU_TRAFFIC[dom][0]
-    if flops is not None:
+    if flops is not None and tensor:
+        # a ~20 ms step timed for well under a second: the burst bf16 figure applies
+        ach = flops / (dom_ms / 1e3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "traffic": traffic,
+                "peak_source": f"bf16 dense burst, {pk['source']}", "ms_per_launch": dom_ms,
+                "flops": "algorithmic"}
+    elif flops is not None:
         ach = flops / (dom_ms / 1e3) / 1e12
         roof = {"kernel": dom, "bound": "alu", "achieved": ach, "peak": FP32_ALU_PEAK_TFLOPS,
                 "unit": "TFLOP/s", "frac": ach / FP32_ALU_PEAK_TFLOPS, "traffic": traffic,

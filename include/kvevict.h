@@ -187,6 +187,13 @@ const char *kve_last_error(void);
  * waits set. Returns KVE_OK, KVE_ETIMEOUT (a wait gave up) or KVE_ECUDA. */
 int kve_check_device(void *stream);
 
+/* Self-test of the bounded on-device waits: launches one CTA whose thread waits, through the same
+ * routine the tensor-core kernels use, on an on-chip barrier that nothing signals, with a limit of
+ * limit_ms milliseconds (1..10000). The wait gives up, records the timeout in the device error word
+ * and the kernel returns normally; kve_check_device(stream) then reports KVE_ETIMEOUT and clears
+ * the word. Asynchronous on `stream`. */
+int kve_selftest_wait_timeout(int limit_ms, void *stream);
+
 /* Host-side fault injection for tests: the next `count` calls of the API (excluding the
  * diagnostics) fail with `status` before touching the GPU. count = 0 clears it. */
 int kve_inject_failure(int status, int count);

@@ -24,7 +24,8 @@ EXPORTED = ("lorekv_prepare_wo", "lorekv_workspace_size", "lorekv_score",
             "lorekv_attention_stats", "lorekv_kept_capacity", "lorekv_select_compact",
             "h2o_state_create", "h2o_prefill", "h2o_decode_step", "h2o_export", "h2o_capacity",
             "h2o_length", "h2o_state_destroy", "kve_last_error", "kve_check_device",
-            "kve_inject_failure", "kve_profile_enable", "kve_profile_report", "kve_version")
+            "kve_inject_failure", "kve_profile_enable", "kve_profile_report", "kve_version",
+            "kve_selftest_wait_timeout")
 
 
 class KveError(RuntimeError):
@@ -76,6 +77,7 @@ def lib():
         L.kve_check_device.argtypes = [P]
         L.kve_inject_failure.argtypes = [I, I]
         L.kve_profile_enable.argtypes = [I]
+        L.kve_selftest_wait_timeout.argtypes = [I, P]
         L.kve_profile_report.argtypes = [ctypes.c_char_p, Z]
         _lib = L
     return _lib
@@ -198,6 +200,10 @@ def lorekv_select_compact(pb, scores, K, V, kept_idx, kept_len, K_out, V_out, wo
 
 def kve_check_device(stream=None):
     _check(lib().kve_check_device(_stream(stream)))
+
+
+def kve_selftest_wait_timeout(limit_ms: int, stream=None):
+    _check(lib().kve_selftest_wait_timeout(limit_ms, _stream(stream)))
 
 
 def kve_inject_failure(status: int, count: int):

@@ -24,6 +24,7 @@ cudaError_t launch_attention_tc(const LorekvDims &D, const void *K, const void *
                                 const LorekvWorkspace &W, unsigned *err_word, cudaStream_t st);
 cudaError_t launch_pack_queries(const LorekvDims &D, const void *QW, const void *QL, void *ws,
                                 const LorekvWorkspace &W, cudaStream_t st);
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, unsigned *err, cudaStream_t st);
 
 namespace {
 
@@ -289,6 +290,18 @@ int kve_check_device(void *stream) {
             return fail(KVE_ETIMEOUT, "a bounded on-device wait gave up (error word 0x%x)", word);
         return fail(KVE_ECUDA, "device error word 0x%x", word);
     }
+    return KVE_OK;
+}
+
+int kve_selftest_wait_timeout(int limit_ms, void *stream) {
+    if (int s = injected()) return s;
+    if (limit_ms < 1 || limit_ms > 10000)
+        return fail(KVE_EINVAL, "kve_selftest_wait_timeout: limit_ms must be in [1, 10000]");
+    unsigned *err = device_error_word();
+    if (!err) return fail(KVE_ECUDA, "kve_selftest_wait_timeout: no device error word");
+    cudaError_t e = launch_wait_timeout_selftest((uint64_t)limit_ms * 1000000ull, err,
+                                                 static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kve_selftest_wait_timeout: launch");
     return KVE_OK;
 }
 

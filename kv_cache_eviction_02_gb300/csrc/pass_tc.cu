@@ -579,7 +579,26 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     }
 }
 
+// One thread waits on an mbarrier that nothing signals, through the same bounded wait the
+// kernels above use; the wait gives up after limit_ns and records the timeout.
+__global__ void wait_timeout_selftest_kernel(uint64_t limit_ns, unsigned *err) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar, 1);
+        abort_flag = 0;
+        tc::mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) tc::mbar_wait(&bar, 0, &abort_flag, err, limit_ns);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, unsigned *err, cudaStream_t st) {
+    wait_timeout_selftest_kernel<<<1, 32, 0, st>>>(limit_ns, err);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_pack_queries(const LorekvDims &D, const void *QW, const void *QL, void *ws,
                                 const LorekvWorkspace &W, cudaStream_t st) {

@@ -54,14 +54,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // returns false, so that every role of the CTA leaves its loop and the CTA tears down.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          unsigned *err) {
+                                          unsigned *err, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255u) == 0u) {
             if (*abort) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
+            if (globaltimer() - t0 > limit_ns) {
                 if (err) atomicOr(err, KVE_DEVERR_TIMEOUT);
                 *abort = 1;
                 return false;
