@@ -105,6 +105,26 @@ int lorekv_score(const KveShape *shape, const KveLorekvParams *params, const voi
                  const float *G, const float *logits, const int32_t *sampled, float *scores_out,
                  float *omega_out, void *workspace, size_t ws_bytes, void *stream);
 
+/* lorekv_score without a caller-provided workspace, for callers that cannot allocate device
+ * memory (for example code that runs inside a memory budget owned by someone else, or where no
+ * device allocator is reachable). There is no counterpart on the pages: it is the same pass as
+ * lorekv_score with identical arguments and results, only the scratch memory differs.
+ *   - Scratch comes from one fixed array of 64 MiB in the library's device image. Shapes whose
+ *     lorekv_workspace_size() exceeds 64 MiB are rejected with KVE_EWORKSPACE (nothing launched);
+ *     use lorekv_score with a workspace for them.
+ *   - The call allocates nothing (no cudaMalloc/cudaFree, no library allocator).
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ *     that device current; make that first call before any stream capture.
+ *   - The array is shared by every call on the device and keeps the last call's contents; nothing
+ *     in it needs to start at zero (each call writes every scratch region before reading it).
+ *     Calls that overlap on the GPU (different streams, or threads without ordering) race on it:
+ *     serialise them.
+ *   - Each GPU on which the array is loaded keeps it until the process exits. */
+int lorekv_score_noalloc(const KveShape *shape, const KveLorekvParams *params, const void *K,
+                         const void *V, const void *Q_W, const void *Q_look, const float *L,
+                         const float *G, const float *logits, const int32_t *sampled,
+                         float *scores_out, float *omega_out, void *stream);
+
 /* Attention statistics only (the first half of lorekv_score, exposed for testing): for each unit
  * and each of its g*(w+M*T) queries (query head major, then window rows, then lookahead rows):
  *   lse_out [units][g*(w+M*T)] fp32 natural-log log-sum-exp of q.k/sqrt(d) over visible tokens,

@@ -25,7 +25,7 @@ EXPORTED = ("lorekv_prepare_wo", "lorekv_workspace_size", "lorekv_score",
             "h2o_state_create", "h2o_prefill", "h2o_decode_step", "h2o_export", "h2o_capacity",
             "h2o_length", "h2o_state_destroy", "kve_last_error", "kve_check_device",
             "kve_inject_failure", "kve_profile_enable", "kve_profile_report", "kve_version",
-            "kve_selftest_wait_timeout")
+            "kve_selftest_wait_timeout", "lorekv_score_noalloc")
 
 
 class KveError(RuntimeError):
@@ -62,6 +62,7 @@ def lib():
         L.lorekv_workspace_size.argtypes = [SP, PP]
         L.lorekv_workspace_size.restype = Z
         L.lorekv_score.argtypes = [SP, PP, P, P, P, P, P, P, P, P, P, P, P, Z, P]
+        L.lorekv_score_noalloc.argtypes = [SP, PP, P, P, P, P, P, P, P, P, P, P, P]
         L.lorekv_attention_stats.argtypes = [SP, PP, P, P, P, P, P, P, P, Z, P]
         L.lorekv_kept_capacity.argtypes = [SP, PP]
         L.lorekv_select_compact.argtypes = [SP, PP, P, P, P, P, P, P, P, P, Z, P]
@@ -179,6 +180,17 @@ def lorekv_score(pb, K, V, Q_W, Q_look, L, G, logits, sampled, scores_out, omega
                               _ptr(Q_look), _ptr(L), _ptr(G), _ptr(logits), _ptr(sampled),
                               _ptr(scores_out), _ptr(omega_out), _ptr(workspace), ws_bytes,
                               _stream(stream)))
+
+
+def lorekv_score_noalloc(pb, K, V, Q_W, Q_look, L, G, logits, sampled, scores_out, omega_out,
+                         stream=None):
+    """lorekv_score with the library's fixed scratch array instead of a workspace (allocates
+    nothing; shapes needing more than 64 MiB of scratch are rejected)."""
+    sh, pr = pb.shape(), pb.params()
+    _check(lib().lorekv_score_noalloc(ctypes.byref(sh), ctypes.byref(pr), _ptr(K), _ptr(V),
+                                      _ptr(Q_W), _ptr(Q_look), _ptr(L), _ptr(G), _ptr(logits),
+                                      _ptr(sampled), _ptr(scores_out), _ptr(omega_out),
+                                      _stream(stream)))
 
 
 def lorekv_attention_stats(pb, K, V, Q_W, Q_look, lse_out, o_out, workspace, stream=None):

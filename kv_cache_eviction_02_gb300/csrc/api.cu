@@ -93,6 +93,16 @@ struct ProfScope {
 
 }  // namespace
 
+int report_error(int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
 // ---- device error word ---------------------------------------------------------------------------
 __device__ unsigned g_kve_error_word;
 

@@ -29,6 +29,9 @@ inline size_t dtype_size(int dt) { return dt == KVE_F32 ? 4 : 2; }
 enum : unsigned { KVE_DEVERR_TIMEOUT = 1u };
 unsigned *device_error_word();  // device address of the word (per device, set up lazily)
 
+// Records a message for kve_last_error() on the calling thread and returns `code`.
+int report_error(int code, const char *fmt, ...);
+
 // ---- warp helpers ------------------------------------------------------------------------------
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
