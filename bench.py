@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--workload", default=WORKLOAD)
+    p.add_argument("--h2o-batch", type=int, default=64, help="H2O batch (64 = OPT-30B workload)")
+    p.add_argument("--h2o-steps", type=int, default=512, help="H2O decode steps")
     return p.parse_args()
 
 
@@ -450,7 +452,7 @@ def bench_h2o(dev, stream, pg, world, args, pk):
     with the first `warmup` steps untimed."""
     import torch
     from kv_cache_eviction_02_gb300 import api, synth
-    cfg = synth.H2O_CONFIGS["opt30b"]
+    cfg = synth.H2O_CONFIGS["opt30b"].replace(batch=args.h2o_batch, steps=args.h2o_steps)
     hin = synth.h2o_inputs(cfg, dev)
     st = api.h2o_state_create(cfg.batch, cfg.L, cfg.H, cfg.d, cfg.prompt + cfg.steps,
                               cfg.budget_frac, torch.float16)
@@ -491,7 +493,7 @@ def bench_h2o(dev, stream, pg, world, args, pk):
     return {"metric": "KV tokens attended+scored/sec (H2O decode step)",
             "value": tokens * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
             "steps": steps, "warmup": w, "prefill_ms": prefill_ms,
-            "config": f"opt30b: batch {cfg.batch}, {cfg.L} layers, {cfg.H} heads, d_head {cfg.d}, "
+            "config": f"{cfg.name}: batch {cfg.batch}, {cfg.L} layers, {cfg.H} heads, d_head {cfg.d}, "
                       f"prompt {cfg.prompt}, {cfg.steps} decode steps, budget 20%, fp16",
             "roofline": {"kernel": "h2o_step", "bound": "hbm", "achieved": ach,
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"],

@@ -170,7 +170,9 @@ bool lorekv_dims(const KveShape *sh, const KveLorekvParams *p, LorekvDims *D, co
     // shared-memory budget of the CUDA-core scoring kernel
     const size_t sc_smem = sizeof(float) * (2 * 32 * (D->d + 1) + 2 * (size_t)D->nq * D->d +
                                             (size_t)D->d * D->d + 3 * D->nq + 256);
-    if (sc_smem > 227 * 1024) return (*why = "w + M*T too large for d_head"), false;
+    const size_t pu_smem = sizeof(float) * ((size_t)D->d * D->d + (size_t)((D->nq + 3) & ~3) * D->d);
+    if (sc_smem > 227 * 1024 || pu_smem > 227 * 1024)
+        return (*why = "w + M*T too large for d_head"), false;
     // token splits of the statistics pass: enough CTAs to fill the GPU several times
     const long qblocks = (D->Qu + 31) / 32;
     long want = (2432 + qblocks * D->units - 1) / (qblocks * D->units);

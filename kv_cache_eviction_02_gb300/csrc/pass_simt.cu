@@ -149,8 +149,9 @@ __global__ void combine_kernel(LorekvDims D, const float2 *__restrict__ part_ml,
     }
 }
 
-// grid (g, units), block 256. u_q = G_h o_q, c_q = o_q^T G_h o_q, weight_q; bf16 copies of u and
-// of the pre-scaled query for the tensor-core path.
+// grid (g, units), block 256. u_q = G_h o_q, c_q = o_q^T G_h o_q and the query's weight, for the
+// nq queries of one query head; bf16 copy of u for the tensor-core path. G_h and the head's o rows
+// are staged in shared memory; a thread computes a 4-query x 8-dimension block of U.
 template <typename T>
 __global__ void __launch_bounds__(256) prep_u_kernel(LorekvDims D, const float *__restrict__ G,
                                                      const float *__restrict__ omega,
@@ -162,40 +163,73 @@ __global__ void __launch_bounds__(256) prep_u_kernel(LorekvDims D, const float *
                                                      float *__restrict__ wq,
                                                      __nv_bfloat16 *__restrict__ u16,
                                                      __nv_bfloat16 *__restrict__ q16) {
-    extern __shared__ float Gs[];  // [d][d]
-    const int j = blockIdx.x, unit = blockIdx.y;
+    extern __shared__ float sm[];
     const int d = D.d;
+    float *Gs = sm;                 // [d][d]
+    float *Os = sm + d * d;         // [nq_pad][d]
+    const int j = blockIdx.x, unit = blockIdx.y;
     const int kh = unit % D.Hkv, l = (unit / D.Hkv) % D.L, s = unit / (D.Hkv * D.L);
     const int h = kh * D.g + j;
     const float *Gh = G + ((size_t)l * D.Hq + h) * d * d;
+    const size_t row0 = (size_t)unit * D.Qu + (size_t)j * D.nq;
+    const int nq_pad = (D.nq + 3) & ~3;
     for (int idx = threadIdx.x; idx < d * d; idx += blockDim.x) Gs[idx] = Gh[idx];
+    for (int idx = threadIdx.x; idx < nq_pad * d; idx += blockDim.x)
+        Os[idx] = (idx / d < D.nq) ? o[row0 * d + idx] : 0.f;
     __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int r = warp; r < D.nq; r += blockDim.x >> 5) {
-        const int qi = j * D.nq + r;
-        const size_t row = (size_t)unit * D.Qu + qi;
-        const float *orow = o + row * d;
-        float cpart = 0.f;
-        for (int jj = lane; jj < d; jj += 32) {
-            float acc = 0.f;
-            for (int k = 0; k < d; ++k) acc = fmaf(Gs[k * d + jj], orow[k], acc);  // G symmetric
-            u32[row * d + jj] = acc;
-            if (u16) u16[row * d + jj] = __float2bfloat16_rn(acc);
-            cpart = fmaf(orow[jj], acc, cpart);
+    const int gsz = d / 8;                       // threads sharing 4 queries (one per 8 dims)
+    const int jb = threadIdx.x % gsz, qg = threadIdx.x / gsz;
+    const int qstep = blockDim.x / gsz;
+    for (int base = 0; base < nq_pad; base += qstep * 4) {  // uniform trip count: shuffles below
+        const bool active = base + qg * 4 < nq_pad;
+        const int q0 = active ? base + qg * 4 : 0;
+        float acc[4][8];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+        for (int k = 0; k < d; ++k) {
+            const float4 g0 = *reinterpret_cast<const float4 *>(Gs + k * d + jb * 8);
+            const float4 g1 = *reinterpret_cast<const float4 *>(Gs + k * d + jb * 8 + 4);
+            const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const float ov = Os[(q0 + a) * d + k];
+#pragma unroll
+                for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(gv[b], ov, acc[a][b]);  // G symmetric
+            }
         }
-        cpart = warp_sum(cpart);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int r = q0 + a;
+            float cpart = 0.f;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) cpart = fmaf(Os[r * d + jb * 8 + b], acc[a][b], cpart);
+            for (int off = gsz / 2; off > 0; off >>= 1)
+                cpart += __shfl_xor_sync(0xffffffffu, cpart, off);
+            if (active && r < D.nq) {
+                const size_t row = row0 + r;
+#pragma unroll
+                for (int b = 0; b < 8; ++b) u32[row * d + jb * 8 + b] = acc[a][b];
+                if (u16)
+#pragma unroll
+                    for (int b = 0; b < 8; ++b)
+                        u16[row * d + jb * 8 + b] = __float2bfloat16_rn(acc[a][b]);
+                if (jb == 0) cq[row] = cpart;
+            }
+        }
+    }
+    for (int r = threadIdx.x; r < D.nq; r += blockDim.x) {
+        const size_t row = row0 + r;
+        float wt;
+        if (r < D.w)
+            wt = 1.f / (float)(D.g * D.w);
+        else
+            wt = D.lambda_L * omega[(size_t)s * D.M + (r - D.w) / D.T] / (float)(D.g * D.T);
+        wq[row] = wt;
         if (q16) {
-            const T *qp = query_ptr(QW, QL, D, unit, qi);
-            for (int k = lane; k < d; k += 32) q16[row * d + k] = __float2bfloat16_rn(to_f(qp[k]));
-        }
-        if (lane == 0) {
-            cq[row] = cpart;
-            float wt;
-            if (r < D.w)
-                wt = 1.f / (float)(D.g * D.w);
-            else
-                wt = D.lambda_L * omega[(size_t)s * D.M + (r - D.w) / D.T] / (float)(D.g * D.T);
-            wq[row] = wt;
+            const T *qp = query_ptr(QW, QL, D, unit, j * D.nq + r);
+            for (int k = 0; k < d; ++k) q16[row * d + k] = __float2bfloat16_rn(to_f(qp[k]));
         }
     }
 }
@@ -377,7 +411,7 @@ cudaError_t launch_prep_u(const LorekvDims &D, const float *G, const float *omeg
                           const LorekvWorkspace &W, cudaStream_t st, const void *QW,
                           const void *QL, bool want_bf16) {
     char *b = static_cast<char *>(ws);
-    const size_t smem = sizeof(float) * D.d * D.d;
+    const size_t smem = sizeof(float) * (D.d * D.d + (size_t)((D.nq + 3) & ~3) * D.d);
     __nv_bfloat16 *u16 = want_bf16 ? reinterpret_cast<__nv_bfloat16 *>(b + W.u16) : nullptr;
     __nv_bfloat16 *q16 = nullptr;  // the tensor-core path packs the queries itself
     const float *o = reinterpret_cast<const float *>(b + W.o);

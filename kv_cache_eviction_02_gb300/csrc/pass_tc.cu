@@ -135,8 +135,12 @@ struct ScoresArgs {
 };
 
 constexpr int kScThreads = 320;
-constexpr uint32_t SC_Q = 0, SC_U = 16384, SC_LT = 32768, SC_ST = 65536;  // stage: K 32K + V 32K
-constexpr uint32_t SC_QC = SC_ST + 2 * 65536;
+// Shared memory: Q_h (2 x 8 KB K-blocks) | [U_h ; L_h^T] merged B operand (2 K-blocks of 24 KB:
+// 64 rows of U then 128 rows of L^T) | ring of 5 x 32 KB TMA boxes (K_i, V_i, K_i+1, ...) |
+// per-query constants | barriers.
+constexpr uint32_t SC_Q = 0, SC_UL = 16384, SC_UL_BLK = 24576, SC_RING = 65536;
+constexpr int SC_SLOTS = 5;
+constexpr uint32_t SC_QC = SC_RING + SC_SLOTS * 32768;
 constexpr uint32_t SC_BAR = SC_QC + 64 * 16;
 constexpr size_t SC_SMEM = SC_BAR + 256 + 1024;
 
@@ -158,17 +162,19 @@ __global__ void __launch_bounds__(kScThreads, 1)
     const int kh = unit % A.Hkv, l = (unit / A.Hkv) % A.L, h = kh * A.g + j;
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SC_BAR);
-    uint64_t *ops_full = bars + 0, *full = bars + 1, *empty = bars + 3, *tfull = bars + 5,
-             *tempty = bars + 7;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 9);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 10);
+    uint64_t *ops_full = bars + 0, *rfull = bars + 1, *rempty = bars + 1 + SC_SLOTS,
+             *tfull = bars + 1 + 2 * SC_SLOTS, *tempty = bars + 3 + 2 * SC_SLOTS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 5 + 2 * SC_SLOTS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 6 + 2 * SC_SLOTS);
     float4 *qc = reinterpret_cast<float4 *>(sm + SC_QC);
 
     if (threadIdx.x == 0) {
         tc::mbar_init(ops_full, 1);
+        for (int s = 0; s < SC_SLOTS; ++s) {
+            tc::mbar_init(&rfull[s], 1);
+            tc::mbar_init(&rempty[s], 1);
+        }
         for (int s = 0; s < 2; ++s) {
-            tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&empty[s], 1);
             tc::mbar_init(&tfull[s], 1);
             tc::mbar_init(&tempty[s], 128);
         }
@@ -193,69 +199,78 @@ __global__ void __launch_bounds__(kScThreads, 1)
             const int qrow = unit * A.Qu + j * A.nq;
             const int lrow = (l * A.Hq + h) * 128;
             tc::mbar_expect_tx(ops_full, 65536);
-            tc::tma_load_2d(sm + SC_Q, &tm_q, 0, qrow, ops_full);
-            tc::tma_load_2d(sm + SC_Q + 8192, &tm_q, 64, qrow, ops_full);
-            tc::tma_load_2d(sm + SC_U, &tm_u, 0, qrow, ops_full);
-            tc::tma_load_2d(sm + SC_U + 8192, &tm_u, 64, qrow, ops_full);
-            tc::tma_load_2d(sm + SC_LT, &tm_lt, 0, lrow, ops_full);
-            tc::tma_load_2d(sm + SC_LT + 16384, &tm_lt, 64, lrow, ops_full);
-            for (int i = 0; i < ntl; ++i) {
-                const int s = i & 1;
-                const uint32_t ph = (i >> 1) & 1;
-                if (!tc::mbar_wait(&empty[s], ph ^ 1, abort_flag, A.err)) break;
-                tc::mbar_expect_tx(&full[s], 65536);
-                const int row = unit * A.n + (t_begin + i) * 128;
-                uint8_t *st = sm + SC_ST + s * 65536;
-                tc::tma_load_2d(st, &tm_k, 0, row, &full[s]);
-                tc::tma_load_2d(st + 16384, &tm_k, 64, row, &full[s]);
-                tc::tma_load_2d(st + 32768, &tm_v, 0, row, &full[s]);
-                tc::tma_load_2d(st + 49152, &tm_v, 64, row, &full[s]);
+            for (int kb = 0; kb < 2; ++kb) {
+                tc::tma_load_2d(sm + SC_Q + kb * 8192, &tm_q, 64 * kb, qrow, ops_full);
+                tc::tma_load_2d(sm + SC_UL + kb * SC_UL_BLK, &tm_u, 64 * kb, qrow, ops_full);
+                tc::tma_load_2d(sm + SC_UL + kb * SC_UL_BLK + 8192, &tm_lt, 64 * kb, lrow,
+                                ops_full);
+            }
+            for (int c = 0; c < 2 * ntl; ++c) {
+                const int slot = c % SC_SLOTS;
+                const uint32_t ph = (c / SC_SLOTS) & 1;
+                if (!tc::mbar_wait(&rempty[slot], ph ^ 1, abort_flag, A.err)) break;
+                tc::mbar_expect_tx(&rfull[slot], 32768);
+                const int row = unit * A.n + (t_begin + (c >> 1)) * 128;
+                const CUtensorMap *map = (c & 1) ? &tm_v : &tm_k;
+                uint8_t *dst = sm + SC_RING + slot * 32768;
+                tc::tma_load_2d(dst, map, 0, row, &rfull[slot]);
+                tc::tma_load_2d(dst + 16384, map, 64, row, &rfull[slot]);
             }
         }
     } else if (warp == 1) {
         if (lane == 0 && tc::mbar_wait(ops_full, 0, abort_flag, A.err)) {  // ---- MMA issuer ----
             tc::fence_after_sync();
-            const uint32_t q_addr = tc::smem_u32(sm + SC_Q), u_addr = tc::smem_u32(sm + SC_U);
-            const uint32_t lt_addr = tc::smem_u32(sm + SC_LT);
+            const uint32_t q_addr = tc::smem_u32(sm + SC_Q);
+            const uint32_t ul_addr = tc::smem_u32(sm + SC_UL);
+            const uint32_t ring = tc::smem_u32(sm + SC_RING);
             constexpr uint32_t id64 = tc::idesc_bf16(128, 64, 0);
+            constexpr uint32_t id128 = tc::idesc_bf16(128, 128, 0);
+            constexpr uint32_t id192 = tc::idesc_bf16(128, 192, 0);
             for (int i = 0; i < ntl; ++i) {
-                const int s = i & 1, bb = i & 1;
-                const uint32_t ph = (i >> 1) & 1;
-                if (!tc::mbar_wait(&full[s], ph, abort_flag, A.err)) break;
-                if (!tc::mbar_wait(&tempty[bb], ph ^ 1, abort_flag, A.err)) break;
+                const int bb = i & 1;
+                const uint32_t pb = (i >> 1) & 1;
+                const int ck = 2 * i, cv = 2 * i + 1;
+                const int sk = ck % SC_SLOTS, sv = cv % SC_SLOTS;
+                if (!tc::mbar_wait(&rfull[sk], (ck / SC_SLOTS) & 1, abort_flag, A.err)) break;
+                if (!tc::mbar_wait(&tempty[bb], pb ^ 1, abort_flag, A.err)) break;
                 tc::fence_after_sync();
-                const uint32_t k_addr = tc::smem_u32(sm + SC_ST + s * 65536);
-                const uint32_t v_addr = k_addr + 32768;
                 const uint32_t d0 = tmem + bb * 256;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;  // 128-row operand
-                    const uint32_t bo = (k >> 2) * 8192 + (k & 3) * 32;   // 64-row operand
-                    tc::mma_bf16(d0 + 0, tc::sdesc_sw128(k_addr + ao, 16, 1024),
-                                 tc::sdesc_sw128(q_addr + bo, 16, 1024), id64, k > 0);
-                }
+                const uint32_t k_addr = ring + sk * 32768;
+                // S^T = K Q_h^T -> columns [0, 64)
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;
                     const uint32_t bo = (k >> 2) * 8192 + (k & 3) * 32;
+                    tc::mma_bf16(d0, tc::sdesc_sw128(k_addr + ao, 16, 1024),
+                                 tc::sdesc_sw128(q_addr + bo, 16, 1024), id64, k > 0);
+                }
+                tc::mma_commit(&rempty[sk]);
+                if (!tc::mbar_wait(&rfull[sv], (cv / SC_SLOTS) & 1, abort_flag, A.err)) break;
+                tc::fence_after_sync();
+                const uint32_t v_addr = ring + sv * 32768;
+                // [V U_h^T | V L_h] -> columns [64, 256). Rows 64..127 of L_h^T are zero for
+                // k < 64, so the first K-block only multiplies [U ; L^T rows 0..63] (N = 128).
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t ao = (k & 3) * 32;
                     tc::mma_bf16(d0 + 64, tc::sdesc_sw128(v_addr + ao, 16, 1024),
-                                 tc::sdesc_sw128(u_addr + bo, 16, 1024), id64, k > 0);
+                                 tc::sdesc_sw128(ul_addr + (k & 3) * 32, 16, 1024), id128, k > 0);
                 }
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {  // columns j < 64 of L^T v: all of k
-                    const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;
-                    const uint32_t bo = (k >> 2) * 16384 + (k & 3) * 32;
-                    tc::mma_bf16(d0 + 128, tc::sdesc_sw128(v_addr + ao, 16, 1024),
-                                 tc::sdesc_sw128(lt_addr + bo, 16, 1024), id64, k > 0);
-                }
-#pragma unroll
-                for (int k = 4; k < 8; ++k) {  // columns j >= 64: L[k][j] = 0 for k < 64
-                    const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;
-                    const uint32_t bo = (k >> 2) * 16384 + 8192 + (k & 3) * 32;
+                {
+                    const uint32_t ao = 16384;  // k = 4: first step of the second K-block
+                    tc::mma_bf16(d0 + 64, tc::sdesc_sw128(v_addr + ao, 16, 1024),
+                                 tc::sdesc_sw128(ul_addr + SC_UL_BLK, 16, 1024), id128, 1);
                     tc::mma_bf16(d0 + 192, tc::sdesc_sw128(v_addr + ao, 16, 1024),
-                                 tc::sdesc_sw128(lt_addr + bo, 16, 1024), id64, k > 4);
+                                 tc::sdesc_sw128(ul_addr + SC_UL_BLK + 16384, 16, 1024), id64, 0);
                 }
-                tc::mma_commit(&empty[s]);
+#pragma unroll
+                for (int k = 5; k < 8; ++k) {
+                    const uint32_t ao = 16384 + (k & 3) * 32;
+                    tc::mma_bf16(d0 + 64, tc::sdesc_sw128(v_addr + ao, 16, 1024),
+                                 tc::sdesc_sw128(ul_addr + SC_UL_BLK + (k & 3) * 32, 16, 1024),
+                                 id192, 1);
+                }
+                tc::mma_commit(&rempty[sv]);
                 tc::mma_commit(&tfull[bb]);
             }
         }
@@ -299,7 +314,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
                 const float a = tc::ex2_approx(fmaf(s0[q], A.k1, c.x));
                 const float x = fmaxf(fmaf(-2.f, x0[q], nv + c.y), 1e-30f);
                 const float dd = one_eps - a;
-                acc = fmaf(c.z, a * x * tc::rsqrt_approx(x * dd * dd), acc);
+                acc = fmaf(c.z * a * x, tc::rsqrt_approx(x * (dd * dd)), acc);
             }
 #pragma unroll
             for (int q = 0; q < 32; ++q) {
@@ -307,7 +322,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
                 const float a = tc::ex2_approx(fmaf(s1[q], A.k1, c.x));
                 const float x = fmaxf(fmaf(-2.f, x1[q], nv + c.y), 1e-30f);
                 const float dd = one_eps - a;
-                acc = fmaf(c.z, a * x * tc::rsqrt_approx(x * dd * dd), acc);
+                acc = fmaf(c.z * a * x, tc::rsqrt_approx(x * (dd * dd)), acc);
             }
             const int tok = (t_begin + i) * 128 + row;
             if (tok < A.n) out[tok] = (tok >= A.sink && tok < A.n - A.w) ? acc : 0.f;
@@ -334,6 +349,7 @@ constexpr uint32_t AT_Q = 0, AT_P = 65536, AT_RING = 131072;  // Q0,Q1 | P0,P1 |
 constexpr uint32_t AT_BAR = AT_RING + 3 * 32768;
 constexpr size_t AT_SMEM = AT_BAR + 256 + 1024;
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when a row maximum grows by > 2^8
+constexpr float kNoMax = -1e30f;     // running maximum before any visible token
 
 // S_t = Q_t K_i^T for query tile t (K_i = ring item 2i).
 __device__ __forceinline__ bool attn_issue_s(uint32_t base, uint32_t tmem, int t, int i,
@@ -482,7 +498,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         const uint32_t s_col = tmem + lane_off + t * 128;
         const uint32_t o_col = tmem + lane_off + 256 + t * 128;
         uint8_t *P = sm + AT_P + t * 32768;
-        float m_used = -INFINITY, l = 0.f;
+        float m_used = kNoMax, l = 0.f;  // finite sentinel: exp2(x - kNoMax) = 0
         bool ok = true;
         for (int i = 0; i < ntl; ++i) {
             if (!tc::mbar_wait(&s_full[t], i & 1, abort_flag, A.err)) {
@@ -498,25 +514,32 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             tc::mbar_arrive(&s_free[t]);
             const int nv_tile = vend - (t0 + i * 128);  // valid columns of this row in the tile
             float mt = -INFINITY;
+            if (nv_tile >= 128) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float x = (c * 32 + e < nv_tile) ? s[c][e] * A.k1 : -INFINITY;
-                    s[c][e] = x;
-                    mt = fmaxf(mt, x);
-                }
-            const float m_new = fmaxf(m_used, mt);
+                    for (int e = 0; e < 32; ++e) mt = fmaxf(mt, s[c][e]);
+            } else {  // the tile crosses the end of the split, the unit or a causal window row
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        if (c * 32 + e >= nv_tile) s[c][e] = -INFINITY;
+                        mt = fmaxf(mt, s[c][e]);
+                    }
+            }
+            const float m_new = fmaxf(m_used, mt * A.k1);
             // O is rescaled only when the row maximum grew by more than 2^8 (and O holds data)
             const bool rescale = m_new > m_used + kRescaleLog2;
             const float f = (rescale && i > 0) ? tc::ex2_approx(m_used - m_new) : 1.f;
             if (rescale) m_used = m_new;
+            const float neg_m = -m_used;
             float lsum = 0.f;
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float p = (m_used == -INFINITY) ? 0.f : tc::ex2_approx(s[c][e] - m_used);
+                    const float p = tc::ex2_approx(fmaf(s[c][e], A.k1, neg_m));
                     s[c][e] = p;
                     lsum += p;
                 }
