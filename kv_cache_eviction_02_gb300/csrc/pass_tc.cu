@@ -472,18 +472,22 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                                    A.err) &&
                       attn_issue_s(base, tmem, 1, 0, rfull, rempty, s_full, s_free, abort_flag,
                                    A.err);
+            // S_t(i+1) only needs the softmax group to have copied S_t(i) into registers, so it
+            // is issued before P_t(i) V_i: the tensor pipe computes the next scores while the
+            // group is still working on this tile's exponentials.
             for (int i = 0; ok && i < ntl; ++i) {
-                ok = attn_issue_pv(base, tmem, 0, i, rfull, rempty, p_full, o_done, abort_flag,
-                                   A.err);
-                if (ok && i + 1 < ntl)
+                if (i + 1 < ntl)
                     ok = attn_issue_s(base, tmem, 0, i + 1, rfull, rempty, s_full, s_free,
                                       abort_flag, A.err);
                 if (ok)
-                    ok = attn_issue_pv(base, tmem, 1, i, rfull, rempty, p_full, o_done,
+                    ok = attn_issue_pv(base, tmem, 0, i, rfull, rempty, p_full, o_done,
                                        abort_flag, A.err);
                 if (ok && i + 1 < ntl)
                     ok = attn_issue_s(base, tmem, 1, i + 1, rfull, rempty, s_full, s_free,
                                       abort_flag, A.err);
+                if (ok)
+                    ok = attn_issue_pv(base, tmem, 1, i, rfull, rempty, p_full, o_done,
+                                       abort_flag, A.err);
             }
         }
     } else {  // ---- softmax groups: warps 2-5 own query tile 0, warps 6-9 tile 1 ----
