@@ -73,7 +73,19 @@ static int balance_parts(long items, long tiles, int max_parts) {
 void tc_plan(LorekvDims *D) {
     const long ntiles = (D->n + 127) / 128;
     const long nqp = (D->Qu + 255) / 256;
-    const int ns = balance_parts((long)D->units * nqp, ntiles, 64);
+    // Each split writes and the combine re-reads a 256-query partial (o, m, l: ~128 KB), about
+    // the DRAM traffic of two 128-token K/V tiles; count that next to the per-SM tile load.
+    const long items = (long)D->units * nqp;
+    int ns = 1;
+    long best = -1;
+    for (int p = 1; p <= 64 && p <= ntiles; ++p) {
+        const long waves = (items * p + kSms - 1) / kSms;
+        const long cost = waves * ((ntiles + p - 1) / p) + 2 * ((items * p + kSms - 1) / kSms);
+        if (best < 0 || cost < best) {
+            best = cost;
+            ns = p;
+        }
+    }
     const long per = (ntiles + ns - 1) / ns;
     D->split_len = (int)(per * 128);
     D->nsplit = (int)((D->n + D->split_len - 1) / D->split_len);
@@ -185,10 +197,13 @@ __global__ void __launch_bounds__(kScThreads, 1)
         tc::tmem_alloc(tmem_slot, 512);
         tc::fence_before_sync();
     }
-    if (threadIdx.x >= 64 && threadIdx.x < 128) {
+    if (threadIdx.x >= 64 && threadIdx.x < 96) {  // query pairs (2t, 2t+1)
         const int t = threadIdx.x - 64;
-        qc[t] = (t < A.nq) ? A.qconst[(size_t)unit * A.Qu + j * A.nq + t]
-                           : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+        float4 c0 = make_float4(-INFINITY, 0.f, 0.f, 0.f), c1 = c0;
+        if (2 * t < A.nq) c0 = A.qconst[(size_t)unit * A.Qu + j * A.nq + 2 * t];
+        if (2 * t + 1 < A.nq) c1 = A.qconst[(size_t)unit * A.Qu + j * A.nq + 2 * t + 1];
+        qc[t] = make_float4(c0.x, c1.x, c0.y, c1.y);       // -lse2 pair, c pair
+        qc[32 + t] = make_float4(c0.z, c1.z, 0.f, 0.f);    // weight pair
     }
     __syncthreads();
     tc::fence_after_sync();
@@ -307,23 +322,34 @@ __global__ void __launch_bounds__(kScThreads, 1)
             tc::tmem_wait_ld();
             tc::fence_before_sync();
             tc::mbar_arrive(&tempty[wg]);
-            float acc = 0.f;
+            // e = w a sqrt(x) / (1 - a + eps) for two queries per packed FP32 instruction
+            const uint64_t k1_2 = tc::pk2(A.k1, A.k1), m2_2 = tc::pk2(-2.f, -2.f);
+            const uint64_t one_2 = tc::pk2(one_eps, one_eps), neg1_2 = tc::pk2(-1.f, -1.f);
+            const uint64_t nv_2 = tc::pk2(nv, nv);
+            uint64_t acc2 = tc::pk2(0.f, 0.f);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                const float4 c = qc[q];
-                const float a = tc::ex2_approx(fmaf(s0[q], A.k1, c.x));
-                const float x = fmaxf(fmaf(-2.f, x0[q], nv + c.y), 1e-30f);
-                const float dd = one_eps - a;
-                acc = fmaf(c.z * a * x, tc::rsqrt_approx(x * (dd * dd)), acc);
+            for (int p = 0; p < 32; ++p) {
+                const float4 ca = qc[p];
+                const float4 cw = qc[32 + p];
+                const float sa = (p < 16) ? s0[2 * p] : s1[2 * p - 32];
+                const float sb = (p < 16) ? s0[2 * p + 1] : s1[2 * p - 31];
+                const float xa = (p < 16) ? x0[2 * p] : x1[2 * p - 32];
+                const float xb = (p < 16) ? x0[2 * p + 1] : x1[2 * p - 31];
+                float ea, eb;
+                tc::upk2(tc::fma2(tc::pk2(sa, sb), k1_2, tc::pk2(ca.x, ca.y)), ea, eb);
+                const uint64_t a2 = tc::pk2(tc::ex2_approx(ea), tc::ex2_approx(eb));
+                float ya, yb;
+                tc::upk2(tc::fma2(tc::pk2(xa, xb), m2_2, tc::add2(nv_2, tc::pk2(ca.z, ca.w))), ya, yb);
+                const uint64_t x2 = tc::pk2(fmaxf(ya, 1e-30f), fmaxf(yb, 1e-30f));
+                const uint64_t dd2 = tc::fma2(a2, neg1_2, one_2);
+                float za, zb;
+                tc::upk2(tc::mul2(tc::mul2(x2, dd2), dd2), za, zb);
+                const uint64_t r2 = tc::pk2(tc::rsqrt_approx(za), tc::rsqrt_approx(zb));
+                acc2 = tc::fma2(tc::mul2(tc::mul2(tc::pk2(cw.x, cw.y), a2), x2), r2, acc2);
             }
-#pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                const float4 c = qc[32 + q];
-                const float a = tc::ex2_approx(fmaf(s1[q], A.k1, c.x));
-                const float x = fmaxf(fmaf(-2.f, x1[q], nv + c.y), 1e-30f);
-                const float dd = one_eps - a;
-                acc = fmaf(c.z * a * x, tc::rsqrt_approx(x * (dd * dd)), acc);
-            }
+            float acca, accb;
+            tc::upk2(acc2, acca, accb);
+            const float acc = acca + accb;
             const int tok = (t_begin + i) * 128 + row;
             if (tok < A.n) out[tok] = (tok >= A.sink && tok < A.n - A.w) ? acc : 0.f;
         }
@@ -344,7 +370,7 @@ struct AttnArgs {
     unsigned *err;
 };
 
-constexpr int kAtThreads = 320;
+constexpr int kAtThreads = 384;  // TMA, 2 MMA issuers, idle, 2 softmax groups
 constexpr uint32_t AT_Q = 0, AT_P = 65536, AT_RING = 131072;  // Q0,Q1 | P0,P1 | 3 x 32 KB ring
 constexpr uint32_t AT_BAR = AT_RING + 3 * 32768;
 constexpr size_t AT_SMEM = AT_BAR + 256 + 1024;
@@ -358,7 +384,7 @@ __device__ __forceinline__ bool attn_issue_s(uint32_t base, uint32_t tmem, int t
                                              unsigned *err) {
     constexpr uint32_t id_s = tc::idesc_bf16(128, 128, 0);
     const int c = 2 * i, slot = c % 3;
-    if (t == 0 && !tc::mbar_wait(&rfull[slot], (c / 3) & 1, abort_flag, err)) return false;
+    if (!tc::mbar_wait(&rfull[slot], (c / 3) & 1, abort_flag, err)) return false;
     if (!tc::mbar_wait(&s_free[t], (i & 1) ^ 1, abort_flag, err)) return false;
     tc::fence_after_sync();
     const uint32_t q_addr = base + AT_Q + t * 32768;
@@ -370,7 +396,7 @@ __device__ __forceinline__ bool attn_issue_s(uint32_t base, uint32_t tmem, int t
                      tc::sdesc_sw128(k_addr + o, 16, 1024), id_s, k > 0);
     }
     tc::mma_commit(&s_full[t]);
-    if (t == 1) tc::mma_commit(&rempty[slot]);
+    tc::mma_commit(&rempty[slot]);
     return true;
 }
 
@@ -381,7 +407,7 @@ __device__ __forceinline__ bool attn_issue_pv(uint32_t base, uint32_t tmem, int 
                                               unsigned *err) {
     constexpr uint32_t id_pv = tc::idesc_bf16(128, 128, 1);
     const int c = 2 * i + 1, slot = c % 3;
-    if (t == 0 && !tc::mbar_wait(&rfull[slot], (c / 3) & 1, abort_flag, err)) return false;
+    if (!tc::mbar_wait(&rfull[slot], (c / 3) & 1, abort_flag, err)) return false;
     if (!tc::mbar_wait(&p_full[t], i & 1, abort_flag, err)) return false;
     tc::fence_after_sync();
     const uint32_t p_addr = base + AT_P + t * 32768;
@@ -395,11 +421,11 @@ __device__ __forceinline__ bool attn_issue_pv(uint32_t base, uint32_t tmem, int 
                      (i > 0 || k > 0) ? 1u : 0u);
     }
     tc::mma_commit(&o_done[t]);
-    if (t == 1) tc::mma_commit(&rempty[slot]);
+    tc::mma_commit(&rempty[slot]);
     return true;
 }
 
-// 10 warps: three share a sub-partition's 16K registers, so at most 168 registers a thread.
+// 12 warps: three share a sub-partition's 16K registers, so at most 168 registers a thread.
 __global__ void __launch_bounds__(kAtThreads, 1)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
@@ -426,7 +452,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         tc::mbar_init(q_full, 1);
         for (int s = 0; s < 3; ++s) {
             tc::mbar_init(&rfull[s], 1);
-            tc::mbar_init(&rempty[s], 1);
+            tc::mbar_init(&rempty[s], 2);  // released by both query tiles' MMA issuers
         }
         for (int t = 0; t < 2; ++t) {
             tc::mbar_init(&s_full[t], 1);
@@ -465,33 +491,26 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 tc::tma_load_2d(dst + 16384, map, 64, row, &rfull[slot]);
             }
         }
-    } else if (warp == 1) {
-        if (lane == 0 && tc::mbar_wait(q_full, 0, abort_flag, A.err)) {  // ---- MMA issuer ----
+    } else if (warp == 1 || warp == 2) {
+        // ---- MMA issuers, one per query tile, so the two tiles never wait on each other. S_t(i+1)
+        // only needs the softmax group to have copied S_t(i) into registers, so it is issued
+        // before P_t(i) V_i: the tensor pipe computes the next scores during the exponentials.
+        const int t = warp - 1;
+        if (lane == 0 && tc::mbar_wait(q_full, 0, abort_flag, A.err)) {
             const uint32_t base = tc::smem_u32(sm);
-            bool ok = attn_issue_s(base, tmem, 0, 0, rfull, rempty, s_full, s_free, abort_flag,
-                                   A.err) &&
-                      attn_issue_s(base, tmem, 1, 0, rfull, rempty, s_full, s_free, abort_flag,
+            bool ok = attn_issue_s(base, tmem, t, 0, rfull, rempty, s_full, s_free, abort_flag,
                                    A.err);
-            // S_t(i+1) only needs the softmax group to have copied S_t(i) into registers, so it
-            // is issued before P_t(i) V_i: the tensor pipe computes the next scores while the
-            // group is still working on this tile's exponentials.
             for (int i = 0; ok && i < ntl; ++i) {
                 if (i + 1 < ntl)
-                    ok = attn_issue_s(base, tmem, 0, i + 1, rfull, rempty, s_full, s_free,
+                    ok = attn_issue_s(base, tmem, t, i + 1, rfull, rempty, s_full, s_free,
                                       abort_flag, A.err);
                 if (ok)
-                    ok = attn_issue_pv(base, tmem, 0, i, rfull, rempty, p_full, o_done,
-                                       abort_flag, A.err);
-                if (ok && i + 1 < ntl)
-                    ok = attn_issue_s(base, tmem, 1, i + 1, rfull, rempty, s_full, s_free,
-                                      abort_flag, A.err);
-                if (ok)
-                    ok = attn_issue_pv(base, tmem, 1, i, rfull, rempty, p_full, o_done,
+                    ok = attn_issue_pv(base, tmem, t, i, rfull, rempty, p_full, o_done,
                                        abort_flag, A.err);
             }
         }
-    } else {  // ---- softmax groups: warps 2-5 own query tile 0, warps 6-9 tile 1 ----
-        const int t = (warp - 2) >> 2, lg = warp & 3;
+    } else if (warp >= 4) {  // ---- softmax groups: warps 4-7 own query tile 0, 8-11 tile 1 ----
+        const int t = (warp - 4) >> 2, lg = warp & 3;
         const int r = lg * 32 + lane;
         const int qi = qbase + 128 * t + r;
         const bool valid_row = qi < A.Qu;
