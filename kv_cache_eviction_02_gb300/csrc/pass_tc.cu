@@ -147,13 +147,23 @@ struct ScoresArgs {
 };
 
 constexpr int kScThreads = 320;
-// Shared memory: Q_h (2 x 8 KB K-blocks) | [U_h ; L_h^T] merged B operand (2 K-blocks of 24 KB:
-// 64 rows of U then 128 rows of L^T) | ring of 5 x 32 KB TMA boxes (K_i, V_i, K_i+1, ...) |
-// per-query constants | barriers.
-constexpr uint32_t SC_Q = 0, SC_UL = 16384, SC_UL_BLK = 24576, SC_RING = 65536;
-constexpr int SC_SLOTS = 5;
-constexpr uint32_t SC_QC = SC_RING + SC_SLOTS * 32768;
-constexpr uint32_t SC_BAR = SC_QC + 64 * 16;
+// One CTA scores two query heads of a unit over a token range: every staged K/V tile serves both,
+// and the heads' operands are interleaved so that each MMA is wide (N = 128 or 256).
+// Shared memory:
+//   Q    2 K-blocks x 16 KB: rows [Q_h0 (64) | Q_h1 (64)]           -> B of S = K [Q_h0;Q_h1]^T
+//   B2   2 K-blocks x 48 KB: rows [U_h0 | U_h1 | Lt_h0 0-63 | Lt_h1 0-63 | Lt_h0 64-127 |
+//        Lt_h1 64-127] (64 rows each; Lt_h = L_h^T)                  -> B of V B2^T
+//   ring 3 x 32 KB TMA boxes (K_i, V_i, K_i+1, ...) | per-query constants | barriers.
+// TMEM (512 columns, one buffer): S_h0 | S_h1 | VU_h0 | VU_h1 | VLa_h0 | VLa_h1 | VLb_h0 | VLb_h1,
+// 64 columns each (VLa/VLb = columns 0-63 / 64-127 of V L_h). Rows 64..127 of L_h^T are zero for
+// k < 64, so VLb only takes the second K-block.
+constexpr int SC_HPC = 2;                          // query heads per CTA
+constexpr uint32_t SC_Q = 0, SC_B2 = 32768, SC_B2_BLK = 49152;
+constexpr uint32_t SC_RING = SC_B2 + 2 * SC_B2_BLK;        // 128 KB
+constexpr int SC_SLOTS = 3;
+constexpr uint32_t SC_QC = SC_RING + SC_SLOTS * 32768;     // [2][32] float4 {-lse2, c} pairs
+constexpr uint32_t SC_QW = SC_QC + SC_HPC * 32 * 16;       // [2][32] float2 weight pairs
+constexpr uint32_t SC_BAR = SC_QW + SC_HPC * 32 * 8;
 constexpr size_t SC_SMEM = SC_BAR + 256 + 1024;
 
 __global__ void __launch_bounds__(kScThreads, 1)
@@ -164,21 +174,25 @@ __global__ void __launch_bounds__(kScThreads, 1)
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int npairs = (A.g + SC_HPC - 1) / SC_HPC;
     const int b = blockIdx.x;
-    const int j = b % A.g;
-    const int range = (b / A.g) % A.nranges;
-    const int unit = b / (A.g * A.nranges);
+    const int hp = b % npairs;
+    const int range = (b / npairs) % A.nranges;
+    const int unit = b / (npairs * A.nranges);
+    const int j0 = hp * SC_HPC;
+    const int nh = min(SC_HPC, A.g - j0);         // heads of this CTA (1 for an odd last pair)
     const int t_begin = range * A.tpr;
     const int ntl = min(A.ntiles, t_begin + A.tpr) - t_begin;
     if (ntl <= 0) return;
-    const int kh = unit % A.Hkv, l = (unit / A.Hkv) % A.L, h = kh * A.g + j;
+    const int kh = unit % A.Hkv, l = (unit / A.Hkv) % A.L;
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SC_BAR);
     uint64_t *ops_full = bars + 0, *rfull = bars + 1, *rempty = bars + 1 + SC_SLOTS,
-             *tfull = bars + 1 + 2 * SC_SLOTS, *tempty = bars + 3 + 2 * SC_SLOTS;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 5 + 2 * SC_SLOTS);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 6 + 2 * SC_SLOTS);
+             *tfull = bars + 1 + 2 * SC_SLOTS, *tempty = bars + 2 + 2 * SC_SLOTS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 + 2 * SC_SLOTS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 4 + 2 * SC_SLOTS);
     float4 *qc = reinterpret_cast<float4 *>(sm + SC_QC);
+    float2 *qw = reinterpret_cast<float2 *>(sm + SC_QW);
 
     if (threadIdx.x == 0) {
         tc::mbar_init(ops_full, 1);
@@ -186,10 +200,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
             tc::mbar_init(&rfull[s], 1);
             tc::mbar_init(&rempty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            tc::mbar_init(&tfull[s], 1);
-            tc::mbar_init(&tempty[s], 128);
-        }
+        tc::mbar_init(tfull, 1);
+        tc::mbar_init(tempty, 128 * nh);  // every epilogue thread has read the tile
         *abort_flag = 0;
         tc::mbar_fence_init();
     }
@@ -197,13 +209,16 @@ __global__ void __launch_bounds__(kScThreads, 1)
         tc::tmem_alloc(tmem_slot, 512);
         tc::fence_before_sync();
     }
-    if (threadIdx.x >= 64 && threadIdx.x < 96) {  // query pairs (2t, 2t+1)
-        const int t = threadIdx.x - 64;
+    if (threadIdx.x >= 64 && threadIdx.x < 64 + 32 * SC_HPC) {  // query pairs (2t, 2t+1)
+        const int hh = (threadIdx.x - 64) >> 5, t = (threadIdx.x - 64) & 31;
         float4 c0 = make_float4(-INFINITY, 0.f, 0.f, 0.f), c1 = c0;
-        if (2 * t < A.nq) c0 = A.qconst[(size_t)unit * A.Qu + j * A.nq + 2 * t];
-        if (2 * t + 1 < A.nq) c1 = A.qconst[(size_t)unit * A.Qu + j * A.nq + 2 * t + 1];
-        qc[t] = make_float4(c0.x, c1.x, c0.y, c1.y);       // -lse2 pair, c pair
-        qc[32 + t] = make_float4(c0.z, c1.z, 0.f, 0.f);    // weight pair
+        if (hh < nh) {
+            const size_t row0 = (size_t)unit * A.Qu + (size_t)(j0 + hh) * A.nq;
+            if (2 * t < A.nq) c0 = A.qconst[row0 + 2 * t];
+            if (2 * t + 1 < A.nq) c1 = A.qconst[row0 + 2 * t + 1];
+        }
+        qc[hh * 32 + t] = make_float4(c0.x, c1.x, c0.y, c1.y);  // -lse2 pair, c pair
+        qw[hh * 32 + t] = make_float2(c0.z, c1.z);              // weight pair
     }
     __syncthreads();
     tc::fence_after_sync();
@@ -211,14 +226,18 @@ __global__ void __launch_bounds__(kScThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {  // ---- TMA producer ----
-            const int qrow = unit * A.Qu + j * A.nq;
-            const int lrow = (l * A.Hq + h) * 128;
-            tc::mbar_expect_tx(ops_full, 65536);
-            for (int kb = 0; kb < 2; ++kb) {
-                tc::tma_load_2d(sm + SC_Q + kb * 8192, &tm_q, 64 * kb, qrow, ops_full);
-                tc::tma_load_2d(sm + SC_UL + kb * SC_UL_BLK, &tm_u, 64 * kb, qrow, ops_full);
-                tc::tma_load_2d(sm + SC_UL + kb * SC_UL_BLK + 8192, &tm_lt, 64 * kb, lrow,
-                                ops_full);
+            tc::mbar_expect_tx(ops_full, 65536u * nh);
+            for (int hh = 0; hh < nh; ++hh) {
+                const int qrow = unit * A.Qu + (j0 + hh) * A.nq;
+                const int lrow = (l * A.Hq + kh * A.g + j0 + hh) * 128;
+                for (int kb = 0; kb < 2; ++kb) {
+                    uint8_t *b2 = sm + SC_B2 + kb * SC_B2_BLK + hh * 8192;
+                    tc::tma_load_2d(sm + SC_Q + kb * 16384 + hh * 8192, &tm_q, 64 * kb, qrow,
+                                    ops_full);
+                    tc::tma_load_2d(b2, &tm_u, 64 * kb, qrow, ops_full);
+                    tc::tma_load_2d(b2 + 16384, &tm_lt, 64 * kb, lrow, ops_full);
+                    tc::tma_load_2d(b2 + 32768, &tm_lt, 64 * kb, lrow + 64, ops_full);
+                }
             }
             for (int c = 0; c < 2 * ntl; ++c) {
                 const int slot = c % SC_SLOTS;
@@ -235,102 +254,100 @@ __global__ void __launch_bounds__(kScThreads, 1)
     } else if (warp == 1) {
         if (lane == 0 && tc::mbar_wait(ops_full, 0, abort_flag, A.err)) {  // ---- MMA issuer ----
             tc::fence_after_sync();
-            const uint32_t q_addr = tc::smem_u32(sm + SC_Q);
-            const uint32_t ul_addr = tc::smem_u32(sm + SC_UL);
             const uint32_t ring = tc::smem_u32(sm + SC_RING);
-            constexpr uint32_t id64 = tc::idesc_bf16(128, 64, 0);
+            const uint32_t q_addr = tc::smem_u32(sm + SC_Q);
+            const uint32_t b2_addr = tc::smem_u32(sm + SC_B2);
             constexpr uint32_t id128 = tc::idesc_bf16(128, 128, 0);
-            constexpr uint32_t id192 = tc::idesc_bf16(128, 192, 0);
+            constexpr uint32_t id256 = tc::idesc_bf16(128, 256, 0);
             for (int i = 0; i < ntl; ++i) {
-                const int bb = i & 1;
-                const uint32_t pb = (i >> 1) & 1;
                 const int ck = 2 * i, cv = 2 * i + 1;
                 const int sk = ck % SC_SLOTS, sv = cv % SC_SLOTS;
                 if (!tc::mbar_wait(&rfull[sk], (ck / SC_SLOTS) & 1, abort_flag, A.err)) break;
-                if (!tc::mbar_wait(&tempty[bb], pb ^ 1, abort_flag, A.err)) break;
+                if (!tc::mbar_wait(tempty, (i & 1) ^ 1, abort_flag, A.err)) break;
                 tc::fence_after_sync();
-                const uint32_t d0 = tmem + bb * 256;
                 const uint32_t k_addr = ring + sk * 32768;
-                // S^T = K Q_h^T -> columns [0, 64)
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;
-                    const uint32_t bo = (k >> 2) * 8192 + (k & 3) * 32;
-                    tc::mma_bf16(d0, tc::sdesc_sw128(k_addr + ao, 16, 1024),
-                                 tc::sdesc_sw128(q_addr + bo, 16, 1024), id64, k > 0);
+                for (int k = 0; k < 8; ++k) {  // [S_h0 | S_h1] = K [Q_h0 ; Q_h1]^T
+                    const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
+                    tc::mma_bf16(tmem, tc::sdesc_sw128(k_addr + o, 16, 1024),
+                                 tc::sdesc_sw128(q_addr + o, 16, 1024), id128, k > 0);
                 }
                 tc::mma_commit(&rempty[sk]);
                 if (!tc::mbar_wait(&rfull[sv], (cv / SC_SLOTS) & 1, abort_flag, A.err)) break;
                 tc::fence_after_sync();
                 const uint32_t v_addr = ring + sv * 32768;
-                // [V U_h^T | V L_h] -> columns [64, 256). Rows 64..127 of L_h^T are zero for
-                // k < 64, so the first K-block only multiplies [U ; L^T rows 0..63] (N = 128).
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t ao = (k & 3) * 32;
-                    tc::mma_bf16(d0 + 64, tc::sdesc_sw128(v_addr + ao, 16, 1024),
-                                 tc::sdesc_sw128(ul_addr + (k & 3) * 32, 16, 1024), id128, k > 0);
-                }
-                {
-                    const uint32_t ao = 16384;  // k = 4: first step of the second K-block
-                    tc::mma_bf16(d0 + 64, tc::sdesc_sw128(v_addr + ao, 16, 1024),
-                                 tc::sdesc_sw128(ul_addr + SC_UL_BLK, 16, 1024), id128, 1);
-                    tc::mma_bf16(d0 + 192, tc::sdesc_sw128(v_addr + ao, 16, 1024),
-                                 tc::sdesc_sw128(ul_addr + SC_UL_BLK + 16384, 16, 1024), id64, 0);
+                for (int k = 0; k < 8; ++k) {  // [VU_h0 | VU_h1 | VLa_h0 | VLa_h1]
+                    const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;
+                    const uint32_t bo = (k >> 2) * SC_B2_BLK + (k & 3) * 32;
+                    tc::mma_bf16(tmem + 128, tc::sdesc_sw128(v_addr + ao, 16, 1024),
+                                 tc::sdesc_sw128(b2_addr + bo, 16, 1024), id256, k > 0);
                 }
 #pragma unroll
-                for (int k = 5; k < 8; ++k) {
+                for (int k = 4; k < 8; ++k) {  // [VLb_h0 | VLb_h1]: second K-block only
                     const uint32_t ao = 16384 + (k & 3) * 32;
-                    tc::mma_bf16(d0 + 64, tc::sdesc_sw128(v_addr + ao, 16, 1024),
-                                 tc::sdesc_sw128(ul_addr + SC_UL_BLK + (k & 3) * 32, 16, 1024),
-                                 id192, 1);
+                    const uint32_t bo = SC_B2_BLK + 32768 + (k & 3) * 32;
+                    tc::mma_bf16(tmem + 384, tc::sdesc_sw128(v_addr + ao, 16, 1024),
+                                 tc::sdesc_sw128(b2_addr + bo, 16, 1024), id128, k > 4);
                 }
                 tc::mma_commit(&rempty[sv]);
-                tc::mma_commit(&tfull[bb]);
+                tc::mma_commit(tfull);
             }
         }
-    } else {  // ---- epilogue: two 4-warp groups, alternate tiles ----
-        const int wg = (warp - 2) >> 2, lg = warp & 3;
+    } else if ((warp - 2) >> 2 < nh) {
+        // ---- epilogue: group hh (warps 2-5 -> head 0, 6-9 -> head 1) ----
+        const int hh = (warp - 2) >> 2, lg = warp & 3;
         const int row = lg * 32 + lane;
         const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
-        float *out = A.part_s + ((size_t)unit * A.g + j) * A.n;
+        float *out = A.part_s + ((size_t)unit * A.g + j0 + hh) * A.n;
         const float one_eps = 1.f + A.eps;
-        for (int i = wg; i < ntl; i += 2) {
-            const uint32_t ph = (i >> 1) & 1;
-            if (!tc::mbar_wait(&tfull[wg], ph, abort_flag, A.err)) break;
+        const float4 *qch = qc + hh * 32;
+        const float2 *qwh = qw + hh * 32;
+        for (int i = 0; i < ntl; ++i) {
+            if (!tc::mbar_wait(tfull, i & 1, abort_flag, A.err)) break;
             tc::fence_after_sync();
-            const uint32_t tb = tmem + lane_off + wg * 256;
-            float nv = 0.f;
+            const uint32_t tb = tmem + lane_off;
+            float nv;
             {
-                float y0[32], y1[32];
-                tc::tmem_ld32(tb + 128, y0);
-                tc::tmem_ld32(tb + 160, y1);
+                float y0[32], y1[32], np[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) np[k] = 0.f;
+                tc::tmem_ld32(tb + 256 + 64 * hh, y0);
+                tc::tmem_ld32(tb + 288 + 64 * hh, y1);
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < 32; ++c) nv = fmaf(y0[c], y0[c], fmaf(y1[c], y1[c], nv));
-                tc::tmem_ld32(tb + 192, y0);
-                tc::tmem_ld32(tb + 224, y1);
+                for (int c = 0; c < 32; ++c) {
+                    np[c & 7] = fmaf(y0[c], y0[c], np[c & 7]);
+                    np[c & 7] = fmaf(y1[c], y1[c], np[c & 7]);
+                }
+                tc::tmem_ld32(tb + 384 + 64 * hh, y0);
+                tc::tmem_ld32(tb + 416 + 64 * hh, y1);
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < 32; ++c) nv = fmaf(y0[c], y0[c], fmaf(y1[c], y1[c], nv));
+                for (int c = 0; c < 32; ++c) {
+                    np[c & 7] = fmaf(y0[c], y0[c], np[c & 7]);
+                    np[c & 7] = fmaf(y1[c], y1[c], np[c & 7]);
+                }
+                nv = ((np[0] + np[1]) + (np[2] + np[3])) + ((np[4] + np[5]) + (np[6] + np[7]));
             }
             float s0[32], s1[32], x0[32], x1[32];
-            tc::tmem_ld32(tb + 0, s0);
-            tc::tmem_ld32(tb + 32, s1);
-            tc::tmem_ld32(tb + 64, x0);
-            tc::tmem_ld32(tb + 96, x1);
+            tc::tmem_ld32(tb + 64 * hh, s0);
+            tc::tmem_ld32(tb + 64 * hh + 32, s1);
+            tc::tmem_ld32(tb + 128 + 64 * hh, x0);
+            tc::tmem_ld32(tb + 160 + 64 * hh, x1);
             tc::tmem_wait_ld();
             tc::fence_before_sync();
-            tc::mbar_arrive(&tempty[wg]);
+            tc::mbar_arrive(tempty);
             // e = w a sqrt(x) / (1 - a + eps) for two queries per packed FP32 instruction
             const uint64_t k1_2 = tc::pk2(A.k1, A.k1), m2_2 = tc::pk2(-2.f, -2.f);
             const uint64_t one_2 = tc::pk2(one_eps, one_eps), neg1_2 = tc::pk2(-1.f, -1.f);
             const uint64_t nv_2 = tc::pk2(nv, nv);
-            uint64_t acc2 = tc::pk2(0.f, 0.f);
+            uint64_t acc2[4] = {tc::pk2(0.f, 0.f), tc::pk2(0.f, 0.f), tc::pk2(0.f, 0.f),
+                                tc::pk2(0.f, 0.f)};
 #pragma unroll
             for (int p = 0; p < 32; ++p) {
-                const float4 ca = qc[p];
-                const float4 cw = qc[32 + p];
+                const float4 ca = qch[p];
+                const float2 cw = qwh[p];
                 const float sa = (p < 16) ? s0[2 * p] : s1[2 * p - 32];
                 const float sb = (p < 16) ? s0[2 * p + 1] : s1[2 * p - 31];
                 const float xa = (p < 16) ? x0[2 * p] : x1[2 * p - 32];
@@ -345,11 +362,16 @@ __global__ void __launch_bounds__(kScThreads, 1)
                 float za, zb;
                 tc::upk2(tc::mul2(tc::mul2(x2, dd2), dd2), za, zb);
                 const uint64_t r2 = tc::pk2(tc::rsqrt_approx(za), tc::rsqrt_approx(zb));
-                acc2 = tc::fma2(tc::mul2(tc::mul2(tc::pk2(cw.x, cw.y), a2), x2), r2, acc2);
+                acc2[p & 3] = tc::fma2(tc::mul2(tc::mul2(tc::pk2(cw.x, cw.y), a2), x2), r2,
+                                       acc2[p & 3]);
             }
-            float acca, accb;
-            tc::upk2(acc2, acca, accb);
-            const float acc = acca + accb;
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float acca, accb;
+                tc::upk2(acc2[k], acca, accb);
+                acc += acca + accb;
+            }
             const int tok = (t_begin + i) * 128 + row;
             if (tok < A.n) out[tok] = (tok >= A.sink && tok < A.n - A.w) ? acc : 0.f;
         }
@@ -700,7 +722,7 @@ cudaError_t launch_scores_tc(const LorekvDims &D, const void *K, const void *V, 
         !make_tmap_bf16_2d(&tv, V, 128, rows, 64, 128) ||
         !make_tmap_bf16_2d(&tq, b + W.q16, 128, (uint64_t)rows_q, 64, 64) ||
         !make_tmap_bf16_2d(&tu, b + W.u16, 128, (uint64_t)rows_q, 64, 64) ||
-        !make_tmap_bf16_2d(&tl, lt16, 128, (uint64_t)D.L * D.Hq * 128, 64, 128))
+        !make_tmap_bf16_2d(&tl, lt16, 128, (uint64_t)D.L * D.Hq * 128, 64, 64))
         return cudaErrorInvalidValue;
     ScoresArgs A;
     A.n = D.n;
@@ -713,7 +735,8 @@ cudaError_t launch_scores_tc(const LorekvDims &D, const void *K, const void *V, 
     A.sink = D.sink;
     A.w = D.w;
     A.ntiles = (D.n + 127) / 128;
-    A.nranges = balance_parts((long)D.units * D.g, A.ntiles, 64);
+    const int npairs = (D.g + SC_HPC - 1) / SC_HPC;
+    A.nranges = balance_parts((long)D.units * npairs, A.ntiles, 64);
     A.tpr = (A.ntiles + A.nranges - 1) / A.nranges;
     A.nranges = (A.ntiles + A.tpr - 1) / A.tpr;
     A.eps = D.eps;
@@ -724,7 +747,7 @@ cudaError_t launch_scores_tc(const LorekvDims &D, const void *K, const void *V, 
     cudaError_t e = cudaFuncSetAttribute(scores_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SC_SMEM);
     if (e != cudaSuccess) return e;
-    scores_tc_kernel<<<D.units * A.nranges * D.g, kScThreads, SC_SMEM, st>>>(tk, tv, tq, tu, tl, A);
+    scores_tc_kernel<<<D.units * A.nranges * npairs, kScThreads, SC_SMEM, st>>>(tk, tv, tq, tu, tl, A);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     reduce_heads_kernel<<<dim3((D.n + 255) / 256, D.units), 256, 0, st>>>(
