@@ -393,21 +393,22 @@ struct AttnArgs {
 };
 
 constexpr int kAtThreads = 384;  // TMA, 2 MMA issuers, idle, 2 softmax groups
-constexpr uint32_t AT_Q = 0, AT_P = 65536, AT_RING = 131072;  // Q0,Q1 | P0,P1 | 3 x 32 KB ring
-constexpr uint32_t AT_BAR = AT_RING + 3 * 32768;
+constexpr int AT_SLOTS = 5;
+constexpr uint32_t AT_Q = 0, AT_RING = 65536;  // Q0, Q1 | 5 x 32 KB ring (K_0, V_0, K_1, ...)
+constexpr uint32_t AT_BAR = AT_RING + AT_SLOTS * 32768;
 constexpr size_t AT_SMEM = AT_BAR + 256 + 1024;
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when a row maximum grows by > 2^8
 constexpr float kNoMax = -1e30f;     // running maximum before any visible token
 
-// S_t = Q_t K_i^T for query tile t (K_i = ring item 2i).
+// S_t = Q_t K_i^T for query tile t (K_i = ring item 2i) into TMEM columns [128 t, 128 t + 128).
+// Issued after P_t(i-1) V_(i-1) by the same thread: MMAs execute in issue order, so the product
+// has read P_t (which lives in these columns) before S_t(i) overwrites it.
 __device__ __forceinline__ bool attn_issue_s(uint32_t base, uint32_t tmem, int t, int i,
                                              uint64_t *rfull, uint64_t *rempty, uint64_t *s_full,
-                                             uint64_t *s_free, volatile int *abort_flag,
-                                             unsigned *err) {
+                                             volatile int *abort_flag, unsigned *err) {
     constexpr uint32_t id_s = tc::idesc_bf16(128, 128, 0);
-    const int c = 2 * i, slot = c % 3;
-    if (!tc::mbar_wait(&rfull[slot], (c / 3) & 1, abort_flag, err)) return false;
-    if (!tc::mbar_wait(&s_free[t], (i & 1) ^ 1, abort_flag, err)) return false;
+    const int c = 2 * i, slot = c % AT_SLOTS;
+    if (!tc::mbar_wait(&rfull[slot], (c / AT_SLOTS) & 1, abort_flag, err)) return false;
     tc::fence_after_sync();
     const uint32_t q_addr = base + AT_Q + t * 32768;
     const uint32_t k_addr = base + AT_RING + slot * 32768;
@@ -422,26 +423,23 @@ __device__ __forceinline__ bool attn_issue_s(uint32_t base, uint32_t tmem, int t
     return true;
 }
 
-// O_t += P_t V_i for query tile t (V_i = ring item 2i+1, the MN-major B operand).
+// O_t += P_t V_i for query tile t: P_t is read from TMEM (bf16 pairs in the first 64 columns of
+// S_t, 8 columns per 16 tokens), V_i (ring item 2i+1) is the MN-major B operand.
 __device__ __forceinline__ bool attn_issue_pv(uint32_t base, uint32_t tmem, int t, int i,
                                               uint64_t *rfull, uint64_t *rempty, uint64_t *p_full,
                                               uint64_t *o_done, volatile int *abort_flag,
                                               unsigned *err) {
     constexpr uint32_t id_pv = tc::idesc_bf16(128, 128, 1);
-    const int c = 2 * i + 1, slot = c % 3;
-    if (!tc::mbar_wait(&rfull[slot], (c / 3) & 1, abort_flag, err)) return false;
+    const int c = 2 * i + 1, slot = c % AT_SLOTS;
+    if (!tc::mbar_wait(&rfull[slot], (c / AT_SLOTS) & 1, abort_flag, err)) return false;
     if (!tc::mbar_wait(&p_full[t], i & 1, abort_flag, err)) return false;
     tc::fence_after_sync();
-    const uint32_t p_addr = base + AT_P + t * 32768;
     const uint32_t v_addr = base + AT_RING + slot * 32768;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {  // K = 16 tokens per step
-        const uint32_t po = (k >> 2) * 16384 + (k & 3) * 32;
-        const uint32_t vo = k * 2048;  // 16 tokens x 128 bytes
-        tc::mma_bf16(tmem + 256 + t * 128, tc::sdesc_sw128(p_addr + po, 16, 1024),
-                     tc::sdesc_sw128(v_addr + vo, 16384, 1024), id_pv,
-                     (i > 0 || k > 0) ? 1u : 0u);
-    }
+    for (int k = 0; k < 8; ++k)  // K = 16 tokens per step: 8 TMEM columns of P, 16 rows of V
+        tc::mma_bf16_ts(tmem + 256 + t * 128, tmem + t * 128 + 8 * k,
+                        tc::sdesc_sw128(v_addr + k * 2048, 16384, 1024), id_pv,
+                        (i > 0 || k > 0) ? 1u : 0u);
     tc::mma_commit(&o_done[t]);
     tc::mma_commit(&rempty[slot]);
     return true;
@@ -465,20 +463,20 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     const int qbase = qp * 256;
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + AT_BAR);
-    uint64_t *q_full = bars + 0, *rfull = bars + 1, *rempty = bars + 4, *s_full = bars + 7,
-             *s_free = bars + 9, *p_full = bars + 11, *o_done = bars + 13;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 16);
+    uint64_t *q_full = bars + 0, *rfull = bars + 1, *rempty = bars + 1 + AT_SLOTS,
+             *s_full = bars + 1 + 2 * AT_SLOTS, *p_full = bars + 3 + 2 * AT_SLOTS,
+             *o_done = bars + 5 + 2 * AT_SLOTS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 7 + 2 * AT_SLOTS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 8 + 2 * AT_SLOTS);
 
     if (threadIdx.x == 0) {
         tc::mbar_init(q_full, 1);
-        for (int s = 0; s < 3; ++s) {
+        for (int s = 0; s < AT_SLOTS; ++s) {
             tc::mbar_init(&rfull[s], 1);
             tc::mbar_init(&rempty[s], 2);  // released by both query tiles' MMA issuers
         }
         for (int t = 0; t < 2; ++t) {
             tc::mbar_init(&s_full[t], 1);
-            tc::mbar_init(&s_free[t], 128);
             tc::mbar_init(&p_full[t], 128);
             tc::mbar_init(&o_done[t], 1);
         }
@@ -494,7 +492,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) {  // ---- TMA producer: Q once, then K_i, V_i through a 3-slot ring ----
+        if (lane == 0) {  // ---- TMA producer: Q once, then K_i, V_i through the ring ----
             const int qrow = unit * A.Qu + qbase;
             tc::mbar_expect_tx(q_full, 65536);
             for (int t = 0; t < 2; ++t) {
@@ -502,8 +500,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 tc::tma_load_2d(sm + AT_Q + t * 32768 + 16384, &tm_q, 64, qrow + 128 * t, q_full);
             }
             for (int c = 0; c < 2 * ntl; ++c) {
-                const int slot = c % 3;
-                const uint32_t ph = (c / 3) & 1;
+                const int slot = c % AT_SLOTS;
+                const uint32_t ph = (c / AT_SLOTS) & 1;
                 if (!tc::mbar_wait(&rempty[slot], ph ^ 1, abort_flag, A.err)) break;
                 tc::mbar_expect_tx(&rfull[slot], 32768);
                 const int row = unit * A.n + t0 + (c >> 1) * 128;
@@ -514,21 +512,17 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             }
         }
     } else if (warp == 1 || warp == 2) {
-        // ---- MMA issuers, one per query tile, so the two tiles never wait on each other. S_t(i+1)
-        // only needs the softmax group to have copied S_t(i) into registers, so it is issued
-        // before P_t(i) V_i: the tensor pipe computes the next scores during the exponentials.
+        // ---- MMA issuers, one per query tile, so the two tiles never wait on each other ----
         const int t = warp - 1;
         if (lane == 0 && tc::mbar_wait(q_full, 0, abort_flag, A.err)) {
             const uint32_t base = tc::smem_u32(sm);
-            bool ok = attn_issue_s(base, tmem, t, 0, rfull, rempty, s_full, s_free, abort_flag,
-                                   A.err);
+            bool ok = attn_issue_s(base, tmem, t, 0, rfull, rempty, s_full, abort_flag, A.err);
             for (int i = 0; ok && i < ntl; ++i) {
-                if (i + 1 < ntl)
-                    ok = attn_issue_s(base, tmem, t, i + 1, rfull, rempty, s_full, s_free,
-                                      abort_flag, A.err);
-                if (ok)
-                    ok = attn_issue_pv(base, tmem, t, i, rfull, rempty, p_full, o_done,
-                                       abort_flag, A.err);
+                ok = attn_issue_pv(base, tmem, t, i, rfull, rempty, p_full, o_done, abort_flag,
+                                   A.err);
+                if (ok && i + 1 < ntl)
+                    ok = attn_issue_s(base, tmem, t, i + 1, rfull, rempty, s_full, abort_flag,
+                                      A.err);
             }
         }
     } else if (warp >= 4) {  // ---- softmax groups: warps 4-7 own query tile 0, 8-11 tile 1 ----
@@ -542,7 +536,6 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
         const uint32_t s_col = tmem + lane_off + t * 128;
         const uint32_t o_col = tmem + lane_off + 256 + t * 128;
-        uint8_t *P = sm + AT_P + t * 32768;
         float m_used = kNoMax, l = 0.f;  // finite sentinel: exp2(x - kNoMax) = 0
         bool ok = true;
         for (int i = 0; i < ntl; ++i) {
@@ -555,8 +548,6 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_col + c * 32, s[c]);
             tc::tmem_wait_ld();
-            tc::fence_before_sync();
-            tc::mbar_arrive(&s_free[t]);
             const int nv_tile = vend - (t0 + i * 128);  // valid columns of this row in the tile
             float mt = -INFINITY;
             if (nv_tile >= 128) {
@@ -579,33 +570,24 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             const float f = (rescale && i > 0) ? tc::ex2_approx(m_used - m_new) : 1.f;
             if (rescale) m_used = m_new;
             const float neg_m = -m_used;
+            // p = exp2(s log2e/sqrt(d) - m), packed at once as bf16 pairs: column j of P holds
+            // tokens 2j, 2j+1
             float lsum = 0.f;
+            float pk[2][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float p = tc::ex2_approx(fmaf(s[c][e], A.k1, neg_m));
-                    s[c][e] = p;
-                    lsum += p;
-                }
+            for (int j = 0; j < 64; ++j) {
+                const float p0 = tc::ex2_approx(fmaf(s[j >> 4][(2 * j) & 31], A.k1, neg_m));
+                const float p1 = tc::ex2_approx(fmaf(s[j >> 4][(2 * j + 1) & 31], A.k1, neg_m));
+                lsum += p0 + p1;
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                pk[j >> 5][j & 31] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&h2));
+            }
             l = fmaf(l, f, lsum);
-            // P_t and O_t are free once the previous P V product has completed
-            if (i > 0 && !tc::mbar_wait(&o_done[t], (i - 1) & 1, abort_flag, A.err)) {
-                ok = false;
-                break;
-            }
-            // P row -> shared memory, 128-byte-swizzled K-major (tokens 0-63 | 64-127 blocks)
-#pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
-                const int c = ch >> 2, e0 = (ch & 3) * 8;
-                uint4 pk;
-                __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    h2[u] = __floats2bfloat162_rn(s[c][e0 + 2 * u], s[c][e0 + 2 * u + 1]);
-                *reinterpret_cast<uint4 *>(P + (ch >> 3) * 16384 + tc::sw128_offset(r, ch & 7)) = pk;
-            }
-            if (f != 1.f) {
+            if (f != 1.f) {  // O must hold the previous product before it is rescaled
+                if (!tc::mbar_wait(&o_done[t], (i - 1) & 1, abort_flag, A.err)) {
+                    ok = false;
+                    break;
+                }
                 tc::fence_after_sync();
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -616,9 +598,12 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                     for (int e = 0; e < 32; ++e) o[e] *= f;
                     tc::tmem_st32(o_col + c * 32, o);
                 }
-                tc::tmem_wait_st();
             }
-            tc::fence_proxy_async_smem();
+            // P row -> TMEM over the first 64 columns of S_t (S_t is in registers; the previous
+            // P_t V product completed before S_t(i) was written)
+            tc::tmem_st32(s_col, pk[0]);
+            tc::tmem_st32(s_col + 32, pk[1]);
+            tc::tmem_wait_st();
             tc::fence_before_sync();
             tc::mbar_arrive(&p_full[t]);
         }
