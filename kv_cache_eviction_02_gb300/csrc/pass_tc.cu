@@ -392,7 +392,7 @@ struct AttnArgs {
     unsigned *err;
 };
 
-constexpr int kAtThreads = 384;  // TMA, 2 MMA issuers, idle, 2 softmax groups
+constexpr int kAtThreads = 384;  // TMA, MMA issuer, 2 idle, 2 softmax groups
 constexpr int AT_SLOTS = 5;
 constexpr uint32_t AT_Q = 0, AT_RING = 65536;  // Q0, Q1 | 5 x 32 KB ring (K_0, V_0, K_1, ...)
 constexpr uint32_t AT_BAR = AT_RING + AT_SLOTS * 32768;
@@ -408,7 +408,8 @@ __device__ __forceinline__ bool attn_issue_s(uint32_t base, uint32_t tmem, int t
                                              volatile int *abort_flag, unsigned *err) {
     constexpr uint32_t id_s = tc::idesc_bf16(128, 128, 0);
     const int c = 2 * i, slot = c % AT_SLOTS;
-    if (!tc::mbar_wait(&rfull[slot], (c / AT_SLOTS) & 1, abort_flag, err)) return false;
+    if (t == 0 && !tc::mbar_wait(&rfull[slot], (c / AT_SLOTS) & 1, abort_flag, err))
+        return false;
     tc::fence_after_sync();
     const uint32_t q_addr = base + AT_Q + t * 32768;
     const uint32_t k_addr = base + AT_RING + slot * 32768;
@@ -419,7 +420,7 @@ __device__ __forceinline__ bool attn_issue_s(uint32_t base, uint32_t tmem, int t
                      tc::sdesc_sw128(k_addr + o, 16, 1024), id_s, k > 0);
     }
     tc::mma_commit(&s_full[t]);
-    tc::mma_commit(&rempty[slot]);
+    if (t == 1) tc::mma_commit(&rempty[slot]);  // K_i is done once both tiles used it
     return true;
 }
 
@@ -431,7 +432,8 @@ __device__ __forceinline__ bool attn_issue_pv(uint32_t base, uint32_t tmem, int 
                                               unsigned *err) {
     constexpr uint32_t id_pv = tc::idesc_bf16(128, 128, 1);
     const int c = 2 * i + 1, slot = c % AT_SLOTS;
-    if (!tc::mbar_wait(&rfull[slot], (c / AT_SLOTS) & 1, abort_flag, err)) return false;
+    if (t == 0 && !tc::mbar_wait(&rfull[slot], (c / AT_SLOTS) & 1, abort_flag, err))
+        return false;
     if (!tc::mbar_wait(&p_full[t], i & 1, abort_flag, err)) return false;
     tc::fence_after_sync();
     const uint32_t v_addr = base + AT_RING + slot * 32768;
@@ -441,7 +443,7 @@ __device__ __forceinline__ bool attn_issue_pv(uint32_t base, uint32_t tmem, int 
                         tc::sdesc_sw128(v_addr + k * 2048, 16384, 1024), id_pv,
                         (i > 0 || k > 0) ? 1u : 0u);
     tc::mma_commit(&o_done[t]);
-    tc::mma_commit(&rempty[slot]);
+    if (t == 1) tc::mma_commit(&rempty[slot]);  // V_i is done once both tiles used it
     return true;
 }
 
@@ -473,7 +475,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         tc::mbar_init(q_full, 1);
         for (int s = 0; s < AT_SLOTS; ++s) {
             tc::mbar_init(&rfull[s], 1);
-            tc::mbar_init(&rempty[s], 2);  // released by both query tiles' MMA issuers
+            tc::mbar_init(&rempty[s], 1);
         }
         for (int t = 0; t < 2; ++t) {
             tc::mbar_init(&s_full[t], 1);
@@ -511,18 +513,22 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 tc::tma_load_2d(dst + 16384, map, 64, row, &rfull[slot]);
             }
         }
-    } else if (warp == 1 || warp == 2) {
-        // ---- MMA issuers, one per query tile, so the two tiles never wait on each other ----
-        const int t = warp - 1;
+    } else if (warp == 1) {
+        // ---- MMA issuer. Per K/V tile it submits [P_0 V, S_0 next] then [P_1 V, S_1 next] as
+        // blocks, so the tensor pipe serves the two softmax groups in turn and they settle half a
+        // cycle apart (one group's exponentials run while the other's products do).
         if (lane == 0 && tc::mbar_wait(q_full, 0, abort_flag, A.err)) {
             const uint32_t base = tc::smem_u32(sm);
-            bool ok = attn_issue_s(base, tmem, t, 0, rfull, rempty, s_full, abort_flag, A.err);
+            bool ok = attn_issue_s(base, tmem, 0, 0, rfull, rempty, s_full, abort_flag, A.err) &&
+                      attn_issue_s(base, tmem, 1, 0, rfull, rempty, s_full, abort_flag, A.err);
             for (int i = 0; ok && i < ntl; ++i) {
-                ok = attn_issue_pv(base, tmem, t, i, rfull, rempty, p_full, o_done, abort_flag,
-                                   A.err);
-                if (ok && i + 1 < ntl)
-                    ok = attn_issue_s(base, tmem, t, i + 1, rfull, rempty, s_full, abort_flag,
-                                      A.err);
+                for (int t = 0; ok && t < 2; ++t) {
+                    ok = attn_issue_pv(base, tmem, t, i, rfull, rempty, p_full, o_done,
+                                       abort_flag, A.err);
+                    if (ok && i + 1 < ntl)
+                        ok = attn_issue_s(base, tmem, t, i + 1, rfull, rempty, s_full, abort_flag,
+                                          A.err);
+                }
             }
         }
     } else if (warp >= 4) {  // ---- softmax groups: warps 4-7 own query tile 0, 8-11 tile 1 ----
