@@ -121,28 +121,46 @@ __global__ void __launch_bounds__(256) attn_partial_kernel(const T *__restrict__
     }
 }
 
-// grid (Qu, units), block d. Merges the token splits of one query.
-__global__ void combine_kernel(LorekvDims D, const float2 *__restrict__ part_ml,
-                               const float *__restrict__ part_o, float *__restrict__ lse2,
-                               float *__restrict__ o, float *__restrict__ lse_out,
-                               float *__restrict__ o_out) {
-    const int qi = blockIdx.x, unit = blockIdx.y, k = threadIdx.x;
+// grid (ceil(Qu/8), units), block 256: one warp per query, 4 dimensions per lane (d = 128) or
+// fewer. Merges the token splits of the query.
+__global__ void __launch_bounds__(256) combine_kernel(LorekvDims D, const float2 *__restrict__ part_ml,
+                                                      const float *__restrict__ part_o,
+                                                      float *__restrict__ lse2,
+                                                      float *__restrict__ o,
+                                                      float *__restrict__ lse_out,
+                                                      float *__restrict__ o_out) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qi = blockIdx.x * 8 + warp, unit = blockIdx.y;
+    if (qi >= D.Qu) return;
     const size_t base = (size_t)unit * D.nsplit * D.Qu + qi;
     float mx = -INFINITY;
     for (int sp = 0; sp < D.nsplit; ++sp) mx = fmaxf(mx, part_ml[base + (size_t)sp * D.Qu].x);
-    float l = 0.f, acc = 0.f;
+    const int dpl = D.d / 32;  // dimensions per lane, contiguous
+    float l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int sp = 0; sp < D.nsplit; ++sp) {
         const float2 ml = part_ml[base + (size_t)sp * D.Qu];
         if (ml.x == -INFINITY) continue;
         const float sc = exp2f(ml.x - mx);
         l = fmaf(ml.y, sc, l);
-        acc = fmaf(part_o[(base + (size_t)sp * D.Qu) * D.d + k], sc, acc);
+        const float *src = part_o + (base + (size_t)sp * D.Qu) * D.d + lane * dpl;
+        if (dpl == 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(src);
+            acc[0] = fmaf(v.x, sc, acc[0]);
+            acc[1] = fmaf(v.y, sc, acc[1]);
+            acc[2] = fmaf(v.z, sc, acc[2]);
+            acc[3] = fmaf(v.w, sc, acc[3]);
+        } else {
+            for (int c = 0; c < dpl; ++c) acc[c] = fmaf(src[c], sc, acc[c]);
+        }
     }
     const size_t row = (size_t)unit * D.Qu + qi;
-    const float ov = acc / l;
-    o[row * D.d + k] = ov;
-    if (o_out) o_out[row * D.d + k] = ov;
-    if (k == 0) {
+    const float inv = 1.f / l;
+    for (int c = 0; c < dpl; ++c) {
+        const float ov = acc[c] * inv;
+        o[row * D.d + lane * dpl + c] = ov;
+        if (o_out) o_out[row * D.d + lane * dpl + c] = ov;
+    }
+    if (lane == 0) {
         const float v = mx + log2f(l);
         lse2[row] = v;
         if (lse_out) lse_out[row] = v * kLn2;
@@ -173,9 +191,17 @@ __global__ void __launch_bounds__(256) prep_u_kernel(LorekvDims D, const float *
     const float *Gh = G + ((size_t)l * D.Hq + h) * d * d;
     const size_t row0 = (size_t)unit * D.Qu + (size_t)j * D.nq;
     const int nq_pad = (D.nq + 3) & ~3;
-    for (int idx = threadIdx.x; idx < d * d; idx += blockDim.x) Gs[idx] = Gh[idx];
-    for (int idx = threadIdx.x; idx < nq_pad * d; idx += blockDim.x)
-        Os[idx] = (idx / d < D.nq) ? o[row0 * d + idx] : 0.f;
+    {
+        const float4 *g4 = reinterpret_cast<const float4 *>(Gh);
+        float4 *s4 = reinterpret_cast<float4 *>(Gs);
+#pragma unroll 4
+        for (int idx = threadIdx.x; idx < d * d / 4; idx += blockDim.x) s4[idx] = g4[idx];
+        const float4 *o4 = reinterpret_cast<const float4 *>(o + row0 * d);
+        float4 *os4 = reinterpret_cast<float4 *>(Os);
+#pragma unroll 4
+        for (int idx = threadIdx.x; idx < nq_pad * d / 4; idx += blockDim.x)
+            os4[idx] = (idx * 4 / d < D.nq) ? o4[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     __syncthreads();
     const int gsz = d / 8;                       // threads sharing 4 queries (one per 8 dims)
     const int jb = threadIdx.x % gsz, qg = threadIdx.x / gsz;
@@ -391,7 +417,7 @@ cudaError_t launch_attention_simt(const LorekvDims &D, const void *K, const void
 cudaError_t launch_combine(const LorekvDims &D, void *ws, const LorekvWorkspace &W,
                            float *lse_out, float *o_out, cudaStream_t st) {
     char *b = static_cast<char *>(ws);
-    combine_kernel<<<dim3(D.Qu, D.units), D.d, 0, st>>>(
+    combine_kernel<<<dim3((D.Qu + 7) / 8, D.units), 256, 0, st>>>(
         D, reinterpret_cast<const float2 *>(b + W.part_ml),
         reinterpret_cast<const float *>(b + W.part_o), reinterpret_cast<float *>(b + W.lse2),
         reinterpret_cast<float *>(b + W.o), lse_out, o_out);
