@@ -16,7 +16,6 @@ namespace kve {
 cudaError_t launch_prep_u(const LorekvDims &D, const float *G, const float *omega, void *ws,
                           const LorekvWorkspace &W, cudaStream_t st, const void *QW,
                           const void *QL, bool want_bf16);
-size_t h2o_prefill_smem(int d, int P, int dtype);
 cudaError_t launch_scores_tc(const LorekvDims &D, const void *K, const void *V, const float *Lf,
                              void *ws, const LorekvWorkspace &W, float *scores,
                              unsigned *err_word, cudaStream_t st);
@@ -539,7 +538,7 @@ int h2o_prefill(KveH2O *h, const void *K, const void *V, const void *Q, int prom
     if (s.prefilled) return fail(KVE_EINVAL, "h2o_prefill: state already holds a prompt");
     if (prompt_len < 1 || prompt_len > s.max_len)
         return fail(KVE_EINVAL, "h2o_prefill: prompt_len must be in [1, max_len]");
-    if (h2o_prefill_smem(s.d, prompt_len, s.dtype) > 227 * 1024)
+    if (!h2o_prefill_fits(s.d, prompt_len, s.dtype))
         return fail(KVE_EINVAL, "h2o_prefill: prompt of %d tokens exceeds the on-chip prefill", prompt_len);
     cudaError_t e;
     {

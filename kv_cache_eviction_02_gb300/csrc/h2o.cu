@@ -59,24 +59,20 @@ template <> struct Vec8<__nv_bfloat16> {
 
 constexpr int kPrefThreads = 256;
 
-// ---- prefill: causal column sums + first compression -------------------------------------------
-// grid units, block 256. Shared: Kt [d][P] (transposed keys, input type), colsum [8][P] f32,
-// qst [8][4][d] f32, keep list [P] int.
+// ---- prefill, CUDA-core column sums ---------------------------------------------------------------
+// acc_j = sum_{i >= j} softmax_i(q_i . K_{<=i} / sqrt d)_j over the prompt (H2O summary, Section 4.1,
+// prompt handled as one block). grid units, block 256. Shared: Kt [d][P] (transposed keys, input
+// type), colsum [8][P] f32, qst [8][4][d] f32. Writes acc_out [unit][P].
 template <typename T>
-__global__ void __launch_bounds__(kPrefThreads) h2o_prefill_kernel(
-    const T *__restrict__ K, const T *__restrict__ V, const T *__restrict__ Q, int P, int d,
-    int keep_k, int cap, T *__restrict__ Ks, T *__restrict__ Vs, float *__restrict__ acc,
-    int32_t *__restrict__ pos, int32_t *__restrict__ nslots, int32_t *__restrict__ hole) {
+__global__ void __launch_bounds__(kPrefThreads) h2o_colsum_kernel(
+    const T *__restrict__ K, const T *__restrict__ Q, int P, int d, float *__restrict__ acc_out) {
     extern __shared__ __align__(16) unsigned char smraw[];
     T *Kt = reinterpret_cast<T *>(smraw);                                  // [d][P]
     float *colsum = reinterpret_cast<float *>(smraw + sizeof(T) * d * P);  // [8][P]
     float *qst = colsum + 8 * P;                                           // [8][4][d]
-    int *keep = reinterpret_cast<int *>(qst + 8 * 4 * d);                  // [P]
-    __shared__ int warp_tot[32];
     const int unit = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const T *Ku = K + (size_t)unit * P * d;
-    const T *Vu = V + (size_t)unit * P * d;
     const T *Qu = Q + (size_t)unit * P * d;
     for (int e = threadIdx.x; e < P * d; e += blockDim.x) {
         const int j = e / d, k = e % d;
@@ -153,11 +149,29 @@ __global__ void __launch_bounds__(kPrefThreads) h2o_prefill_kernel(
     for (int j = threadIdx.x; j < P; j += blockDim.x) {
         float t = 0.f;
         for (int w2 = 0; w2 < 8; ++w2) t += colsum[w2 * P + j];
-        colsum[j] = t;  // row 0 now holds acc_j (rows 1..7 are no longer read)
+        acc_out[(size_t)unit * P + j] = t;
     }
+}
+
+// ---- prefill, first compression ---------------------------------------------------------------------
+// The r most recent prompt tokens stay; among the rest the keep_k - r highest acc (equal acc: the
+// newer token stays, i.e. eviction takes the oldest first). Kept tokens fill slots 0.. in position
+// order. grid units, block 256. Shared: accs [P] f32, keep [P] int.
+template <typename T>
+__global__ void __launch_bounds__(kPrefThreads) h2o_compress_kernel(
+    const T *__restrict__ K, const T *__restrict__ V, const float *__restrict__ acc_in, int P,
+    int d, int keep_k, int cap, T *__restrict__ Ks, T *__restrict__ Vs, float *__restrict__ acc,
+    int32_t *__restrict__ pos, int32_t *__restrict__ nslots, int32_t *__restrict__ hole) {
+    extern __shared__ __align__(16) unsigned char smraw[];
+    float *colsum = reinterpret_cast<float *>(smraw);  // [P]
+    int *keep = reinterpret_cast<int *>(colsum + P);   // [P]
+    __shared__ int warp_tot[32];
+    const int unit = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const T *Ku = K + (size_t)unit * P * d;
+    const T *Vu = V + (size_t)unit * P * d;
+    for (int j = threadIdx.x; j < P; j += blockDim.x) colsum[j] = acc_in[(size_t)unit * P + j];
     __syncthreads();
-    // first compression: the r most recent stay; among the rest the keep_k - r highest acc
-    // (equal acc: the newer token stays, i.e. eviction takes the oldest first)
     const int r = keep_k / 2;
     const int heavy = keep_k - r;
     for (int j = threadIdx.x; j < P; j += blockDim.x) {
@@ -376,16 +390,26 @@ __global__ void h2o_count_kernel(const int32_t *__restrict__ nslots,
 
 template <typename T>
 cudaError_t prefill_t(H2OState &s, const void *K, const void *V, const void *Q, int P,
-                      int keep_k, cudaStream_t st) {
-    const size_t smem = sizeof(T) * s.d * P + sizeof(float) * (8 * P + 8 * 4 * s.d) +
-                        sizeof(int) * P;
-    auto kern = h2o_prefill_kernel<T>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+                      int keep_k, float *acc_tmp, cudaStream_t st) {
+    cudaError_t e;
+    if (h2o_colsum_tc_supported(s.d, P, s.dtype)) {
+        e = launch_h2o_colsum_tc(s.units, P, K, Q, s.dtype, acc_tmp, st);
+    } else {
+        const size_t smem = h2o_prefill_smem(s.d, P, s.dtype);
+        auto kern = h2o_colsum_kernel<T>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<s.units, kPrefThreads, smem, st>>>((const T *)K, (const T *)Q, P, s.d, acc_tmp);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
-    kern<<<s.units, kPrefThreads, smem, st>>>((const T *)K, (const T *)V, (const T *)Q, P, s.d,
-                                              keep_k, s.cap, (T *)s.K, (T *)s.V, s.acc, s.pos,
-                                              s.nslots, s.hole);
+    const size_t smem = (sizeof(float) + sizeof(int)) * P;
+    auto comp = h2o_compress_kernel<T>;
+    e = cudaFuncSetAttribute(comp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    comp<<<s.units, kPrefThreads, smem, st>>>((const T *)K, (const T *)V, acc_tmp, P, s.d, keep_k,
+                                              s.cap, (T *)s.K, (T *)s.V, s.acc, s.pos, s.nslots,
+                                              s.hole);
     return cudaGetLastError();
 }
 
@@ -411,15 +435,27 @@ cudaError_t step_t(H2OState &s, const void *q, const void *k, const void *v, voi
 }  // namespace
 
 size_t h2o_prefill_smem(int d, int P, int dtype) {
-    return dtype_size(dtype) * d * P + sizeof(float) * (8 * P + 8 * 4 * d) + sizeof(int) * P;
+    return dtype_size(dtype) * d * P + sizeof(float) * (8 * P + 8 * 4 * d);
+}
+
+bool h2o_prefill_fits(int d, int P, int dtype) {
+    return h2o_colsum_tc_supported(d, P, dtype) || h2o_prefill_smem(d, P, dtype) <= 227 * 1024;
 }
 
 cudaError_t launch_h2o_prefill(H2OState &s, const void *K, const void *V, const void *Q, int P,
                                cudaStream_t st) {
     int keep_k = (int)floor((double)s.frac * (double)P);
     if (keep_k > P) keep_k = P;
-    if (s.dtype == KVE_F16) return prefill_t<__half>(s, K, V, Q, P, keep_k, st);
-    return prefill_t<__nv_bfloat16>(s, K, V, Q, P, keep_k, st);
+    // per-token prefill scores [units][P], stream-ordered scratch freed after the compression
+    float *acc_tmp = nullptr;
+    cudaError_t e = cudaMallocAsync(&acc_tmp, sizeof(float) * (size_t)s.units * P, st);
+    if (e != cudaSuccess) return e;
+    if (s.dtype == KVE_F16)
+        e = prefill_t<__half>(s, K, V, Q, P, keep_k, acc_tmp, st);
+    else
+        e = prefill_t<__nv_bfloat16>(s, K, V, Q, P, keep_k, acc_tmp, st);
+    const cudaError_t ef = cudaFreeAsync(acc_tmp, st);
+    return e != cudaSuccess ? e : ef;
 }
 
 cudaError_t launch_h2o_step(H2OState &s, const void *q, const void *k, const void *v, void *out,

@@ -114,6 +114,12 @@ struct H2OState {
 };
 cudaError_t launch_h2o_prefill(H2OState &s, const void *K, const void *V, const void *Q, int P,
                                cudaStream_t st);
+bool h2o_prefill_fits(int d, int P, int dtype);
+size_t h2o_prefill_smem(int d, int P, int dtype);  // CUDA-core column-sum kernel
+// tensor-core prefill column sums (h2o_tc.cu)
+bool h2o_colsum_tc_supported(int d, int P, int dtype);
+cudaError_t launch_h2o_colsum_tc(int units, int P, const void *K, const void *Q, int dtype,
+                                 float *acc_out, cudaStream_t st);
 cudaError_t launch_h2o_step(H2OState &s, const void *q, const void *k, const void *v, void *out,
                             cudaStream_t st);
 cudaError_t launch_h2o_export(const H2OState &s, void *K, void *V, int32_t *pos, float *acc,

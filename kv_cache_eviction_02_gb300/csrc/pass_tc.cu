@@ -31,7 +31,7 @@ bool tc_supported(const LorekvDims &D) {
 
 // ---- host: tensor maps ---------------------------------------------------------------------------
 bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
-                       uint32_t box_inner, uint32_t box_rows) {
+                       uint32_t box_inner, uint32_t box_rows, bool f16) {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
         void *p = nullptr;
@@ -47,7 +47,7 @@ bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint6
     cuuint64_t strides[1] = {inner * 2};
     cuuint32_t box[2] = {box_inner, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+    return fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;

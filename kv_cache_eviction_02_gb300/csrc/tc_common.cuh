@@ -178,15 +178,18 @@ __device__ __forceinline__ void tmem_wait_st() {
 }
 
 // ---- descriptors -----------------------------------------------------------------------------------
-// Instruction descriptor of kind::f16: bf16 A and B, fp32 D, M x N, A K-major, B K-major
-// (b_mn_major = 0) or MN-major (1).
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) {
+// Instruction descriptor of kind::f16: A and B both bf16 (ab_bf16 = 1) or both f16 (0), fp32 D,
+// M x N, A K-major, B K-major (b_mn_major = 0) or MN-major (1).
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, int b_mn_major, int ab_bf16) {
     return (1u << 4)                       // D format: f32
-           | (1u << 7)                     // A format: bf16
-           | (1u << 10)                    // B format: bf16
+           | (uint32_t(ab_bf16) << 7)      // A format: f16 (0) / bf16 (1)
+           | (uint32_t(ab_bf16) << 10)     // B format: same as A
            | (uint32_t(b_mn_major) << 16)  // B major-ness
            | (uint32_t(N >> 3) << 17)      // N / 8
            | (uint32_t(M >> 4) << 24);     // M / 16
+}
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) {
+    return idesc_f16kind(M, N, b_mn_major, 1);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle. `addr` is the shared-space byte address of
@@ -241,9 +244,9 @@ __device__ __forceinline__ float rsqrt_approx(float x) {
 
 }  // namespace tc
 
-// Host: encode a 2D bf16 tensor map {inner, rows} with a {box_inner, box_rows} box and 128-byte
-// swizzle (box_inner * 2 bytes must be <= 128).
+// Host: encode a 2D tensor map of 16-bit elements (bf16, or f16 when `f16`) {inner, rows} with a
+// {box_inner, box_rows} box and 128-byte swizzle (box_inner * 2 bytes must be <= 128).
 bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
-                       uint32_t box_inner, uint32_t box_rows);
+                       uint32_t box_inner, uint32_t box_rows, bool f16 = false);
 
 }  // namespace kve

@@ -199,3 +199,47 @@ def test_h2o_full_size_sampled_units():
     st.close()
     del hin
     torch.cuda.empty_cache()
+
+
+_PREFILL_CASES = [
+    # (prompt length, dtype, (batch, layers, heads)): ragged last tiles, one to five 128-token
+    # tiles, bf16 and f16, and more units than SMs (the prefill kernel walks units persistently)
+    (100, "f16", (1, 1, 3)),
+    (129, "bf16", (1, 2, 2)),
+    (300, "f16", (1, 1, 4)),
+    (512, "bf16", (1, 1, 2)),
+    (640, "f16", (1, 1, 2)),
+    (256, "f16", (2, 10, 16)),
+]
+
+
+@pytest.mark.parametrize("P,dtype,shape", _PREFILL_CASES,
+                         ids=[f"P{c[0]}-{c[1]}-u{c[2][0] * c[2][1] * c[2][2]}" for c in _PREFILL_CASES])
+def test_h2o_prefill_shapes(P, dtype, shape):
+    """Prefill scores and the first compression at d_head 128 against the oracle: retained
+    positions, their accumulated scores and their K/V rows."""
+    b, L, H = shape
+    cfg = synth.H2OConfig(f"prefill{P}", dtype, batch=b, L=L, H=H, d=128, prompt=P, steps=1)
+    hin = {k: v.to(_dev()) for k, v in synth.h2o_inputs(cfg, "cpu", steps=1).items()}
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    st = api.h2o_state_create(b, L, H, 128, P + 1, cfg.budget_frac, tdt)
+    st.prefill(hin["K"], hin["V"], hin["Q"])
+    n = cfg.units
+    units = list(range(n)) if n <= 16 else sorted({0, 1, 150, 151, 152, 153, n // 2, n - 2, n - 1})
+    orc = {}
+    for u in units:
+        bb, l, h = _unit_coords(cfg, u)
+        orc[u] = oracle.H2OUnit(hin["K"][bb, l, h], hin["V"][bb, l, h], hin["Q"][bb, l, h],
+                                cfg.budget_frac, P + 1)
+    ex = st.export()
+    _check_prefill(ex, units, orc, cfg, hin)
+    _check_state(ex, units, orc, "prefill")
+    pos = ex["pos"].cpu().numpy()
+    Kx, Vx = ex["K"].cpu(), ex["V"].cpu()
+    for u in units:
+        bb, l, h = _unit_coords(cfg, u)
+        for slot in np.flatnonzero(pos[u] >= 0):
+            p = int(pos[u][slot])
+            assert torch.equal(Kx[u, slot], hin["K"][bb, l, h, p].cpu()), (u, p)
+            assert torch.equal(Vx[u, slot], hin["V"][bb, l, h, p].cpu()), (u, p)
+    st.close()
