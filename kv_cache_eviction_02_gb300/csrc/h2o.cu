@@ -156,11 +156,12 @@ __global__ void __launch_bounds__(kPrefThreads) h2o_colsum_kernel(
 // ---- prefill, first compression ---------------------------------------------------------------------
 // The r most recent prompt tokens stay; among the rest the keep_k - r highest acc (equal acc: the
 // newer token stays, i.e. eviction takes the oldest first). Kept tokens fill slots 0.. in position
-// order. grid units, block 256. Shared: accs [P] f32, keep [P] int.
+// order. acc_in [unit][parts][P] holds partial sums of the prefill scores, added in part order.
+// grid units, block 256. Shared: accs [P] f32, keep [P] int.
 template <typename T>
 __global__ void __launch_bounds__(kPrefThreads) h2o_compress_kernel(
-    const T *__restrict__ K, const T *__restrict__ V, const float *__restrict__ acc_in, int P,
-    int d, int keep_k, int cap, T *__restrict__ Ks, T *__restrict__ Vs, float *__restrict__ acc,
+    const T *__restrict__ K, const T *__restrict__ V, const float *__restrict__ acc_in, int parts,
+    int P, int d, int keep_k, int cap, T *__restrict__ Ks, T *__restrict__ Vs, float *__restrict__ acc,
     int32_t *__restrict__ pos, int32_t *__restrict__ nslots, int32_t *__restrict__ hole) {
     extern __shared__ __align__(16) unsigned char smraw[];
     float *colsum = reinterpret_cast<float *>(smraw);  // [P]
@@ -170,7 +171,11 @@ __global__ void __launch_bounds__(kPrefThreads) h2o_compress_kernel(
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const T *Ku = K + (size_t)unit * P * d;
     const T *Vu = V + (size_t)unit * P * d;
-    for (int j = threadIdx.x; j < P; j += blockDim.x) colsum[j] = acc_in[(size_t)unit * P + j];
+    for (int j = threadIdx.x; j < P; j += blockDim.x) {
+        float t = 0.f;
+        for (int p = 0; p < parts; ++p) t += acc_in[((size_t)unit * parts + p) * P + j];
+        colsum[j] = t;
+    }
     __syncthreads();
     const int r = keep_k / 2;
     const int heavy = keep_k - r;
@@ -392,7 +397,8 @@ template <typename T>
 cudaError_t prefill_t(H2OState &s, const void *K, const void *V, const void *Q, int P,
                       int keep_k, float *acc_tmp, cudaStream_t st) {
     cudaError_t e;
-    if (h2o_colsum_tc_supported(s.d, P, s.dtype)) {
+    const bool tc = h2o_colsum_tc_supported(s.d, P, s.dtype);
+    if (tc) {
         e = launch_h2o_colsum_tc(s.units, P, K, Q, s.dtype, acc_tmp, st);
     } else {
         const size_t smem = h2o_prefill_smem(s.d, P, s.dtype);
@@ -407,7 +413,8 @@ cudaError_t prefill_t(H2OState &s, const void *K, const void *V, const void *Q, 
     auto comp = h2o_compress_kernel<T>;
     e = cudaFuncSetAttribute(comp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    comp<<<s.units, kPrefThreads, smem, st>>>((const T *)K, (const T *)V, acc_tmp, P, s.d, keep_k,
+    comp<<<s.units, kPrefThreads, smem, st>>>((const T *)K, (const T *)V, acc_tmp,
+                                              tc ? kColsumTcParts : 1, P, s.d, keep_k,
                                               s.cap, (T *)s.K, (T *)s.V, s.acc, s.pos, s.nslots,
                                               s.hole);
     return cudaGetLastError();
@@ -446,9 +453,10 @@ cudaError_t launch_h2o_prefill(H2OState &s, const void *K, const void *V, const 
                                cudaStream_t st) {
     int keep_k = (int)floor((double)s.frac * (double)P);
     if (keep_k > P) keep_k = P;
-    // per-token prefill scores [units][P], stream-ordered scratch freed after the compression
+    // partial prefill scores [units][parts][P], stream-ordered scratch freed after the compression
     float *acc_tmp = nullptr;
-    cudaError_t e = cudaMallocAsync(&acc_tmp, sizeof(float) * (size_t)s.units * P, st);
+    cudaError_t e =
+        cudaMallocAsync(&acc_tmp, sizeof(float) * (size_t)s.units * kColsumTcParts * P, st);
     if (e != cudaSuccess) return e;
     if (s.dtype == KVE_F16)
         e = prefill_t<__half>(s, K, V, Q, P, keep_k, acc_tmp, st);

@@ -20,13 +20,14 @@ namespace kve {
 
 namespace {
 
-constexpr int kHpThreads = 192;
+constexpr int kHpThreads = 320;
 constexpr int HP_KSLOTS = 5, HP_QSLOTS = 2, HP_TSLOTS = 4;
 constexpr int kHpMaxTiles = HP_KSLOTS;  // a unit's K tiles must fit in the ring at once
 constexpr uint32_t HP_K = 0;
 constexpr uint32_t HP_Q = HP_K + HP_KSLOTS * 32768;
-constexpr uint32_t HP_LSE = HP_Q + HP_QSLOTS * 32768;  // [2][128] f32
-constexpr uint32_t HP_BAR = HP_LSE + 2 * 128 * 4;
+constexpr uint32_t HP_ML = HP_Q + HP_QSLOTS * 32768;   // [128] float2: (m, l) of column half 1
+constexpr uint32_t HP_LSE = HP_ML + 128 * 8;           // [128] f32: lse2 of the tile's queries
+constexpr uint32_t HP_BAR = HP_LSE + 128 * 4;
 constexpr size_t HP_SMEM = HP_BAR + 256 + 1024;
 constexpr float kNoMax = -1e30f;
 
@@ -38,10 +39,10 @@ struct ColsumArgs {
     unsigned *err;
 };
 
-// The 128 fp32 columns of one TMEM slot in this thread's lane.
-__device__ __forceinline__ void load_block(uint32_t taddr, float (&v)[128]) {
+// 64 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void load_half(uint32_t taddr, float (&v)[64]) {
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
+    for (int h = 0; h < 2; ++h) {
         float t[32];
         tc::tmem_ld32(taddr + 32 * h, t);
 #pragma unroll
@@ -63,9 +64,10 @@ __global__ void __launch_bounds__(kHpThreads, 1)
     uint64_t *kfull = bars, *kempty = bars + HP_KSLOTS;
     uint64_t *qfull = bars + 2 * HP_KSLOTS, *qempty = qfull + HP_QSLOTS;
     uint64_t *tfull = qempty + HP_QSLOTS, *tempty = tfull + HP_TSLOTS;
-    uint64_t *lsef = tempty + HP_TSLOTS;
+    uint64_t *lsef = tempty + HP_TSLOTS, *lsef2 = lsef + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(lsef + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(lsef + 3);
+    float2 *ml_s = reinterpret_cast<float2 *>(sm + HP_ML);
     float *lse_s = reinterpret_cast<float *>(sm + HP_LSE);
 
     if (threadIdx.x == 0) {
@@ -79,10 +81,10 @@ __global__ void __launch_bounds__(kHpThreads, 1)
         }
         for (int i = 0; i < HP_TSLOTS; ++i) {
             tc::mbar_init(&tfull[i], 1);
-            tc::mbar_init(&tempty[i], 128);
+            tc::mbar_init(&tempty[i], 256);
         }
-        tc::mbar_init(&lsef[0], 128);
-        tc::mbar_init(&lsef[1], 128);
+        tc::mbar_init(lsef, 256);
+        tc::mbar_init(lsef2, 256);
         *abort_flag = 0;
         tc::mbar_fence_init();
     }
@@ -189,17 +191,20 @@ __global__ void __launch_bounds__(kHpThreads, 1)
             }
         }
     } else {
-        // ---- lane owners: warp w reads TMEM lanes 32 (w % 4) .. +31 ----
+        // ---- lane owners: warp w reads TMEM lanes 32 (w % 4) .. +31, columns 64 hf .. +63 of
+        // every block (hf = 0 for warps 2-5, 1 for warps 6-9) ----
         const int row = (warp & 3) * 32 + lane;
-        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const int hf = (warp - 2) >> 2;
+        const uint32_t tcol = (uint32_t)(64 * hf) + ((uint32_t)((warp & 3) * 32) << 16);
         const float k1 = A.k1;
         const uint64_t k1_2 = tc::pk2(k1, k1);
         int tcn = 0, lcn = 0;
         bool ok = true;
         for (int unit = blockIdx.x; unit < A.units && ok; unit += gridDim.x) {
-            float *accu = A.acc + (size_t)unit * A.P;
+            float *accu = A.acc + ((size_t)unit * 2 + hf) * A.P;  // this half's partial sums
             for (int r = nt - 1; r >= 0 && ok; --r) {
-                // phase 1: online softmax statistics of query row q = 128 r + row
+                // phase 1: online softmax statistics of query row q = 128 r + row over this
+                // half's key columns
                 const int q = 128 * r + row;
                 float m = kNoMax, l = 0.f;
                 for (int b = r; b >= 0; --b) {
@@ -209,20 +214,21 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                         break;
                     }
                     tc::fence_after_sync();
-                    float v[128];
-                    load_block(tmem + lane_off + ts * 128, v);
+                    float v[64];
+                    load_half(tmem + tcol + ts * 128, v);
                     tc::fence_before_sync();
                     tc::mbar_arrive(&tempty[ts]);
                     ++tcn;
                     const bool full = b < r && 128 * (b + 1) <= A.P;  // warp-uniform
-                    const int lim = min(q - 128 * b, A.P - 1 - 128 * b);  // key column c valid iff c <= lim
+                    // key column c of this half valid iff c <= lim
+                    const int lim = min(q - 128 * b, A.P - 1 - 128 * b) - 64 * hf;
                     float mx = kNoMax;
                     if (full) {
 #pragma unroll
-                        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, v[c]);
+                        for (int c = 0; c < 64; ++c) mx = fmaxf(mx, v[c]);
                     } else {
 #pragma unroll
-                        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, c <= lim ? v[c] : kNoMax);
+                        for (int c = 0; c < 64; ++c) mx = fmaxf(mx, c <= lim ? v[c] : kNoMax);
                     }
                     const float mn = fmaxf(m, mx);
                     const float nmk = -mn * k1;
@@ -230,7 +236,7 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                     uint64_t s2[4] = {0, 0, 0, 0};  // bit pattern 0 = (0.f, 0.f)
                     if (full) {
 #pragma unroll
-                        for (int c = 0; c < 128; c += 2) {
+                        for (int c = 0; c < 64; c += 2) {
                             float ta, tb;
                             tc::upk2(tc::fma2(tc::pk2(v[c], v[c + 1]), k1_2, nmk_2), ta, tb);
                             s2[(c >> 1) & 3] = tc::add2(
@@ -238,7 +244,7 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                         }
                     } else {
 #pragma unroll
-                        for (int c = 0; c < 128; c += 2) {
+                        for (int c = 0; c < 64; c += 2) {
                             float ta, tb;
                             tc::upk2(tc::fma2(tc::pk2(v[c], v[c + 1]), k1_2, nmk_2), ta, tb);
                             const float ea = c <= lim ? tc::ex2_approx(ta) : 0.f;
@@ -253,21 +259,36 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                         tc::upk2(s2[k], a, bb);
                         bs += a + bb;
                     }
+                    // a half may see no valid column yet (m stays kNoMax, l 0): the merge below
+                    // weights it by 2^(-huge) = 0
                     l = l * tc::ex2_approx((m - mn) * k1) + bs;
                     m = mn;
                 }
                 if (!ok) break;
-                const int lb = lcn & 1;
-                lse_s[lb * 128 + row] = m * k1 + __log2f(l);
-                tc::mbar_arrive(&lsef[lb]);
-                if (!tc::mbar_wait(&lsef[lb], (lcn >> 1) & 1, abort_flag, A.err)) {
+                // merge the halves: half 1 hands (m, l) over, half 0 writes lse2 of the row
+                if (hf == 1) ml_s[row] = make_float2(m, l);
+                tc::mbar_arrive(lsef);
+                if (!tc::mbar_wait(lsef, lcn & 1, abort_flag, A.err)) {
+                    ok = false;
+                    break;
+                }
+                if (hf == 0) {
+                    const float2 o = ml_s[row];
+                    const float mm = fmaxf(m, o.x);
+                    const float ll = l * tc::ex2_approx((m - mm) * k1) +
+                                     o.y * tc::ex2_approx((o.x - mm) * k1);
+                    lse_s[row] = mm * k1 + __log2f(ll);
+                }
+                tc::mbar_arrive(lsef2);
+                if (!tc::mbar_wait(lsef2, lcn & 1, abort_flag, A.err)) {
                     ok = false;
                     break;
                 }
                 ++lcn;
-                const float4 *lse4 = reinterpret_cast<const float4 *>(lse_s + lb * 128);
-                // phase 2: key row j = 128 b + row adds its probabilities under the tile's queries
-                const int qmax = A.P - 1 - 128 * r;  // query column c valid iff c <= qmax
+                const float4 *lse4 = reinterpret_cast<const float4 *>(lse_s + 64 * hf);
+                // phase 2: key row j = 128 b + row adds its probabilities under this half's
+                // query columns of the tile
+                const int qmax = A.P - 1 - 128 * r - 64 * hf;  // query column c valid iff c <= qmax
                 for (int b = r; b >= 0; --b) {
                     const int j = 128 * b + row;
                     const float prev = (r == nt - 1 || j >= A.P) ? 0.f : accu[j];
@@ -277,16 +298,16 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                         break;
                     }
                     tc::fence_after_sync();
-                    float v[128];
-                    load_block(tmem + lane_off + ts * 128, v);
+                    float v[64];
+                    load_half(tmem + tcol + ts * 128, v);
                     tc::fence_before_sync();
                     tc::mbar_arrive(&tempty[ts]);
                     ++tcn;
-                    const bool full = b < r && qmax >= 127;  // warp-uniform
-                    const int lo = j - 128 * r;              // query column c valid iff c >= lo
+                    const bool full = b < r && qmax >= 63;  // warp-uniform
+                    const int lo = j - 128 * r - 64 * hf;   // query column c valid iff c >= lo
                     uint64_t s2[4] = {0, 0, 0, 0};
 #pragma unroll
-                    for (int c = 0; c < 128; c += 4) {
+                    for (int c = 0; c < 64; c += 4) {
                         const float4 ls = lse4[c >> 2];
                         float ta, tb, tc_, td;
                         tc::upk2(tc::fma2(tc::pk2(v[c], v[c + 1]), k1_2, tc::pk2(-ls.x, -ls.y)),

@@ -116,7 +116,9 @@ cudaError_t launch_h2o_prefill(H2OState &s, const void *K, const void *V, const 
                                cudaStream_t st);
 bool h2o_prefill_fits(int d, int P, int dtype);
 size_t h2o_prefill_smem(int d, int P, int dtype);  // CUDA-core column-sum kernel
-// tensor-core prefill column sums (h2o_tc.cu)
+// tensor-core prefill column sums (h2o_tc.cu): writes kColsumTcParts partial sums per token,
+// acc_out [units][kColsumTcParts][P]
+constexpr int kColsumTcParts = 2;
 bool h2o_colsum_tc_supported(int d, int P, int dtype);
 cudaError_t launch_h2o_colsum_tc(int units, int P, const void *K, const void *Q, int dtype,
                                  float *acc_out, cudaStream_t st);
