@@ -157,7 +157,38 @@ __global__ void __launch_bounds__(kPrefThreads) h2o_colsum_kernel(
 // The r most recent prompt tokens stay; among the rest the keep_k - r highest acc (equal acc: the
 // newer token stays, i.e. eviction takes the oldest first). Kept tokens fill slots 0.. in position
 // order. acc_in [unit][parts][P] holds partial sums of the prefill scores, added in part order.
-// grid units, block 256. Shared: accs [P] f32, keep [P] int.
+// The (keep_k - r)-th largest score tau is found by an MSB-first radix select (4 passes of 8 bits
+// over shared-memory histograms); scores above tau stay, and among those equal to tau the newest
+// fill the remainder. grid units, block 256. Shared: accs [P] f32, slot [P] int, src [P] int.
+
+__device__ __forceinline__ uint32_t score_key(float f) {  // order-preserving for all floats
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exclusive block-wide scan of one value per thread; *total = the block's sum. All threads call.
+__device__ __forceinline__ int block_scan_excl(int v, int *warp_tot, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nw = blockDim.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    int before = 0, tot = 0;
+    for (int w2 = 0; w2 < nw; ++w2) {
+        const int t = warp_tot[w2];
+        before += (w2 < warp) ? t : 0;
+        tot += t;
+    }
+    __syncthreads();
+    *total = tot;
+    return before + x - v;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kPrefThreads) h2o_compress_kernel(
     const T *__restrict__ K, const T *__restrict__ V, const float *__restrict__ acc_in, int parts,
@@ -165,8 +196,12 @@ __global__ void __launch_bounds__(kPrefThreads) h2o_compress_kernel(
     int32_t *__restrict__ pos, int32_t *__restrict__ nslots, int32_t *__restrict__ hole) {
     extern __shared__ __align__(16) unsigned char smraw[];
     float *colsum = reinterpret_cast<float *>(smraw);  // [P]
-    int *keep = reinterpret_cast<int *>(colsum + P);   // [P]
+    int *slot_of = reinterpret_cast<int *>(colsum + P);  // [P] slot of position j, or -1
+    int *src_of = slot_of + P;                           // [P] position held by slot s
     __shared__ int warp_tot[32];
+    __shared__ uint32_t hist[256];
+    __shared__ uint32_t s_prefix;
+    __shared__ int s_krem;
     const int unit = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const T *Ku = K + (size_t)unit * P * d;
@@ -176,74 +211,121 @@ __global__ void __launch_bounds__(kPrefThreads) h2o_compress_kernel(
         for (int p = 0; p < parts; ++p) t += acc_in[((size_t)unit * parts + p) * P + j];
         colsum[j] = t;
     }
-    __syncthreads();
     const int r = keep_k / 2;
     const int heavy = keep_k - r;
-    for (int j = threadIdx.x; j < P; j += blockDim.x) {
-        int kp;
-        if (keep_k >= P || j >= P - r) {
-            kp = 1;
-        } else {
-            const float aj = colsum[j];
-            int rank = 0;
-            for (int j2 = 0; j2 < P - r; ++j2) {
-                const float a2 = colsum[j2];
-                rank += (a2 > aj || (a2 == aj && j2 > j)) ? 1 : 0;
-            }
-            kp = rank < heavy ? 1 : 0;
-        }
-        keep[j] = kp;
+    const int ncand = keep_k >= P ? 0 : P - r;  // candidates for the heavy part: [0, ncand)
+    if (threadIdx.x == 0) {
+        s_prefix = 0u;
+        s_krem = heavy;
     }
     __syncthreads();
-    // ordered slot assignment (block scan over positions)
+    if (ncand > 0 && heavy > 0) {
+        for (int pass = 0; pass < 4; ++pass) {
+            const int shift = 24 - 8 * pass;
+            const uint32_t mask = pass == 0 ? 0u : (0xffffffffu << (shift + 8));
+            for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0u;
+            __syncthreads();
+            const uint32_t prefix = s_prefix;
+            for (int j = threadIdx.x; j < ncand; j += blockDim.x) {
+                const uint32_t key = score_key(colsum[j]);
+                if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+            }
+            __syncthreads();
+            if (warp == 0) {
+                // lane l holds bins 255-8l .. 248-8l (descending); find the bin of the krem-th
+                // largest key among those matching the prefix
+                uint32_t c[8];
+                int sum = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    c[i] = hist[255 - 8 * lane - i];
+                    sum += (int)c[i];
+                }
+                int incl = sum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const int krem = s_krem;
+                const unsigned ball = __ballot_sync(0xffffffffu, incl >= krem);
+                if (ball != 0u && lane == __ffs(ball) - 1) {
+                    int kr = krem - (incl - sum);
+                    int bsel = 248 - 8 * lane;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if ((int)c[i] >= kr) {
+                            bsel = 255 - 8 * lane - i;
+                            break;
+                        }
+                        kr -= (int)c[i];
+                    }
+                    s_krem = kr;
+                    s_prefix = prefix | ((uint32_t)bsel << shift);
+                }
+            }
+            __syncthreads();
+        }
+    }
+    const uint32_t tau = s_prefix;
+    const int take_eq = s_krem;  // candidates equal to tau that stay, newest first
+    // keep flags; ranks among the candidates equal to tau by descending position
+    int run_eq = 0;
+    for (int base = 0; base < P; base += blockDim.x) {
+        const int j = P - 1 - (base + (int)threadIdx.x);  // descending positions
+        int keep = 0, eq = 0;
+        if (j >= 0) {
+            if (j >= ncand) {
+                keep = 1;
+            } else if (heavy > 0) {
+                const uint32_t key = score_key(colsum[j]);
+                keep = key > tau ? 1 : 0;
+                eq = key == tau ? 1 : 0;
+            }
+        }
+        int tot_eq;
+        const int rank_eq = run_eq + block_scan_excl(eq, warp_tot, &tot_eq);
+        if (j >= 0) slot_of[j] = (keep || (eq && rank_eq < take_eq)) ? 1 : 0;
+        run_eq += tot_eq;
+    }
+    __syncthreads();
+    // ordered slot assignment (block scan over ascending positions)
     int run = 0;
     for (int base = 0; base < P; base += blockDim.x) {
         const int j = base + threadIdx.x;
-        const int v = (j < P) ? keep[j] : 0;
-        int x = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
+        const int v = j < P ? slot_of[j] : 0;
+        int tot;
+        const int before = run + block_scan_excl(v, warp_tot, &tot);
+        if (j < P) {
+            slot_of[j] = v ? before : -1;
+            if (v) src_of[before] = j;
         }
-        if (lane == 31) warp_tot[warp] = x;
-        __syncthreads();
-        int before = 0, tot = 0;
-        for (int w2 = 0; w2 < (int)(blockDim.x >> 5); ++w2) {
-            if (w2 < warp) before += warp_tot[w2];
-            tot += warp_tot[w2];
-        }
-        __syncthreads();
-        if (j < P) keep[j] = v ? (run + before + x - v) : -1;  // slot index or -1
         run += tot;
     }
     __syncthreads();
     const int kept = run;
     float *accu = acc + (size_t)unit * cap;
     int32_t *posu = pos + (size_t)unit * cap;
-    for (int j = threadIdx.x; j < P; j += blockDim.x) {
-        const int slot = keep[j];
-        if (slot >= 0) {
-            accu[slot] = colsum[j];
-            posu[slot] = j;
+    for (int sl = threadIdx.x; sl < cap; sl += blockDim.x) {
+        if (sl < kept) {
+            const int j = src_of[sl];
+            accu[sl] = colsum[j];
+            posu[sl] = j;
+        } else {
+            accu[sl] = 0.f;
+            posu[sl] = -1;
         }
-    }
-    for (int sl = kept + threadIdx.x; sl < cap; sl += blockDim.x) {
-        accu[sl] = 0.f;
-        posu[sl] = -1;
     }
     const int vpr = d * (int)sizeof(T) / 16;
     const uint4 *Ksrc = reinterpret_cast<const uint4 *>(Ku);
     const uint4 *Vsrc = reinterpret_cast<const uint4 *>(Vu);
     uint4 *Kd = reinterpret_cast<uint4 *>(Ks + (size_t)unit * cap * d);
     uint4 *Vd = reinterpret_cast<uint4 *>(Vs + (size_t)unit * cap * d);
-    for (int e = threadIdx.x; e < P * vpr; e += blockDim.x) {
-        const int j = e / vpr, c = e % vpr;
-        const int slot = keep[j];
-        if (slot >= 0) {
-            Kd[(size_t)slot * vpr + c] = Ksrc[e];
-            Vd[(size_t)slot * vpr + c] = Vsrc[e];
-        }
+    for (int e = threadIdx.x; e < kept * vpr; e += blockDim.x) {
+        const int sl = e / vpr, c = e % vpr;
+        const size_t src = (size_t)src_of[sl] * vpr + c;
+        Kd[e] = Ksrc[src];
+        Vd[e] = Vsrc[src];
     }
     if (threadIdx.x == 0) {
         nslots[unit] = kept;
@@ -409,7 +491,7 @@ cudaError_t prefill_t(H2OState &s, const void *K, const void *V, const void *Q, 
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
-    const size_t smem = (sizeof(float) + sizeof(int)) * P;
+    const size_t smem = (sizeof(float) + 2 * sizeof(int)) * P;
     auto comp = h2o_compress_kernel<T>;
     e = cudaFuncSetAttribute(comp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

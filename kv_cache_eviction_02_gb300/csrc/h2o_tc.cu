@@ -26,7 +26,7 @@ constexpr int kHpMaxTiles = HP_KSLOTS;  // a unit's K tiles must fit in the ring
 constexpr uint32_t HP_K = 0;
 constexpr uint32_t HP_Q = HP_K + HP_KSLOTS * 32768;
 constexpr uint32_t HP_ML = HP_Q + HP_QSLOTS * 32768;   // [128] float2: (m, l) of column half 1
-constexpr uint32_t HP_LSE = HP_ML + 128 * 8;           // [128] f32: lse2 of the tile's queries
+constexpr uint32_t HP_LSE = HP_ML + 128 * 8;           // [128] f32: -lse2 of the tile's queries
 constexpr uint32_t HP_BAR = HP_LSE + 128 * 4;
 constexpr size_t HP_SMEM = HP_BAR + 256 + 1024;
 constexpr float kNoMax = -1e30f;
@@ -202,6 +202,9 @@ __global__ void __launch_bounds__(kHpThreads, 1)
         bool ok = true;
         for (int unit = blockIdx.x; unit < A.units && ok; unit += gridDim.x) {
             float *accu = A.acc + ((size_t)unit * 2 + hf) * A.P;  // this half's partial sums
+            float accb[kHpMaxTiles];  // running sums of key rows 128 b + row
+#pragma unroll
+            for (int b = 0; b < kHpMaxTiles; ++b) accb[b] = 0.f;
             for (int r = nt - 1; r >= 0 && ok; --r) {
                 // phase 1: online softmax statistics of query row q = 128 r + row over this
                 // half's key columns
@@ -277,7 +280,7 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                     const float mm = fmaxf(m, o.x);
                     const float ll = l * tc::ex2_approx((m - mm) * k1) +
                                      o.y * tc::ex2_approx((o.x - mm) * k1);
-                    lse_s[row] = mm * k1 + __log2f(ll);
+                    lse_s[row] = -(mm * k1 + __log2f(ll));  // -lse2 of query row q
                 }
                 tc::mbar_arrive(lsef2);
                 if (!tc::mbar_wait(lsef2, lcn & 1, abort_flag, A.err)) {
@@ -285,17 +288,17 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                     break;
                 }
                 ++lcn;
-                const float4 *lse4 = reinterpret_cast<const float4 *>(lse_s + 64 * hf);
+                const float4 *nlse4 = reinterpret_cast<const float4 *>(lse_s + 64 * hf);
                 // phase 2: key row j = 128 b + row adds its probabilities under this half's
-                // query columns of the tile
+                // query columns of the tile; key tile b is complete after query tile r = b
                 const int qmax = A.P - 1 - 128 * r - 64 * hf;  // query column c valid iff c <= qmax
-                for (int b = r; b >= 0; --b) {
-                    const int j = 128 * b + row;
-                    const float prev = (r == nt - 1 || j >= A.P) ? 0.f : accu[j];
+#pragma unroll
+                for (int b = kHpMaxTiles - 1; b >= 0; --b) {
+                    if (b > r || !ok) continue;
                     const int ts = tcn % HP_TSLOTS;
                     if (!tc::mbar_wait(&tfull[ts], (tcn / HP_TSLOTS) & 1, abort_flag, A.err)) {
                         ok = false;
-                        break;
+                        continue;
                     }
                     tc::fence_after_sync();
                     float v[64];
@@ -303,17 +306,17 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                     tc::fence_before_sync();
                     tc::mbar_arrive(&tempty[ts]);
                     ++tcn;
+                    const int j = 128 * b + row;
                     const bool full = b < r && qmax >= 63;  // warp-uniform
                     const int lo = j - 128 * r - 64 * hf;   // query column c valid iff c >= lo
                     uint64_t s2[4] = {0, 0, 0, 0};
 #pragma unroll
                     for (int c = 0; c < 64; c += 4) {
-                        const float4 ls = lse4[c >> 2];
+                        const float4 nl = nlse4[c >> 2];
                         float ta, tb, tc_, td;
-                        tc::upk2(tc::fma2(tc::pk2(v[c], v[c + 1]), k1_2, tc::pk2(-ls.x, -ls.y)),
-                                 ta, tb);
-                        tc::upk2(tc::fma2(tc::pk2(v[c + 2], v[c + 3]), k1_2,
-                                          tc::pk2(-ls.z, -ls.w)),
+                        tc::upk2(tc::fma2(tc::pk2(v[c], v[c + 1]), k1_2, tc::pk2(nl.x, nl.y)), ta,
+                                 tb);
+                        tc::upk2(tc::fma2(tc::pk2(v[c + 2], v[c + 3]), k1_2, tc::pk2(nl.z, nl.w)),
                                  tc_, td);
                         float ea = tc::ex2_approx(ta), eb = tc::ex2_approx(tb);
                         float ec = tc::ex2_approx(tc_), ed = tc::ex2_approx(td);
@@ -333,7 +336,8 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                         tc::upk2(s2[k], a, bb);
                         bs += a + bb;
                     }
-                    if (j < A.P) accu[j] = prev + bs;
+                    accb[b] = (r == nt - 1 ? 0.f : accb[b]) + bs;
+                    if (b == r && j < A.P) accu[j] = accb[b];
                 }
             }
         }

@@ -117,7 +117,7 @@ __global__ void pack_queries_kernel(const __nv_bfloat16 *__restrict__ QW,
     for (int k = threadIdx.x; k < D.d; k += blockDim.x) dst[k] = src[k];
 }
 
-// Per-query constants of the scoring epilogue: {-lse2, c, weight, 0}.
+// Per-query constants of the scoring epilogue: {-lse2, c, w, 0}.
 __global__ void pack_qconst_kernel(const float *__restrict__ lse2, const float *__restrict__ cq,
                                    const float *__restrict__ wq, long rows,
                                    float4 *__restrict__ qconst) {
@@ -146,26 +146,34 @@ struct ScoresArgs {
     unsigned *err;
 };
 
-constexpr int kScThreads = 320;
+constexpr int kScThreads = 320;  // TMA, MMA issuer, 2 epilogue groups (one per head)
 // One CTA scores two query heads of a unit over a token range: every staged K/V tile serves both,
 // and the heads' operands are interleaved so that each MMA is wide (N = 128 or 256).
 // Shared memory:
 //   Q    2 K-blocks x 16 KB: rows [Q_h0 (64) | Q_h1 (64)]           -> B of S = K [Q_h0;Q_h1]^T
-//   B2   2 K-blocks x 48 KB: rows [U_h0 | U_h1 | Lt_h0 0-63 | Lt_h1 0-63 | Lt_h0 64-127 |
-//        Lt_h1 64-127] (64 rows each; Lt_h = L_h^T)                  -> B of V B2^T
-//   ring 3 x 32 KB TMA boxes (K_i, V_i, K_i+1, ...) | per-query constants | barriers.
-// TMEM (512 columns, one buffer): S_h0 | S_h1 | VU_h0 | VU_h1 | VLa_h0 | VLa_h1 | VLb_h0 | VLb_h1,
-// 64 columns each (VLa/VLb = columns 0-63 / 64-127 of V L_h). Rows 64..127 of L_h^T are zero for
-// k < 64, so VLb only takes the second K-block.
-constexpr int SC_HPC = 2;                          // query heads per CTA
-constexpr uint32_t SC_Q = 0, SC_B2 = 32768, SC_B2_BLK = 49152;
-constexpr uint32_t SC_RING = SC_B2 + 2 * SC_B2_BLK;        // 128 KB
+//   B2   rows [U_h0 | U_h1 | Lt_h0 0-63 | Lt_h1 0-63 | Lt_h0 64-127 | Lt_h1 64-127] (64 rows
+//        each; Lt_h = L_h^T) -> B of V B2^T. Rows 64..127 of L_h^T are zero for k < 64, so
+//        K-block 0 holds rows 0-255 (32 KB) and K-block 1 rows 0-383 (48 KB).
+//   ring 3 x 32 KB TMA boxes (V_i, K_i, V_i+1, ...) | per-query constants | per-set weights |
+//   barriers.
+// TMEM (512 columns, one buffer): S_h0 | S_h1 | X_h0 | X_h1 | Ya_h0 | Ya_h1 | Yb_h0 | Yb_h1,
+// 64 columns each (X = V U^T; Ya/Yb = columns 0-63 / 64-127 of Y = V L_h); Yb only takes the
+// second K-block of V.
+constexpr int SC_HPC = 2;                                  // query heads per CTA
+constexpr uint32_t SC_Q = 0, SC_B2 = 32768;
+constexpr uint32_t SC_B2_K0 = 0, SC_B2_K1 = 32768;         // K-block offsets inside B2
+constexpr uint32_t SC_RING = SC_B2 + 32768 + 49152;        // 112 KB
 constexpr int SC_SLOTS = 3;
-constexpr uint32_t SC_QC = SC_RING + SC_SLOTS * 32768;     // [2][32] float4 {-lse2, c} pairs
-constexpr uint32_t SC_QW = SC_QC + SC_HPC * 32 * 16;       // [2][32] float2 weight pairs
-constexpr uint32_t SC_BAR = SC_QW + SC_HPC * 32 * 8;
+constexpr uint32_t SC_QC = SC_RING + SC_SLOTS * 32768;     // [2][32] float4 {t pair, c pair}
+constexpr uint32_t SC_QW = SC_QC + SC_HPC * 32 * 16;       // [2][32] float2 -1/w pairs
+constexpr uint32_t SC_SW = SC_QW + SC_HPC * 32 * 8;        // [2][8] per-set weights
+constexpr uint32_t SC_BAR = SC_SW + SC_HPC * 8 * 4;
+// Query layout with compile-time sets: w = 32 window queries, then M = 4 trajectories of T = 8
+// lookahead queries; pairs 0-15 are the window, pairs 16 + 4m .. 19 + 4m trajectory m.
+constexpr int kSetW = 32, kSetM = 4, kSetT = 8;
 constexpr size_t SC_SMEM = SC_BAR + 256 + 1024;
 
+template <bool kFixedSets>
 __global__ void __launch_bounds__(kScThreads, 1)
     scores_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_u,
@@ -187,10 +195,13 @@ __global__ void __launch_bounds__(kScThreads, 1)
     const int kh = unit % A.Hkv, l = (unit / A.Hkv) % A.L;
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SC_BAR);
+    // tfull1/tfree1: the V-tile products X, Y (columns 128-511); tfull2/tfree2: S (columns 0-127)
     uint64_t *ops_full = bars + 0, *rfull = bars + 1, *rempty = bars + 1 + SC_SLOTS,
-             *tfull = bars + 1 + 2 * SC_SLOTS, *tempty = bars + 2 + 2 * SC_SLOTS;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 + 2 * SC_SLOTS);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 4 + 2 * SC_SLOTS);
+             *tfull1 = bars + 1 + 2 * SC_SLOTS, *tfree1 = tfull1 + 1, *tfull2 = tfull1 + 2,
+             *tfree2 = tfull1 + 3;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tfull1 + 4);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tfull1 + 5);
+    float *sw = reinterpret_cast<float *>(sm + SC_SW);
     float4 *qc = reinterpret_cast<float4 *>(sm + SC_QC);
     float2 *qw = reinterpret_cast<float2 *>(sm + SC_QW);
 
@@ -200,8 +211,10 @@ __global__ void __launch_bounds__(kScThreads, 1)
             tc::mbar_init(&rfull[s], 1);
             tc::mbar_init(&rempty[s], 1);
         }
-        tc::mbar_init(tfull, 1);
-        tc::mbar_init(tempty, 128 * nh);  // every epilogue thread has read the tile
+        tc::mbar_init(tfull1, 1);
+        tc::mbar_init(tfull2, 1);
+        tc::mbar_init(tfree1, 128 * nh);  // every epilogue thread has read the columns
+        tc::mbar_init(tfree2, 128 * nh);
         *abort_flag = 0;
         tc::mbar_fence_init();
     }
@@ -217,8 +230,20 @@ __global__ void __launch_bounds__(kScThreads, 1)
             if (2 * t < A.nq) c0 = A.qconst[row0 + 2 * t];
             if (2 * t + 1 < A.nq) c1 = A.qconst[row0 + 2 * t + 1];
         }
-        qc[hh * 32 + t] = make_float4(c0.x, c1.x, c0.y, c1.y);  // -lse2 pair, c pair
-        qw[hh * 32 + t] = make_float2(c0.z, c1.z);              // weight pair
+        if (kFixedSets) {
+            // {-lse2 pair, c pair}; the weight is per set: window, then one per trajectory
+            qc[hh * 32 + t] = make_float4(c0.x, c1.x, c0.y, c1.y);
+            if (t == 0) sw[hh * 8] = c0.z;
+            if (t >= 16 && (t & 3) == 0) sw[hh * 8 + 1 + ((t - 16) >> 2)] = c0.z;
+        } else {
+            // {log2(w) - lse2 pair, c pair} and -1/w: w a = exp2(s log2e/sqrt(d) + log2(w) - lse2)
+            // from one exp2 and a = (w a) / w; weight 0 contributes nothing (exp2(-inf) = 0)
+            const float ta = c0.z > 0.f ? log2f(c0.z) + c0.x : -INFINITY;
+            const float tb = c1.z > 0.f ? log2f(c1.z) + c1.x : -INFINITY;
+            qc[hh * 32 + t] = make_float4(ta, tb, c0.y, c1.y);
+            qw[hh * 32 + t] = make_float2(c0.z > 0.f ? -1.f / c0.z : 0.f,
+                                          c1.z > 0.f ? -1.f / c1.z : 0.f);
+        }
     }
     __syncthreads();
     tc::fence_after_sync();
@@ -226,17 +251,17 @@ __global__ void __launch_bounds__(kScThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {  // ---- TMA producer ----
-            tc::mbar_expect_tx(ops_full, 65536u * nh);
+            tc::mbar_expect_tx(ops_full, 57344u * nh);
             for (int hh = 0; hh < nh; ++hh) {
                 const int qrow = unit * A.Qu + (j0 + hh) * A.nq;
                 const int lrow = (l * A.Hq + kh * A.g + j0 + hh) * 128;
                 for (int kb = 0; kb < 2; ++kb) {
-                    uint8_t *b2 = sm + SC_B2 + kb * SC_B2_BLK + hh * 8192;
+                    uint8_t *b2 = sm + SC_B2 + (kb ? SC_B2_K1 : SC_B2_K0) + hh * 8192;
                     tc::tma_load_2d(sm + SC_Q + kb * 16384 + hh * 8192, &tm_q, 64 * kb, qrow,
                                     ops_full);
                     tc::tma_load_2d(b2, &tm_u, 64 * kb, qrow, ops_full);
                     tc::tma_load_2d(b2 + 16384, &tm_lt, 64 * kb, lrow, ops_full);
-                    tc::tma_load_2d(b2 + 32768, &tm_lt, 64 * kb, lrow + 64, ops_full);
+                    if (kb) tc::tma_load_2d(b2 + 32768, &tm_lt, 64 * kb, lrow + 64, ops_full);
                 }
             }
             for (int c = 0; c < 2 * ntl; ++c) {
@@ -245,7 +270,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
                 if (!tc::mbar_wait(&rempty[slot], ph ^ 1, abort_flag, A.err)) break;
                 tc::mbar_expect_tx(&rfull[slot], 32768);
                 const int row = unit * A.n + (t_begin + (c >> 1)) * 128;
-                const CUtensorMap *map = (c & 1) ? &tm_v : &tm_k;
+                const CUtensorMap *map = (c & 1) ? &tm_k : &tm_v;  // V_i, K_i, V_i+1, ...
                 uint8_t *dst = sm + SC_RING + slot * 32768;
                 tc::tma_load_2d(dst, map, 0, row, &rfull[slot]);
                 tc::tma_load_2d(dst + 16384, map, 64, row, &rfull[slot]);
@@ -260,42 +285,48 @@ __global__ void __launch_bounds__(kScThreads, 1)
             constexpr uint32_t id128 = tc::idesc_bf16(128, 128, 0);
             constexpr uint32_t id256 = tc::idesc_bf16(128, 256, 0);
             for (int i = 0; i < ntl; ++i) {
-                const int ck = 2 * i, cv = 2 * i + 1;
-                const int sk = ck % SC_SLOTS, sv = cv % SC_SLOTS;
+                const int cv = 2 * i, ck = 2 * i + 1;
+                const int sv = cv % SC_SLOTS, sk = ck % SC_SLOTS;
+                // group 1: [X_h0 | X_h1 | Ya_h0 | Ya_h1] = V [U_h0; U_h1; L_h0^T(0:64); L_h1^T(0:64)]^T
+                // and [Yb_h0 | Yb_h1] from the second K-block of V
+                if (!tc::mbar_wait(&rfull[sv], (cv / SC_SLOTS) & 1, abort_flag, A.err)) break;
+                if (!tc::mbar_wait(tfree1, (i & 1) ^ 1, abort_flag, A.err)) break;
+                tc::fence_after_sync();
+                const uint32_t v_addr = ring + sv * 32768;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;
+                    const uint32_t bo = ((k >> 2) ? SC_B2_K1 : SC_B2_K0) + (k & 3) * 32;
+                    tc::mma_bf16(tmem + 128, tc::sdesc_sw128(v_addr + ao, 16, 1024),
+                                 tc::sdesc_sw128(b2_addr + bo, 16, 1024), id256, k > 0);
+                }
+#pragma unroll
+                for (int k = 4; k < 8; ++k) {
+                    const uint32_t ao = 16384 + (k & 3) * 32;
+                    const uint32_t bo = SC_B2_K1 + 32768 + (k & 3) * 32;
+                    tc::mma_bf16(tmem + 384, tc::sdesc_sw128(v_addr + ao, 16, 1024),
+                                 tc::sdesc_sw128(b2_addr + bo, 16, 1024), id128, k > 4);
+                }
+                tc::mma_commit(&rempty[sv]);
+                tc::mma_commit(tfull1);
+                // group 2: [S_h0 | S_h1] = K [Q_h0; Q_h1]^T
                 if (!tc::mbar_wait(&rfull[sk], (ck / SC_SLOTS) & 1, abort_flag, A.err)) break;
-                if (!tc::mbar_wait(tempty, (i & 1) ^ 1, abort_flag, A.err)) break;
+                if (!tc::mbar_wait(tfree2, (i & 1) ^ 1, abort_flag, A.err)) break;
                 tc::fence_after_sync();
                 const uint32_t k_addr = ring + sk * 32768;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {  // [S_h0 | S_h1] = K [Q_h0 ; Q_h1]^T
+                for (int k = 0; k < 8; ++k) {
                     const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
                     tc::mma_bf16(tmem, tc::sdesc_sw128(k_addr + o, 16, 1024),
                                  tc::sdesc_sw128(q_addr + o, 16, 1024), id128, k > 0);
                 }
                 tc::mma_commit(&rempty[sk]);
-                if (!tc::mbar_wait(&rfull[sv], (cv / SC_SLOTS) & 1, abort_flag, A.err)) break;
-                tc::fence_after_sync();
-                const uint32_t v_addr = ring + sv * 32768;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {  // [VU_h0 | VU_h1 | VLa_h0 | VLa_h1]
-                    const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;
-                    const uint32_t bo = (k >> 2) * SC_B2_BLK + (k & 3) * 32;
-                    tc::mma_bf16(tmem + 128, tc::sdesc_sw128(v_addr + ao, 16, 1024),
-                                 tc::sdesc_sw128(b2_addr + bo, 16, 1024), id256, k > 0);
-                }
-#pragma unroll
-                for (int k = 4; k < 8; ++k) {  // [VLb_h0 | VLb_h1]: second K-block only
-                    const uint32_t ao = 16384 + (k & 3) * 32;
-                    const uint32_t bo = SC_B2_BLK + 32768 + (k & 3) * 32;
-                    tc::mma_bf16(tmem + 384, tc::sdesc_sw128(v_addr + ao, 16, 1024),
-                                 tc::sdesc_sw128(b2_addr + bo, 16, 1024), id128, k > 4);
-                }
-                tc::mma_commit(&rempty[sv]);
-                tc::mma_commit(tfull);
+                tc::mma_commit(tfull2);
             }
         }
     } else if ((warp - 2) >> 2 < nh) {
-        // ---- epilogue: group hh (warps 2-5 -> head 0, 6-9 -> head 1) ----
+        // ---- epilogue: group hh (warps 2-5 -> head 0, 6-9 -> head 1); warp w reads TMEM lanes
+        // 32 (w % 4) .. +31 ----
         const int hh = (warp - 2) >> 2, lg = warp & 3;
         const int row = lg * 32 + lane;
         const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
@@ -303,51 +334,65 @@ __global__ void __launch_bounds__(kScThreads, 1)
         const float one_eps = 1.f + A.eps;
         const float4 *qch = qc + hh * 32;
         const float2 *qwh = qw + hh * 32;
+        const uint64_t k1_2 = tc::pk2(A.k1, A.k1), m2_2 = tc::pk2(-2.f, -2.f);
+        const uint64_t one_2 = tc::pk2(one_eps, one_eps), neg1_2 = tc::pk2(-1.f, -1.f);
+        float wset[1 + kSetM];
+#pragma unroll
+        for (int k = 0; k < 1 + kSetM; ++k) wset[k] = kFixedSets ? sw[hh * 8 + k] : 0.f;
         for (int i = 0; i < ntl; ++i) {
-            if (!tc::mbar_wait(tfull, i & 1, abort_flag, A.err)) break;
+            if (!tc::mbar_wait(tfull1, i & 1, abort_flag, A.err)) break;
             tc::fence_after_sync();
             const uint32_t tb = tmem + lane_off;
-            float nv;
+            // ||L_h^T v||^2 of this thread's token (the 128 columns of Y), and X
+            float x0[32], x1[32];
+            uint64_t np2[4] = {0, 0, 0, 0};  // bit pattern 0 = (0.f, 0.f)
             {
-                float y0[32], y1[32], np[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) np[k] = 0.f;
+                float y0[32], y1[32];
                 tc::tmem_ld32(tb + 256 + 64 * hh, y0);
                 tc::tmem_ld32(tb + 288 + 64 * hh, y1);
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    np[c & 7] = fmaf(y0[c], y0[c], np[c & 7]);
-                    np[c & 7] = fmaf(y1[c], y1[c], np[c & 7]);
+                for (int c = 0; c < 32; c += 2) {
+                    const uint64_t a = tc::pk2(y0[c], y0[c + 1]), b = tc::pk2(y1[c], y1[c + 1]);
+                    np2[(c >> 1) & 3] = tc::fma2(a, a, np2[(c >> 1) & 3]);
+                    np2[(c >> 1) & 3] = tc::fma2(b, b, np2[(c >> 1) & 3]);
                 }
                 tc::tmem_ld32(tb + 384 + 64 * hh, y0);
                 tc::tmem_ld32(tb + 416 + 64 * hh, y1);
+                tc::tmem_ld32(tb + 128 + 64 * hh, x0);
+                tc::tmem_ld32(tb + 160 + 64 * hh, x1);
                 tc::tmem_wait_ld();
+                tc::fence_before_sync();
+                tc::mbar_arrive(tfree1);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    np[c & 7] = fmaf(y0[c], y0[c], np[c & 7]);
-                    np[c & 7] = fmaf(y1[c], y1[c], np[c & 7]);
+                for (int c = 0; c < 32; c += 2) {
+                    const uint64_t a = tc::pk2(y0[c], y0[c + 1]), b = tc::pk2(y1[c], y1[c + 1]);
+                    np2[(c >> 1) & 3] = tc::fma2(a, a, np2[(c >> 1) & 3]);
+                    np2[(c >> 1) & 3] = tc::fma2(b, b, np2[(c >> 1) & 3]);
                 }
-                nv = ((np[0] + np[1]) + (np[2] + np[3])) + ((np[4] + np[5]) + (np[6] + np[7]));
             }
-            float s0[32], s1[32], x0[32], x1[32];
+            float nv;
+            {
+                float n[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) tc::upk2(np2[k], n[2 * k], n[2 * k + 1]);
+                nv = ((n[0] + n[1]) + (n[2] + n[3])) + ((n[4] + n[5]) + (n[6] + n[7]));
+            }
+            if (!tc::mbar_wait(tfull2, i & 1, abort_flag, A.err)) break;
+            tc::fence_after_sync();
+            float s0[32], s1[32];
             tc::tmem_ld32(tb + 64 * hh, s0);
             tc::tmem_ld32(tb + 64 * hh + 32, s1);
-            tc::tmem_ld32(tb + 128 + 64 * hh, x0);
-            tc::tmem_ld32(tb + 160 + 64 * hh, x1);
             tc::tmem_wait_ld();
             tc::fence_before_sync();
-            tc::mbar_arrive(tempty);
-            // e = w a sqrt(x) / (1 - a + eps) for two queries per packed FP32 instruction
-            const uint64_t k1_2 = tc::pk2(A.k1, A.k1), m2_2 = tc::pk2(-2.f, -2.f);
-            const uint64_t one_2 = tc::pk2(one_eps, one_eps), neg1_2 = tc::pk2(-1.f, -1.f);
+            tc::mbar_arrive(tfree2);
+            // e = a sqrt(x) / (1 - a + eps) for two queries per packed FP32 instruction, with
+            // x = ||L^T v||^2 - 2 v.u + c and sqrt(x) / dd = x rsqrt(x dd^2)
             const uint64_t nv_2 = tc::pk2(nv, nv);
-            uint64_t acc2[4] = {tc::pk2(0.f, 0.f), tc::pk2(0.f, 0.f), tc::pk2(0.f, 0.f),
-                                tc::pk2(0.f, 0.f)};
+            uint64_t acc2[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
             for (int p = 0; p < 32; ++p) {
                 const float4 ca = qch[p];
-                const float2 cw = qwh[p];
                 const float sa = (p < 16) ? s0[2 * p] : s1[2 * p - 32];
                 const float sb = (p < 16) ? s0[2 * p + 1] : s1[2 * p - 31];
                 const float xa = (p < 16) ? x0[2 * p] : x1[2 * p - 32];
@@ -358,19 +403,46 @@ __global__ void __launch_bounds__(kScThreads, 1)
                 float ya, yb;
                 tc::upk2(tc::fma2(tc::pk2(xa, xb), m2_2, tc::add2(nv_2, tc::pk2(ca.z, ca.w))), ya, yb);
                 const uint64_t x2 = tc::pk2(fmaxf(ya, 1e-30f), fmaxf(yb, 1e-30f));
-                const uint64_t dd2 = tc::fma2(a2, neg1_2, one_2);
                 float za, zb;
-                tc::upk2(tc::mul2(tc::mul2(x2, dd2), dd2), za, zb);
-                const uint64_t r2 = tc::pk2(tc::rsqrt_approx(za), tc::rsqrt_approx(zb));
-                acc2[p & 3] = tc::fma2(tc::mul2(tc::mul2(tc::pk2(cw.x, cw.y), a2), x2), r2,
-                                       acc2[p & 3]);
+                if (kFixedSets) {
+                    // a unweighted; the set's weight is applied once at the end
+                    const uint64_t dd2 = tc::fma2(a2, neg1_2, one_2);
+                    tc::upk2(tc::mul2(tc::mul2(x2, dd2), dd2), za, zb);
+                    const uint64_t r2 = tc::pk2(tc::rsqrt_approx(za), tc::rsqrt_approx(zb));
+                    const int slot = p < 16 ? (p & 3) : 4 + ((p - 16) >> 2);
+                    acc2[slot] = tc::fma2(tc::mul2(a2, x2), r2, acc2[slot]);
+                } else {
+                    // a2 holds w a: dd = 1 + eps - (w a) / w
+                    const float2 cw = qwh[p];
+                    const uint64_t dd2 = tc::fma2(a2, tc::pk2(cw.x, cw.y), one_2);
+                    tc::upk2(tc::mul2(tc::mul2(x2, dd2), dd2), za, zb);
+                    const uint64_t r2 = tc::pk2(tc::rsqrt_approx(za), tc::rsqrt_approx(zb));
+                    acc2[p & 3] = tc::fma2(tc::mul2(a2, x2), r2, acc2[p & 3]);
+                }
             }
             float acc = 0.f;
+            if (kFixedSets) {
+                float win = 0.f;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                float acca, accb;
-                tc::upk2(acc2[k], acca, accb);
-                acc += acca + accb;
+                for (int k = 0; k < 4; ++k) {
+                    float u, v;
+                    tc::upk2(acc2[k], u, v);
+                    win += u + v;
+                }
+                acc = wset[0] * win;
+#pragma unroll
+                for (int m = 0; m < kSetM; ++m) {
+                    float u, v;
+                    tc::upk2(acc2[4 + m], u, v);
+                    acc = fmaf(wset[1 + m], u + v, acc);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float u, v;
+                    tc::upk2(acc2[k], u, v);
+                    acc += u + v;
+                }
             }
             const int tok = (t_begin + i) * 128 + row;
             if (tok < A.n) out[tok] = (tok >= A.sink && tok < A.n - A.w) ? acc : 0.f;
@@ -735,10 +807,13 @@ cudaError_t launch_scores_tc(const LorekvDims &D, const void *K, const void *V, 
     A.qconst = reinterpret_cast<const float4 *>(b + W.qconst);
     A.part_s = reinterpret_cast<float *>(b + W.part_s);
     A.err = err;
-    cudaError_t e = cudaFuncSetAttribute(scores_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SC_SMEM);
+    // the window / trajectory layout of the configured workloads gets compile-time query sets
+    const bool fixed_sets = D.w == kSetW && D.M == kSetM && D.T == kSetT;
+    auto kern = fixed_sets ? scores_tc_kernel<true> : scores_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SC_SMEM);
     if (e != cudaSuccess) return e;
-    scores_tc_kernel<<<D.units * A.nranges * npairs, kScThreads, SC_SMEM, st>>>(tk, tv, tq, tu, tl, A);
+    kern<<<D.units * A.nranges * npairs, kScThreads, SC_SMEM, st>>>(tk, tv, tq, tu, tl, A);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     reduce_heads_kernel<<<dim3((D.n + 255) / 256, D.units), 256, 0, st>>>(
