@@ -237,10 +237,10 @@ __global__ void __launch_bounds__(256) prep_u_kernel(LorekvDims D, const float *
                 const size_t row = row0 + r;
 #pragma unroll
                 for (int b = 0; b < 8; ++b) u32[row * d + jb * 8 + b] = acc[a][b];
-                if (u16)
+                if (u16)  // -2 u_q (exact scaling of the rounded u_q): B operand of X = -2 V U^T
 #pragma unroll
                     for (int b = 0; b < 8; ++b)
-                        u16[row * d + jb * 8 + b] = __float2bfloat16_rn(acc[a][b]);
+                        u16[row * d + jb * 8 + b] = __float2bfloat16_rn(-2.f * acc[a][b]);
                 if (jb == 0) cq[row] = cpart;
             }
         }

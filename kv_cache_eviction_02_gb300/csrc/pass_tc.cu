@@ -154,8 +154,13 @@ constexpr int kScThreads = 320;  // TMA, MMA issuer, 2 epilogue groups (one per 
 //   B2   rows [U_h0 | U_h1 | Lt_h0 0-63 | Lt_h1 0-63 | Lt_h0 64-127 | Lt_h1 64-127] (64 rows
 //        each; Lt_h = L_h^T) -> B of V B2^T. Rows 64..127 of L_h^T are zero for k < 64, so
 //        K-block 0 holds rows 0-255 (32 KB) and K-block 1 rows 0-383 (48 KB).
-//   ring 3 x 32 KB TMA boxes (V_i, K_i, V_i+1, ...) | per-query constants | per-set weights |
-//   barriers.
+//   ring 3 x 32 KB TMA boxes (V_i, K_i, V_i+1, ...).
+//   one extra K step (32-byte swizzle, 16 bf16 per row) that adds per-query constants inside the
+//   MMAs: A_aug (128 token rows [1, 1, 1, 0, ...]), B_aug_S (the 128 query rows of S: -lse2/k1
+//   split into three bf16 terms) and B_aug_V (the 128 query rows of X: c split into three bf16
+//   terms, then 128 zero rows under Y). With U staged as -2u, the MMAs give S' = s - lse2/k1 and
+//   X' = c - 2 v.u directly.
+//   per-query weights (general query layout) | per-set weights | barriers.
 // TMEM (512 columns, one buffer): S_h0 | S_h1 | X_h0 | X_h1 | Ya_h0 | Ya_h1 | Yb_h0 | Yb_h1,
 // 64 columns each (X = V U^T; Ya/Yb = columns 0-63 / 64-127 of Y = V L_h); Yb only takes the
 // second K-block of V.
@@ -164,14 +169,34 @@ constexpr uint32_t SC_Q = 0, SC_B2 = 32768;
 constexpr uint32_t SC_B2_K0 = 0, SC_B2_K1 = 32768;         // K-block offsets inside B2
 constexpr uint32_t SC_RING = SC_B2 + 32768 + 49152;        // 112 KB
 constexpr int SC_SLOTS = 3;
-constexpr uint32_t SC_QC = SC_RING + SC_SLOTS * 32768;     // [2][32] float4 {t pair, c pair}
-constexpr uint32_t SC_QW = SC_QC + SC_HPC * 32 * 16;       // [2][32] float2 -1/w pairs
+constexpr uint32_t SC_AUG_A = SC_RING + SC_SLOTS * 32768;  // 128 rows x 32 B
+constexpr uint32_t SC_AUG_S = SC_AUG_A + 4096;             // 128 rows x 32 B
+constexpr uint32_t SC_AUG_V = SC_AUG_S + 4096;             // 256 rows x 32 B
+constexpr uint32_t SC_QW = SC_AUG_V + 8192;                // [2][32] float2 weight pairs
 constexpr uint32_t SC_SW = SC_QW + SC_HPC * 32 * 8;        // [2][8] per-set weights
 constexpr uint32_t SC_BAR = SC_SW + SC_HPC * 8 * 4;
+constexpr size_t SC_SMEM = SC_BAR + 256 + 1024;
 // Query layout with compile-time sets: w = 32 window queries, then M = 4 trajectories of T = 8
 // lookahead queries; pairs 0-15 are the window, pairs 16 + 4m .. 19 + 4m trajectory m.
 constexpr int kSetW = 32, kSetM = 4, kSetT = 8;
-constexpr size_t SC_SMEM = SC_BAR + 256 + 1024;
+
+// v as the sum of three bf16 terms (relative error about 2^-24); a value below -1e30 (a padded
+// query's -inf) becomes (-1e30, 0, 0).
+__device__ __forceinline__ void split3_bf16(float v, __nv_bfloat16 *dst0, __nv_bfloat16 *dst1,
+                                            __nv_bfloat16 *dst2) {
+    if (!(v > -1e30f)) {
+        *dst0 = __float2bfloat16_rn(-1e30f);
+        *dst1 = *dst2 = __float2bfloat16_rn(0.f);
+        return;
+    }
+    const __nv_bfloat16 a = __float2bfloat16_rn(v);
+    float r = v - __bfloat162float(a);
+    const __nv_bfloat16 b = __float2bfloat16_rn(r);
+    r -= __bfloat162float(b);
+    *dst0 = a;
+    *dst1 = b;
+    *dst2 = __float2bfloat16_rn(r);
+}
 
 template <bool kFixedSets>
 __global__ void __launch_bounds__(kScThreads, 1)
@@ -202,7 +227,6 @@ __global__ void __launch_bounds__(kScThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tfull1 + 4);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tfull1 + 5);
     float *sw = reinterpret_cast<float *>(sm + SC_SW);
-    float4 *qc = reinterpret_cast<float4 *>(sm + SC_QC);
     float2 *qw = reinterpret_cast<float2 *>(sm + SC_QW);
 
     if (threadIdx.x == 0) {
@@ -222,29 +246,35 @@ __global__ void __launch_bounds__(kScThreads, 1)
         tc::tmem_alloc(tmem_slot, 512);
         tc::fence_before_sync();
     }
-    if (threadIdx.x >= 64 && threadIdx.x < 64 + 32 * SC_HPC) {  // query pairs (2t, 2t+1)
-        const int hh = (threadIdx.x - 64) >> 5, t = (threadIdx.x - 64) & 31;
-        float4 c0 = make_float4(-INFINITY, 0.f, 0.f, 0.f), c1 = c0;
-        if (hh < nh) {
-            const size_t row0 = (size_t)unit * A.Qu + (size_t)(j0 + hh) * A.nq;
-            if (2 * t < A.nq) c0 = A.qconst[row0 + 2 * t];
-            if (2 * t + 1 < A.nq) c1 = A.qconst[row0 + 2 * t + 1];
-        }
+    // the augmentation K step: zero it, then write the ones of A_aug and the constants of the queries
+    for (int e = threadIdx.x; e < 16384 / 16; e += blockDim.x)
+        reinterpret_cast<uint4 *>(sm + SC_AUG_A)[e] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    if (threadIdx.x < 128) {
+        __nv_bfloat16 *aa = reinterpret_cast<__nv_bfloat16 *>(sm + SC_AUG_A);
+        const __nv_bfloat16 one = __float2bfloat16_rn(1.f);
+        for (int k = 0; k < 3; ++k) aa[tc::sw32_offset(threadIdx.x, k) / 2] = one;
+    }
+    if (threadIdx.x >= 128 && threadIdx.x < 128 + 64 * SC_HPC) {  // one query each
+        const int q = threadIdx.x - 128;                           // B row: head q / 64
+        const int hh = q >> 6, r = q & 63;
+        float4 c = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+        if (hh < nh && r < A.nq) c = A.qconst[(size_t)unit * A.Qu + (size_t)(j0 + hh) * A.nq + r];
+        __nv_bfloat16 *bs = reinterpret_cast<__nv_bfloat16 *>(sm + SC_AUG_S);
+        __nv_bfloat16 *bv = reinterpret_cast<__nv_bfloat16 *>(sm + SC_AUG_V);
+        const uint32_t o0 = tc::sw32_offset(q, 0) / 2, o1 = tc::sw32_offset(q, 1) / 2,
+                       o2 = tc::sw32_offset(q, 2) / 2;
+        split3_bf16(c.x / A.k1, bs + o0, bs + o1, bs + o2);  // -lse2 / k1
+        split3_bf16(c.y, bv + o0, bv + o1, bv + o2);         // c
         if (kFixedSets) {
-            // {-lse2 pair, c pair}; the weight is per set: window, then one per trajectory
-            qc[hh * 32 + t] = make_float4(c0.x, c1.x, c0.y, c1.y);
-            if (t == 0) sw[hh * 8] = c0.z;
-            if (t >= 16 && (t & 3) == 0) sw[hh * 8 + 1 + ((t - 16) >> 2)] = c0.z;
+            // the weight is per set: window, then one per trajectory
+            if (r == 0) sw[hh * 8] = c.z;
+            if (r >= kSetW && (r - kSetW) % kSetT == 0) sw[hh * 8 + 1 + (r - kSetW) / kSetT] = c.z;
         } else {
-            // {log2(w) - lse2 pair, c pair} and -1/w: w a = exp2(s log2e/sqrt(d) + log2(w) - lse2)
-            // from one exp2 and a = (w a) / w; weight 0 contributes nothing (exp2(-inf) = 0)
-            const float ta = c0.z > 0.f ? log2f(c0.z) + c0.x : -INFINITY;
-            const float tb = c1.z > 0.f ? log2f(c1.z) + c1.x : -INFINITY;
-            qc[hh * 32 + t] = make_float4(ta, tb, c0.y, c1.y);
-            qw[hh * 32 + t] = make_float2(c0.z > 0.f ? -1.f / c0.z : 0.f,
-                                          c1.z > 0.f ? -1.f / c1.z : 0.f);
+            reinterpret_cast<float *>(qw)[hh * 64 + r] = c.z;  // weight pairs (2t, 2t+1)
         }
     }
+    tc::fence_proxy_async_smem();  // generic-proxy writes -> MMA operand reads
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
@@ -282,6 +312,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
             const uint32_t ring = tc::smem_u32(sm + SC_RING);
             const uint32_t q_addr = tc::smem_u32(sm + SC_Q);
             const uint32_t b2_addr = tc::smem_u32(sm + SC_B2);
+            const uint32_t aug_a = tc::smem_u32(sm + SC_AUG_A), aug_s = tc::smem_u32(sm + SC_AUG_S),
+                           aug_v = tc::smem_u32(sm + SC_AUG_V);
             constexpr uint32_t id128 = tc::idesc_bf16(128, 128, 0);
             constexpr uint32_t id256 = tc::idesc_bf16(128, 256, 0);
             for (int i = 0; i < ntl; ++i) {
@@ -300,6 +332,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
                     tc::mma_bf16(tmem + 128, tc::sdesc_sw128(v_addr + ao, 16, 1024),
                                  tc::sdesc_sw128(b2_addr + bo, 16, 1024), id256, k > 0);
                 }
+                tc::mma_bf16(tmem + 128, tc::sdesc_sw32(aug_a), tc::sdesc_sw32(aug_v), id256, 1);
 #pragma unroll
                 for (int k = 4; k < 8; ++k) {
                     const uint32_t ao = 16384 + (k & 3) * 32;
@@ -320,6 +353,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
                     tc::mma_bf16(tmem, tc::sdesc_sw128(k_addr + o, 16, 1024),
                                  tc::sdesc_sw128(q_addr + o, 16, 1024), id128, k > 0);
                 }
+                tc::mma_bf16(tmem, tc::sdesc_sw32(aug_a), tc::sdesc_sw32(aug_s), id128, 1);
                 tc::mma_commit(&rempty[sk]);
                 tc::mma_commit(tfull2);
             }
@@ -332,9 +366,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
         const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
         float *out = A.part_s + ((size_t)unit * A.g + j0 + hh) * A.n;
         const float one_eps = 1.f + A.eps;
-        const float4 *qch = qc + hh * 32;
         const float2 *qwh = qw + hh * 32;
-        const uint64_t k1_2 = tc::pk2(A.k1, A.k1), m2_2 = tc::pk2(-2.f, -2.f);
+        const uint64_t k1_2 = tc::pk2(A.k1, A.k1);
         const uint64_t one_2 = tc::pk2(one_eps, one_eps), neg1_2 = tc::pk2(-1.f, -1.f);
         float wset[1 + kSetM];
 #pragma unroll
@@ -387,37 +420,33 @@ __global__ void __launch_bounds__(kScThreads, 1)
             tc::fence_before_sync();
             tc::mbar_arrive(tfree2);
             // e = a sqrt(x) / (1 - a + eps) for two queries per packed FP32 instruction, with
-            // x = ||L^T v||^2 - 2 v.u + c and sqrt(x) / dd = x rsqrt(x dd^2)
+            // a = exp2(S' k1) (S' = s - lse2/k1), x = ||L^T v||^2 + X' (X' = c - 2 v.u) and
+            // sqrt(x) / dd = x rsqrt(x dd^2)
             const uint64_t nv_2 = tc::pk2(nv, nv);
             uint64_t acc2[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
             for (int p = 0; p < 32; ++p) {
-                const float4 ca = qch[p];
                 const float sa = (p < 16) ? s0[2 * p] : s1[2 * p - 32];
                 const float sb = (p < 16) ? s0[2 * p + 1] : s1[2 * p - 31];
                 const float xa = (p < 16) ? x0[2 * p] : x1[2 * p - 32];
                 const float xb = (p < 16) ? x0[2 * p + 1] : x1[2 * p - 31];
                 float ea, eb;
-                tc::upk2(tc::fma2(tc::pk2(sa, sb), k1_2, tc::pk2(ca.x, ca.y)), ea, eb);
+                tc::upk2(tc::mul2(tc::pk2(sa, sb), k1_2), ea, eb);
                 const uint64_t a2 = tc::pk2(tc::ex2_approx(ea), tc::ex2_approx(eb));
                 float ya, yb;
-                tc::upk2(tc::fma2(tc::pk2(xa, xb), m2_2, tc::add2(nv_2, tc::pk2(ca.z, ca.w))), ya, yb);
+                tc::upk2(tc::add2(tc::pk2(xa, xb), nv_2), ya, yb);
                 const uint64_t x2 = tc::pk2(fmaxf(ya, 1e-30f), fmaxf(yb, 1e-30f));
+                const uint64_t dd2 = tc::fma2(a2, neg1_2, one_2);
                 float za, zb;
-                if (kFixedSets) {
-                    // a unweighted; the set's weight is applied once at the end
-                    const uint64_t dd2 = tc::fma2(a2, neg1_2, one_2);
-                    tc::upk2(tc::mul2(tc::mul2(x2, dd2), dd2), za, zb);
-                    const uint64_t r2 = tc::pk2(tc::rsqrt_approx(za), tc::rsqrt_approx(zb));
+                tc::upk2(tc::mul2(tc::mul2(x2, dd2), dd2), za, zb);
+                const uint64_t r2 = tc::pk2(tc::rsqrt_approx(za), tc::rsqrt_approx(zb));
+                if (kFixedSets) {  // unweighted; the set's weight is applied once at the end
                     const int slot = p < 16 ? (p & 3) : 4 + ((p - 16) >> 2);
                     acc2[slot] = tc::fma2(tc::mul2(a2, x2), r2, acc2[slot]);
                 } else {
-                    // a2 holds w a: dd = 1 + eps - (w a) / w
                     const float2 cw = qwh[p];
-                    const uint64_t dd2 = tc::fma2(a2, tc::pk2(cw.x, cw.y), one_2);
-                    tc::upk2(tc::mul2(tc::mul2(x2, dd2), dd2), za, zb);
-                    const uint64_t r2 = tc::pk2(tc::rsqrt_approx(za), tc::rsqrt_approx(zb));
-                    acc2[p & 3] = tc::fma2(tc::mul2(a2, x2), r2, acc2[p & 3]);
+                    acc2[p & 3] = tc::fma2(tc::mul2(tc::mul2(a2, tc::pk2(cw.x, cw.y)), x2), r2,
+                                           acc2[p & 3]);
                 }
             }
             float acc = 0.f;

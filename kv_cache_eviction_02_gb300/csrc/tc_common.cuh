@@ -200,6 +200,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr, uint32_t lbo, uin
            (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// Shared-memory matrix descriptor of a 32-byte-swizzled K-major operand of one K step (16 bf16 per
+// row): 8-row atoms of 256 bytes, 256-byte aligned.
+__device__ __forceinline__ uint64_t sdesc_sw32(uint32_t addr) {
+    return uint64_t((addr >> 4) & 0x3FFFu) | (uint64_t(1) << 16) | (uint64_t(256 >> 4) << 32) |
+           (1ull << 46) | (6ull << 61);
+}
+// Byte offset of element k (0..15) of row r in the 32-byte-swizzled K-major layout: 16-byte chunk
+// k / 8 of the row is stored at chunk (k / 8) ^ ((r / 4) & 1).
+__device__ __forceinline__ uint32_t sw32_offset(uint32_t r, uint32_t k) {
+    return (r >> 3) * 256u + (r & 7u) * 32u + ((((k >> 3) ^ (r >> 2)) & 1u) << 4) + (k & 7u) * 2u;
+}
+
 // bf16 x 8 (16 bytes) of an operand row written by threads into the 128-byte-swizzled K-major
 // layout: row r, 16-byte chunk c (0..7) of a 64-element block lands at r*128 + ((c ^ (r&7)) * 16).
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
