@@ -657,19 +657,20 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             tc::tmem_wait_ld();
             const int nv_tile = vend - (t0 + i * 128);  // valid columns of this row in the tile
             float mt = -INFINITY;
-            if (nv_tile >= 128) {
+            if (nv_tile < 128) {  // the tile crosses the end of the split, the unit or a causal window row
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) mt = fmaxf(mt, s[c][e]);
-            } else {  // the tile crosses the end of the split, the unit or a causal window row
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
+                    for (int e = 0; e < 32; ++e)
                         if (c * 32 + e >= nv_tile) s[c][e] = -INFINITY;
-                        mt = fmaxf(mt, s[c][e]);
-                    }
+            }
+            {
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) m4[c] = tc::max3(m4[c], s[c][e], s[c][e + 1]);
+                mt = tc::max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
             }
             const float m_new = fmaxf(m_used, mt * A.k1);
             // O is rescaled only when the row maximum grew by more than 2^8 (and O holds data)
@@ -679,15 +680,26 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             const float neg_m = -m_used;
             // p = exp2(s log2e/sqrt(d) - m), packed at once as bf16 pairs: column j of P holds
             // tokens 2j, 2j+1
-            float lsum = 0.f;
+            const uint64_t k1_2 = tc::pk2(A.k1, A.k1), negm_2 = tc::pk2(neg_m, neg_m);
+            uint64_t lsum2[4] = {0, 0, 0, 0};  // bit pattern 0 = (0.f, 0.f)
             float pk[2][32];
 #pragma unroll
             for (int j = 0; j < 64; ++j) {
-                const float p0 = tc::ex2_approx(fmaf(s[j >> 4][(2 * j) & 31], A.k1, neg_m));
-                const float p1 = tc::ex2_approx(fmaf(s[j >> 4][(2 * j + 1) & 31], A.k1, neg_m));
-                lsum += p0 + p1;
+                float t0, t1;
+                tc::upk2(tc::fma2(tc::pk2(s[j >> 4][(2 * j) & 31], s[j >> 4][(2 * j + 1) & 31]),
+                                  k1_2, negm_2),
+                         t0, t1);
+                const float p0 = tc::ex2_approx(t0), p1 = tc::ex2_approx(t1);
+                lsum2[j & 3] = tc::add2(lsum2[j & 3], tc::pk2(p0, p1));
                 const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
                 pk[j >> 5][j & 31] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&h2));
+            }
+            float lsum;
+            {
+                float a[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) tc::upk2(lsum2[k], a[2 * k], a[2 * k + 1]);
+                lsum = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
             }
             l = fmaf(l, f, lsum);
             if (f != 1.f) {  // O must hold the previous product before it is rescaled
