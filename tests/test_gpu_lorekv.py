@@ -140,6 +140,35 @@ def test_eviction_pass_matches_oracle(name):
     assert torch.equal(run.V_out, torch.gather(Vf, 1, idx[..., None].expand(-1, -1, cfg.d)))
 
 
+def test_eviction_pass_rising_scores():
+    """The second half of every unit's keys is shifted by 30 along the unit's mean query direction:
+    nearly every query's running maximum rises by more than 2^8 (in exp2 units) half-way through
+    the cache, which takes the attention pass's lazy-rescale path, while attention stays spread
+    over the shifted half (largest probability about 0.2)."""
+    cfg = SMALL["bf16_gqa4_D"]
+    inp = synth.lorekv_inputs(cfg, "cpu")
+    K = inp["K"].float()
+    for s in range(cfg.S):
+        for l in range(cfg.L):
+            for kh in range(cfg.Hkv):
+                heads = slice(kh * cfg.g, (kh + 1) * cfg.g)
+                qs = torch.cat([inp["Q_W"][s, l, heads].reshape(-1, cfg.d),
+                                inp["Q_look"][s, l, heads].reshape(-1, cfg.d)]).float()
+                mu = qs.mean(0)
+                K[s, l, kh, cfg.n // 2:] += 30.0 * mu / mu.norm()
+    inp["K"] = K.to(inp["K"].dtype)
+    g = {k: v.to(_dev()) for k, v in inp.items()}
+    run = _run_pass(cfg, g)
+    ref = oracle.lorekv_config_units(cfg, inp, _all_units(cfg))
+    S = run.scores.double().cpu().numpy()
+    kept = run.kept_idx.cpu().numpy()
+    for (s, l, kh), r in ref.items():
+        ui = _unit_index(cfg, s, l, kh)
+        assert_scores_close(S[ui], r["S"], cfg.dtype, f"rising unit {ui}")
+        assert_kept_matches(kept[ui, :run.cap], r["S"], sink=cfg.sink, w=cfg.w, chunk=cfg.chunk,
+                            B=cfg.B, rtol=SCORE_RTOL[cfg.dtype], what=f"rising unit {ui}")
+
+
 def test_scores_are_deterministic():
     cfg = SMALL["bf16_gqa4_D"]
     g = {k: v.to(_dev()) for k, v in synth.lorekv_inputs(cfg, "cpu").items()}
