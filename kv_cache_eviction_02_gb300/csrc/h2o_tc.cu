@@ -64,9 +64,9 @@ __global__ void __launch_bounds__(kHpThreads, 1)
     uint64_t *kfull = bars, *kempty = bars + HP_KSLOTS;
     uint64_t *qfull = bars + 2 * HP_KSLOTS, *qempty = qfull + HP_QSLOTS;
     uint64_t *tfull = qempty + HP_QSLOTS, *tempty = tfull + HP_TSLOTS;
-    uint64_t *lsef = tempty + HP_TSLOTS, *lsef2 = lsef + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(lsef + 2);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(lsef + 3);
+    uint64_t *lsef = tempty + HP_TSLOTS, *lsef2 = lsef + 1, *drain = lsef + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(lsef + 3);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(lsef + 4);
     float2 *ml_s = reinterpret_cast<float2 *>(sm + HP_ML);
     float *lse_s = reinterpret_cast<float *>(sm + HP_LSE);
 
@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(kHpThreads, 1)
         }
         tc::mbar_init(lsef, 256);
         tc::mbar_init(lsef2, 256);
+        tc::mbar_init(drain, 1);
         *abort_flag = 0;
         tc::mbar_fence_init();
     }
@@ -135,6 +136,11 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                     }
                 }
             }
+            // copies still in flight land before the CTA exits (immediate on the normal path)
+            for (int c = kc - HP_KSLOTS < 0 ? 0 : kc - HP_KSLOTS; c < kc; ++c)
+                tc::mbar_drain(&kfull[c % HP_KSLOTS], (c / HP_KSLOTS) & 1);
+            for (int c = qc - HP_QSLOTS < 0 ? 0 : qc - HP_QSLOTS; c < qc; ++c)
+                tc::mbar_drain(&qfull[c % HP_QSLOTS], (c / HP_QSLOTS) & 1);
         }
     } else if (warp == 1) {
         if (lane == 0) {  // ---- MMA issuer ----
@@ -190,6 +196,10 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                 }
             }
         }
+        if (lane == 0) {  // every product issued has completed before the tensor memory is freed
+            tc::mma_commit(drain);
+            tc::mbar_drain(drain, 0);
+        }
     } else {
         // ---- lane owners: warp w reads TMEM lanes 32 (w % 4) .. +31, columns 64 hf .. +63 of
         // every block (hf = 0 for warps 2-5, 1 for warps 6-9) ----
@@ -212,7 +222,7 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                 float m = kNoMax, l = 0.f;
                 for (int b = r; b >= 0; --b) {
                     const int ts = tcn % HP_TSLOTS;
-                    if (!tc::mbar_wait(&tfull[ts], (tcn / HP_TSLOTS) & 1, abort_flag, A.err)) {
+                    if (!tc::mbar_wait_warp(&tfull[ts], (tcn / HP_TSLOTS) & 1, abort_flag, A.err)) {
                         ok = false;
                         break;
                     }
@@ -271,7 +281,7 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                 // merge the halves: half 1 hands (m, l) over, half 0 writes lse2 of the row
                 if (hf == 1) ml_s[row] = make_float2(m, l);
                 tc::mbar_arrive(lsef);
-                if (!tc::mbar_wait(lsef, lcn & 1, abort_flag, A.err)) {
+                if (!tc::mbar_wait_warp(lsef, lcn & 1, abort_flag, A.err)) {
                     ok = false;
                     break;
                 }
@@ -283,7 +293,7 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                     lse_s[row] = -(mm * k1 + __log2f(ll));  // -lse2 of query row q
                 }
                 tc::mbar_arrive(lsef2);
-                if (!tc::mbar_wait(lsef2, lcn & 1, abort_flag, A.err)) {
+                if (!tc::mbar_wait_warp(lsef2, lcn & 1, abort_flag, A.err)) {
                     ok = false;
                     break;
                 }
@@ -296,7 +306,7 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                 for (int b = kHpMaxTiles - 1; b >= 0; --b) {
                     if (b > r || !ok) continue;
                     const int ts = tcn % HP_TSLOTS;
-                    if (!tc::mbar_wait(&tfull[ts], (tcn / HP_TSLOTS) & 1, abort_flag, A.err)) {
+                    if (!tc::mbar_wait_warp(&tfull[ts], (tcn / HP_TSLOTS) & 1, abort_flag, A.err)) {
                         ok = false;
                         continue;
                     }

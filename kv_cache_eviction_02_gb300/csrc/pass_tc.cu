@@ -223,9 +223,9 @@ __global__ void __launch_bounds__(kScThreads, 1)
     // tfull1/tfree1: the V-tile products X, Y (columns 128-511); tfull2/tfree2: S (columns 0-127)
     uint64_t *ops_full = bars + 0, *rfull = bars + 1, *rempty = bars + 1 + SC_SLOTS,
              *tfull1 = bars + 1 + 2 * SC_SLOTS, *tfree1 = tfull1 + 1, *tfull2 = tfull1 + 2,
-             *tfree2 = tfull1 + 3;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tfull1 + 4);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tfull1 + 5);
+             *tfree2 = tfull1 + 3, *drain = tfull1 + 4;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tfull1 + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tfull1 + 6);
     float *sw = reinterpret_cast<float *>(sm + SC_SW);
     float2 *qw = reinterpret_cast<float2 *>(sm + SC_QW);
 
@@ -239,6 +239,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
         tc::mbar_init(tfull2, 1);
         tc::mbar_init(tfree1, 128 * nh);  // every epilogue thread has read the columns
         tc::mbar_init(tfree2, 128 * nh);
+        tc::mbar_init(drain, 1);
         *abort_flag = 0;
         tc::mbar_fence_init();
     }
@@ -294,6 +295,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
                     if (kb) tc::tma_load_2d(b2 + 32768, &tm_lt, 64 * kb, lrow + 64, ops_full);
                 }
             }
+            int issued = 0;
             for (int c = 0; c < 2 * ntl; ++c) {
                 const int slot = c % SC_SLOTS;
                 const uint32_t ph = (c / SC_SLOTS) & 1;
@@ -304,7 +306,12 @@ __global__ void __launch_bounds__(kScThreads, 1)
                 uint8_t *dst = sm + SC_RING + slot * 32768;
                 tc::tma_load_2d(dst, map, 0, row, &rfull[slot]);
                 tc::tma_load_2d(dst + 16384, map, 64, row, &rfull[slot]);
+                issued = c + 1;
             }
+            // copies still in flight land before the CTA exits (immediate on the normal path)
+            tc::mbar_drain(ops_full, 0);
+            for (int c = issued - SC_SLOTS < 0 ? 0 : issued - SC_SLOTS; c < issued; ++c)
+                tc::mbar_drain(&rfull[c % SC_SLOTS], (c / SC_SLOTS) & 1);
         }
     } else if (warp == 1) {
         if (lane == 0 && tc::mbar_wait(ops_full, 0, abort_flag, A.err)) {  // ---- MMA issuer ----
@@ -358,6 +365,10 @@ __global__ void __launch_bounds__(kScThreads, 1)
                 tc::mma_commit(tfull2);
             }
         }
+        if (lane == 0) {  // every product issued has completed before the tensor memory is freed
+            tc::mma_commit(drain);
+            tc::mbar_drain(drain, 0);
+        }
     } else if ((warp - 2) >> 2 < nh) {
         // ---- epilogue: group hh (warps 2-5 -> head 0, 6-9 -> head 1); warp w reads TMEM lanes
         // 32 (w % 4) .. +31 ----
@@ -373,7 +384,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
 #pragma unroll
         for (int k = 0; k < 1 + kSetM; ++k) wset[k] = kFixedSets ? sw[hh * 8 + k] : 0.f;
         for (int i = 0; i < ntl; ++i) {
-            if (!tc::mbar_wait(tfull1, i & 1, abort_flag, A.err)) break;
+            if (!tc::mbar_wait_warp(tfull1, i & 1, abort_flag, A.err)) break;
             tc::fence_after_sync();
             const uint32_t tb = tmem + lane_off;
             // ||L_h^T v||^2 of this thread's token (the 128 columns of Y), and X
@@ -411,7 +422,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
                 for (int k = 0; k < 4; ++k) tc::upk2(np2[k], n[2 * k], n[2 * k + 1]);
                 nv = ((n[0] + n[1]) + (n[2] + n[3])) + ((n[4] + n[5]) + (n[6] + n[7]));
             }
-            if (!tc::mbar_wait(tfull2, i & 1, abort_flag, A.err)) break;
+            if (!tc::mbar_wait_warp(tfull2, i & 1, abort_flag, A.err)) break;
             tc::fence_after_sync();
             float s0[32], s1[32];
             tc::tmem_ld32(tb + 64 * hh, s0);
@@ -568,9 +579,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + AT_BAR);
     uint64_t *q_full = bars + 0, *rfull = bars + 1, *rempty = bars + 1 + AT_SLOTS,
              *s_full = bars + 1 + 2 * AT_SLOTS, *p_full = bars + 3 + 2 * AT_SLOTS,
-             *o_done = bars + 5 + 2 * AT_SLOTS;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 7 + 2 * AT_SLOTS);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 8 + 2 * AT_SLOTS);
+             *o_done = bars + 5 + 2 * AT_SLOTS, *drain = bars + 7 + 2 * AT_SLOTS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 8 + 2 * AT_SLOTS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 9 + 2 * AT_SLOTS);
 
     if (threadIdx.x == 0) {
         tc::mbar_init(q_full, 1);
@@ -583,6 +594,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             tc::mbar_init(&p_full[t], 128);
             tc::mbar_init(&o_done[t], 1);
         }
+        tc::mbar_init(drain, 1);
         *abort_flag = 0;
         tc::mbar_fence_init();
     }
@@ -602,6 +614,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 tc::tma_load_2d(sm + AT_Q + t * 32768, &tm_q, 0, qrow + 128 * t, q_full);
                 tc::tma_load_2d(sm + AT_Q + t * 32768 + 16384, &tm_q, 64, qrow + 128 * t, q_full);
             }
+            int issued = 0;
             for (int c = 0; c < 2 * ntl; ++c) {
                 const int slot = c % AT_SLOTS;
                 const uint32_t ph = (c / AT_SLOTS) & 1;
@@ -612,7 +625,12 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 uint8_t *dst = sm + AT_RING + slot * 32768;
                 tc::tma_load_2d(dst, map, 0, row, &rfull[slot]);
                 tc::tma_load_2d(dst + 16384, map, 64, row, &rfull[slot]);
+                issued = c + 1;
             }
+            // copies still in flight land before the CTA exits (immediate on the normal path)
+            tc::mbar_drain(q_full, 0);
+            for (int c = issued - AT_SLOTS < 0 ? 0 : issued - AT_SLOTS; c < issued; ++c)
+                tc::mbar_drain(&rfull[c % AT_SLOTS], (c / AT_SLOTS) & 1);
         }
     } else if (warp == 1) {
         // ---- MMA issuer. Per K/V tile it submits [P_0 V, S_0 next] then [P_1 V, S_1 next] as
@@ -632,6 +650,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 }
             }
         }
+        if (lane == 0) {  // every product issued has completed before the tensor memory is freed
+            tc::mma_commit(drain);
+            tc::mbar_drain(drain, 0);
+        }
     } else if (warp >= 4) {  // ---- softmax groups: warps 4-7 own query tile 0, 8-11 tile 1 ----
         const int t = (warp - 4) >> 2, lg = warp & 3;
         const int r = lg * 32 + lane;
@@ -646,7 +668,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         float m_used = kNoMax, l = 0.f;  // finite sentinel: exp2(x - kNoMax) = 0
         bool ok = true;
         for (int i = 0; i < ntl; ++i) {
-            if (!tc::mbar_wait(&s_full[t], i & 1, abort_flag, A.err)) {
+            if (!tc::mbar_wait_warp(&s_full[t], i & 1, abort_flag, A.err)) {
                 ok = false;
                 break;
             }
@@ -702,8 +724,11 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 lsum = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
             }
             l = fmaf(l, f, lsum);
-            if (f != 1.f) {  // O must hold the previous product before it is rescaled
-                if (!tc::mbar_wait(&o_done[t], (i - 1) & 1, abort_flag, A.err)) {
+            // tcgen05.ld/st are warp-collective (.sync.aligned): the rescale branch is taken by the
+            // whole warp when any of its rows needs it (f = 1 leaves the other rows unchanged)
+            if (__any_sync(0xffffffffu, f != 1.f)) {
+                // O must hold the previous product before it is rescaled
+                if (!tc::mbar_wait_warp(&o_done[t], (i - 1) & 1, abort_flag, A.err)) {
                     ok = false;
                     break;
                 }
@@ -726,7 +751,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             tc::fence_before_sync();
             tc::mbar_arrive(&p_full[t]);
         }
-        if (ok && tc::mbar_wait(&o_done[t], (ntl - 1) & 1, abort_flag, A.err)) {
+        // warp-uniform condition before the warp-collective TMEM loads
+        if (__all_sync(0xffffffffu,
+                       ok && tc::mbar_wait(&o_done[t], (ntl - 1) & 1, abort_flag, A.err))) {
             tc::fence_after_sync();
             const size_t rowi = ((size_t)unit * A.nsplit + sp) * A.Qu + qi;
 #pragma unroll

@@ -50,11 +50,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Waits for the phase of `bar` with the given parity. Gives up after `limit_ns` nanoseconds or when
-// another role has set *abort: records KVE_DEVERR_TIMEOUT in the device error word, sets *abort and
-// returns false, so that every role of the CTA leaves its loop and the CTA tears down.
+// another role has set *abort: records KVE_DEVERR_TIMEOUT in the device error word (plus bit
+// 8 + site when a site number 0..23 is given, to tell which wait gave up), sets *abort and returns
+// false, so that every role of the CTA leaves its loop and the CTA tears down.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          unsigned *err, uint64_t limit_ns = kWaitLimitNs) {
+                                          unsigned *err, uint64_t limit_ns = kWaitLimitNs,
+                                          int site = -1) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
@@ -62,11 +64,35 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
         if ((it & 255u) == 0u) {
             if (*abort) return false;
             if (globaltimer() - t0 > limit_ns) {
-                if (err) atomicOr(err, KVE_DEVERR_TIMEOUT);
+                if (err)
+                    atomicOr(err, KVE_DEVERR_TIMEOUT |
+                                      (site >= 0 && site < 24 ? (1u << (8 + site)) : 0u));
                 *abort = 1;
                 return false;
             }
         }
+    }
+}
+
+// mbar_wait by every lane of a warp that goes on to warp-collective tcgen05.ld/st: the warp gives
+// up as a whole if any lane gave up, so no instruction is left to a partial warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                               unsigned *err, uint64_t limit_ns = kWaitLimitNs,
+                                               int site = -1) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, err, limit_ns, site));
+}
+
+// Teardown wait: for the phase of `bar` with the given parity, regardless of the abort flag, for
+// at most `limit_ns` (default 100 ms). A role that leaves its loop calls it for its own copies or
+// products still in flight before the CTA frees its tensor memory and exits.
+constexpr uint64_t kDrainLimitNs = 100000000ull;  // 100 ms
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity,
+                                           uint64_t limit_ns = kDrainLimitNs) {
+    if (mbar_try_wait(bar, parity)) return;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return;
+        if ((it & 255u) == 0u && globaltimer() - t0 > limit_ns) return;
     }
 }
 

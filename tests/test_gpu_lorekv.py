@@ -33,6 +33,13 @@ SMALL = {
 }
 
 
+# 80 units: enough (unit, query tile) pairs that the attention pass splits the 2048 tokens into a
+# few multi-tile ranges (the small configurations above plan one 128-token tile per range)
+MULTITILE = CFG("bf16_multitile", "bf16", S=1, L=10, Hq=32, Hkv=8, d=128, d_model=512, n=2048,
+                vocab=1000)
+MULTITILE_UNITS = [(0, 0, 0), (0, 4, 3), (0, 9, 7)]
+
+
 def _dev():
     return torch.device("cuda:0")
 
@@ -140,12 +147,81 @@ def test_eviction_pass_matches_oracle(name):
     assert torch.equal(run.V_out, torch.gather(Vf, 1, idx[..., None].expand(-1, -1, cfg.d)))
 
 
+def _attention_weighted_vnorm(cfg, u, lse):
+    """sqrt(sum_j a_{q,j}^2 |v_j|^2) for every query of the unit (fp64), with the kernels' masking:
+    window query r of a causal window sees tokens <= n - w + r."""
+    K = np.asarray(u["K"], dtype=np.float64)
+    vn = np.linalg.norm(np.asarray(u["V"], dtype=np.float64), axis=1)
+    qs = []
+    for h in range(cfg.g):
+        qs.append(np.asarray(u["Q_W"][h], dtype=np.float64).reshape(-1, cfg.d))
+        qs.append(np.asarray(u["Q_look"][h], dtype=np.float64).reshape(-1, cfg.d))
+    out = []
+    row = 0
+    for blk in qs:
+        sc = blk @ K.T / np.sqrt(cfg.d)
+        for i in range(blk.shape[0]):
+            srow = sc[i].copy()
+            is_window = blk.shape[0] == cfg.w and cfg.window_causal
+            if is_window:
+                srow[cfg.n - cfg.w + i + 1:] = -np.inf
+            a = np.exp(srow - lse[row])
+            out.append(float(np.sqrt((a * a) @ (vn * vn))))
+            row += 1
+    return np.array(out)
+
+
+def _check_units(cfg, inp, run, units, what):
+    ref = oracle.lorekv_config_units(cfg, inp, units)
+    S = run.scores.double().cpu().numpy()
+    kept = run.kept_idx.cpu().numpy()
+    for (s, l, kh), r in ref.items():
+        ui = _unit_index(cfg, s, l, kh)
+        assert_scores_close(S[ui], r["S"], cfg.dtype, f"{what} unit {ui}")
+        assert_kept_matches(kept[ui, :run.cap], r["S"], sink=cfg.sink, w=cfg.w, chunk=cfg.chunk,
+                            B=cfg.B, rtol=SCORE_RTOL[cfg.dtype], what=f"{what} unit {ui}")
+
+
+def test_multitile_ranges_match_oracle():
+    """Attention statistics and the whole pass when every attention CTA walks several K/V tiles
+    (double-buffered S, ring wrap-around, per-half partial merge)."""
+    cfg = MULTITILE
+    inp = synth.lorekv_inputs(cfg, "cpu")
+    g = {k: v.to(_dev()) for k, v in inp.items()}
+    pb = api.LorekvProblem.from_config(cfg)
+    ws = torch.empty(api.lorekv_workspace_size(pb), dtype=torch.uint8, device=_dev())
+    Qu = cfg.g * cfg.queries_per_head
+    lse = torch.empty(cfg.units, Qu, device=_dev())
+    o = torch.empty(cfg.units, Qu, cfg.d, device=_dev())
+    api.lorekv_attention_stats(pb, g["K"], g["V"], g["Q_W"], g["Q_look"], lse, o, ws)
+    api.kve_check_device()
+    lse, o = lse.double().cpu().numpy(), o.double().cpu().numpy()
+    for (s, l, kh) in MULTITILE_UNITS:
+        u = synth.unit_slice(cfg, inp, s, l, kh)
+        eye = np.stack([np.eye(cfg.d)] * cfg.g)
+        r = oracle.lorekv_unit(u["K"], u["V"], u["Q_W"], u["Q_look"], eye, np.ones(cfg.M) / cfg.M,
+                               M=cfg.M, T=cfg.T, sink=cfg.sink, lambda_L=1.0, eps=cfg.eps,
+                               window_causal=cfg.window_causal, want=("lse", "o"))
+        ui = _unit_index(cfg, s, l, kh)
+        lse_ref, o_ref = r["lse"].reshape(-1), r["o"].reshape(-1, cfg.d)
+        assert np.allclose(lse[ui], lse_ref, rtol=0, atol=2e-3 * np.maximum(1, np.abs(lse_ref)).max())
+        # o = sum_j a_j v_j with every a_j rounded to bf16 on its way to the tensor cores:
+        # independent relative errors in [-2^-9, 2^-9] give |o_gpu - o| an RMS of
+        # 2^-9/sqrt(3) sqrt(sum_j a_j^2 |v_j|^2); allow 4 sigma plus fp32 accumulation
+        err = np.linalg.norm(o[ui] - o_ref, axis=1)
+        sigma = 2.0 ** -9 / np.sqrt(3.0) * _attention_weighted_vnorm(cfg, u, lse_ref)
+        bound = 4.0 * sigma + 1e-5 * np.linalg.norm(o_ref, axis=1) + 1e-6
+        assert np.all(err <= bound), (ui, float((err / bound).max()))
+    run = _run_pass(cfg, g)
+    _check_units(cfg, inp, run, MULTITILE_UNITS, "multitile")
+
+
 def test_eviction_pass_rising_scores():
     """The second half of every unit's keys is shifted by 30 along the unit's mean query direction:
     nearly every query's running maximum rises by more than 2^8 (in exp2 units) half-way through
-    the cache, which takes the attention pass's lazy-rescale path, while attention stays spread
-    over the shifted half (largest probability about 0.2)."""
-    cfg = SMALL["bf16_gqa4_D"]
+    the cache, which takes the attention pass's lazy-rescale path inside multi-tile ranges, while
+    attention stays spread over the shifted half (largest probability about 0.2)."""
+    cfg = MULTITILE
     inp = synth.lorekv_inputs(cfg, "cpu")
     K = inp["K"].float()
     for s in range(cfg.S):
@@ -159,14 +235,7 @@ def test_eviction_pass_rising_scores():
     inp["K"] = K.to(inp["K"].dtype)
     g = {k: v.to(_dev()) for k, v in inp.items()}
     run = _run_pass(cfg, g)
-    ref = oracle.lorekv_config_units(cfg, inp, _all_units(cfg))
-    S = run.scores.double().cpu().numpy()
-    kept = run.kept_idx.cpu().numpy()
-    for (s, l, kh), r in ref.items():
-        ui = _unit_index(cfg, s, l, kh)
-        assert_scores_close(S[ui], r["S"], cfg.dtype, f"rising unit {ui}")
-        assert_kept_matches(kept[ui, :run.cap], r["S"], sink=cfg.sink, w=cfg.w, chunk=cfg.chunk,
-                            B=cfg.B, rtol=SCORE_RTOL[cfg.dtype], what=f"rising unit {ui}")
+    _check_units(cfg, inp, run, MULTITILE_UNITS, "rising")
 
 
 def test_scores_are_deterministic():
