@@ -238,6 +238,35 @@ def test_eviction_pass_rising_scores():
     _check_units(cfg, inp, run, MULTITILE_UNITS, "rising")
 
 
+def test_layer_chunks_match_whole_pass():
+    """With lambda_D = 0 the units and omega do not depend on other layers, so the pass issued per
+    chunk of layers (sub-shape views of the same buffers) gives the whole pass's results."""
+    import dataclasses
+    cfg = MULTITILE
+    assert cfg.lambda_D == 0
+    g = {k: v.to(_dev()) for k, v in synth.lorekv_inputs(cfg, "cpu").items()}
+    pb, Lf, G = _prepare(cfg, g)
+    whole = api.LorekvPass(pb, _dev())
+    whole.run(g, Lf, G)
+    cl, upc = 2, 2 * cfg.Hkv
+    sub = api.LorekvPass(dataclasses.replace(pb, n_layers=cl), _dev())
+    for c in range(cfg.L // cl):
+        part = {k: (g[k][:, c * cl:(c + 1) * cl] if k in ("K", "V", "Q_W", "Q_look") else g[k])
+                for k in g}
+        sub.run(part, Lf[c * cl:(c + 1) * cl], G[c * cl:(c + 1) * cl])
+        api.kve_check_device()
+        u0, u1 = c * upc, (c + 1) * upc
+        assert torch.allclose(sub.omega, whole.omega, rtol=1e-6, atol=0)
+        S_w, S_c = whole.scores[u0:u1].double(), sub.scores.double()
+        assert torch.allclose(S_c, S_w, rtol=1e-4, atol=1e-9 * float(S_w.max())), c
+        # kept sets of the chunk are the top-B of the chunk's own scores
+        kept = sub.kept_idx.cpu().numpy()
+        Sc = S_c.cpu().numpy()
+        for ui in range(upc):
+            assert_kept_valid_for_own_scores(kept[ui], Sc[ui], sink=cfg.sink, w=cfg.w,
+                                             chunk=cfg.chunk, B=cfg.B, what=f"chunk {c} unit {ui}")
+
+
 def test_scores_are_deterministic():
     cfg = SMALL["bf16_gqa4_D"]
     g = {k: v.to(_dev()) for k, v in synth.lorekv_inputs(cfg, "cpu").items()}
