@@ -438,7 +438,7 @@ def e2e_lorekv(cfg, g, run, Lf, G, dev, stream, pg, world, args):
         pb = api.LorekvProblem.from_config(cfg)
         sub = dataclasses.replace(pb, n_layers=cl)
         upc = cl * cfg.Hkv  # units per chunk
-        runs = [api.LorekvPass(sub, dev) for _ in range(2)]
+        ws = torch.empty(api.lorekv_workspace_size(sub), dtype=torch.uint8, device=dev)
         dev_in = [{k: torch.empty((1, cl) + tuple(g[k].shape[2:]), dtype=g[k].dtype, device=dev)
                    for k in layered} for _ in range(2)]
         small = {k: torch.empty_like(g[k]) for k in ("logits", "sampled")}
@@ -447,6 +447,7 @@ def e2e_lorekv(cfg, g, run, Lf, G, dev, stream, pg, world, args):
         copied = [torch.cuda.Event() for _ in range(2)]
         done = [torch.cuda.Event() for _ in range(2)]
         nch = cfg.L // cl
+        scores = run.scores  # every chunk writes its slice of the full-size outputs
 
         def one():
             start_ev.record(stream)
@@ -463,19 +464,19 @@ def e2e_lorekv(cfg, g, run, Lf, G, dev, stream, pg, world, args):
                         dev_in[b][k].copy_(host[k][:, c * cl:(c + 1) * cl], non_blocking=True)
                     copied[b].record(cs)
                 stream.wait_event(copied[b])
-                inp = dict(dev_in[b], **small)
-                runs[b].run(inp, Lf[c * cl:(c + 1) * cl], G[c * cl:(c + 1) * cl],
-                            stream.cuda_stream)
-                with torch.cuda.stream(stream):
-                    r = runs[b]
-                    u0, u1 = c * upc, (c + 1) * upc
-                    host_out[0][u0:u1].copy_(r.kept_idx, non_blocking=True)
-                    host_out[1][u0:u1].copy_(r.kept_len, non_blocking=True)
-                    host_out[2][u0:u1].copy_(r.K_out, non_blocking=True)
-                    host_out[3][u0:u1].copy_(r.V_out, non_blocking=True)
-                    if c == nch - 1:
-                        host_out[4].copy_(r.omega, non_blocking=True)
+                x = dev_in[b]
+                u0, u1 = c * upc, (c + 1) * upc
+                sl = slice(c * cl, (c + 1) * cl)
+                api.lorekv_score(sub, x["K"], x["V"], x["Q_W"], x["Q_look"], Lf[sl], G[sl],
+                                 small["logits"], small["sampled"], scores[u0:u1], run.omega,
+                                 ws, stream.cuda_stream)
+                api.lorekv_select_compact(sub, scores[u0:u1], x["K"], x["V"], run.kept_idx[u0:u1],
+                                          run.kept_len[u0:u1], run.K_out[u0:u1],
+                                          run.V_out[u0:u1], None, stream.cuda_stream)
                 done[b].record(stream)
+            with torch.cuda.stream(stream):  # the step's results, read back once
+                for t, h in zip(outs, host_out):
+                    h.copy_(t, non_blocking=True)
     else:
         dev_in = {k: torch.empty_like(g[k]) for k in names}
 
@@ -516,6 +517,13 @@ def bench_h2o(dev, stream, pg, world, args, pk):
     from kv_cache_eviction_02_gb300 import api, synth
     cfg = synth.H2O_CONFIGS["opt30b"].replace(batch=args.h2o_batch, steps=args.h2o_steps)
     hin = synth.h2o_inputs(cfg, dev)
+    # one untimed prefill on a throwaway state first (first-call costs: the stream-ordered
+    # scratch pool growing, first touch of the state), then the timed prefill on a fresh state
+    warm = api.h2o_state_create(cfg.batch, cfg.L, cfg.H, cfg.d, cfg.prompt + cfg.steps,
+                                cfg.budget_frac, torch.float16)
+    warm.prefill(hin["K"], hin["V"], hin["Q"])
+    torch.cuda.synchronize(dev)
+    warm.close()
     st = api.h2o_state_create(cfg.batch, cfg.L, cfg.H, cfg.d, cfg.prompt + cfg.steps,
                               cfg.budget_frac, torch.float16)
     api.kve_profile_enable(True)
