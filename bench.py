@@ -77,6 +77,12 @@ def dist_init(args):
     return rank, world, local, pg
 
 
+def whole_job_value(tokens_per_rank: float, world: int, ms: float) -> float:
+    """Weak scaling over independent replicas: every rank scores its own sequence, so the job
+    processes tokens_per_rank x world tokens in the slowest rank's time (ms)."""
+    return tokens_per_rank * world / (ms / 1e3)
+
+
 def barrier(pg):
     if pg is not None:
         pg.barrier()
@@ -334,7 +340,7 @@ def run_native(args):
     ms = ev0.elapsed_time(ev1) / args.steps
     ms = max_over_ranks(pg, ms, dev)
     tokens_per_step = cfg.units * cfg.n
-    value = tokens_per_step * world / (ms / 1e3)
+    value = whole_job_value(tokens_per_step, world, ms)
     alg_bytes = lorekv_algorithmic_bytes(cfg)
     gpu_launches = sum(v["kernels"] for v in prof.values())
 
