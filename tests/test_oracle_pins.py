@@ -384,6 +384,28 @@ def test_greedy_eviction_is_argmin_of_accumulated_score():
         assert np.flatnonzero(ev).tolist() == [best]
 
 
+@pytest.mark.parametrize("hname", ["sqrt", "log"])
+def test_greedy_eviction_with_concave_score_function(hname):
+    """F_score(T) = h(sum_{s in T} acc_s) with a non-decreasing concave h (H2O summary, "Define
+    the score function": sqrt(z + 1), log(z + 1)): argmax_v h(total - acc_v) over the candidates is
+    the same token as with linear h, because h is increasing; the eviction the kernels implement
+    (argmin acc, oldest on ties) therefore serves every such h."""
+    h = {"sqrt": lambda z: np.sqrt(z + 1.0), "log": lambda z: np.log(z + 1.0)}[hname]
+    rng = np.random.default_rng(23)
+    for trial in range(200):
+        t = int(rng.integers(20, 80))
+        k, r = oracle.h2o_budget(t, 0.2)
+        cnt = k + 1
+        pos = np.sort(rng.choice(np.arange(t - 1), size=cnt - 1, replace=False)).tolist() + [t - 1]
+        pos = np.array(pos, dtype=np.int32)
+        acc = rng.integers(0, 5, size=cnt).astype(np.float64) / 4.0
+        ev = oracle.h2o_evict(pos, acc, t, 0.2)
+        cands = [j for j in range(cnt) if pos[j] < t - r]
+        F = lambda keep: h(sum(acc[j] for j in keep))
+        best = max(cands, key=lambda v: (F([j for j in range(cnt) if j != v]), -pos[v]))
+        assert np.flatnonzero(ev).tolist() == [best]
+
+
 def test_h2o_decode_invariants():
     rng = np.random.default_rng(20)
     P, d, steps, frac = 64, 16, 64, 0.2
