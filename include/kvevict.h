@@ -125,6 +125,18 @@ int lorekv_score_noalloc(const KveShape *shape, const KveLorekvParams *params, c
                          const float *G, const float *logits, const int32_t *sampled,
                          float *scores_out, float *omega_out, void *stream);
 
+/* Attention-output fidelity of a compressed cache (LORE-KV page, analyses, "Attention-output
+ * fidelity"; reading: per query, the cosine similarity between its attention output over the
+ * compressed cache and over the full cache). Typical use: lorekv_attention_stats for the same
+ * held-out queries over the full K/V and over the compacted K_out/V_out (a cache of kept_capacity
+ * tokens), then this call.
+ *   o_full, o_comp [rows][d_head] fp32 device (row-major, 16-byte aligned for the vector path);
+ *   cos_out [rows] fp32 device: o_full.o_comp / (|o_full| |o_comp|), 0 when either norm is 0;
+ *   mean_out [1] fp32 device or NULL: the mean of cos_out, summed in a fixed order.
+ * Returns KVE_EINVAL for null inputs, rows < 1 or d_head < 1. Asynchronous on `stream`. */
+int lorekv_output_fidelity(const float *o_full, const float *o_comp, int rows, int d_head,
+                           float *cos_out, float *mean_out, void *stream);
+
 /* Attention statistics only (the first half of lorekv_score, exposed for testing): for each unit
  * and each of its g*(w+M*T) queries (query head major, then window rows, then lookahead rows):
  *   lse_out [units][g*(w+M*T)] fp32 natural-log log-sum-exp of q.k/sqrt(d) over visible tokens,

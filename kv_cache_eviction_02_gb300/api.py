@@ -22,6 +22,7 @@ _DT = {torch.float32: KVE_F32, torch.bfloat16: KVE_BF16, torch.float16: KVE_F16}
 
 EXPORTED = ("lorekv_prepare_wo", "lorekv_workspace_size", "lorekv_score",
             "lorekv_attention_stats", "lorekv_kept_capacity", "lorekv_select_compact",
+            "lorekv_output_fidelity",
             "h2o_state_create", "h2o_prefill", "h2o_decode_step", "h2o_export", "h2o_capacity",
             "h2o_length", "h2o_state_destroy", "kve_last_error", "kve_check_device",
             "kve_inject_failure", "kve_profile_enable", "kve_profile_report", "kve_version",
@@ -64,6 +65,7 @@ def lib():
         L.lorekv_score.argtypes = [SP, PP, P, P, P, P, P, P, P, P, P, P, P, Z, P]
         L.lorekv_score_noalloc.argtypes = [SP, PP, P, P, P, P, P, P, P, P, P, P, P]
         L.lorekv_attention_stats.argtypes = [SP, PP, P, P, P, P, P, P, P, Z, P]
+        L.lorekv_output_fidelity.argtypes = [P, P, I, I, P, P, P]
         L.lorekv_kept_capacity.argtypes = [SP, PP]
         L.lorekv_select_compact.argtypes = [SP, PP, P, P, P, P, P, P, P, P, Z, P]
         L.h2o_state_create.argtypes = [ctypes.POINTER(P), I, I, I, I, I, F, I]
@@ -199,6 +201,12 @@ def lorekv_attention_stats(pb, K, V, Q_W, Q_look, lse_out, o_out, workspace, str
     _check(lib().lorekv_attention_stats(ctypes.byref(sh), ctypes.byref(pr), _ptr(K), _ptr(V),
                                         _ptr(Q_W), _ptr(Q_look), _ptr(lse_out), _ptr(o_out),
                                         _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def lorekv_output_fidelity(o_full, o_comp, cos_out, mean_out=None, stream=None):
+    rows, d = o_full.shape[0], o_full.shape[-1]
+    _check(lib().lorekv_output_fidelity(_ptr(o_full), _ptr(o_comp), int(rows), int(d),
+                                        _ptr(cos_out), _ptr(mean_out), _stream(stream)))
 
 
 def lorekv_select_compact(pb, scores, K, V, kept_idx, kept_len, K_out, V_out, workspace=None,

@@ -415,6 +415,23 @@ int lorekv_attention_stats(const KveShape *shape, const KveLorekvParams *params,
     return KVE_OK;
 }
 
+int lorekv_output_fidelity(const float *o_full, const float *o_comp, int rows, int d_head,
+                           float *cos_out, float *mean_out, void *stream) {
+    if (int s = injected()) return s;
+    if (!o_full || !o_comp || !cos_out)
+        return fail(KVE_EINVAL, "lorekv_output_fidelity: null argument");
+    if (rows < 1 || d_head < 1)
+        return fail(KVE_EINVAL, "lorekv_output_fidelity: rows and d_head must be >= 1");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    {
+        ProfScope ps("fidelity", mean_out ? 2 : 1, st);
+        e = launch_output_fidelity(o_full, o_comp, rows, d_head, cos_out, mean_out, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "lorekv_output_fidelity: launch");
+    return KVE_OK;
+}
+
 int lorekv_score(const KveShape *shape, const KveLorekvParams *params, const void *K,
                  const void *V, const void *Q_W, const void *Q_look, const float *L,
                  const float *G, const float *logits, const int32_t *sampled, float *scores_out,

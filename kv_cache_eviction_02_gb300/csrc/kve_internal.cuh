@@ -116,6 +116,8 @@ cudaError_t launch_h2o_prefill(H2OState &s, const void *K, const void *V, const 
                                cudaStream_t st);
 bool h2o_prefill_fits(int d, int P, int dtype);
 size_t h2o_prefill_smem(int d, int P, int dtype);  // CUDA-core column-sum kernel
+cudaError_t launch_output_fidelity(const float *o_full, const float *o_comp, int rows, int d,
+                                   float *cos_out, float *mean_out, cudaStream_t st);
 // tensor-core prefill column sums (h2o_tc.cu): writes kColsumTcParts partial sums per token,
 // acc_out [units][kColsumTcParts][P]
 constexpr int kColsumTcParts = 2;

@@ -98,6 +98,14 @@ def test_score_rejects_bad_arguments_before_touching_the_gpu(api):
     assert st == api.KVE_EINVAL
 
 
+def test_fidelity_rejects_bad_arguments_before_touching_the_gpu(api):
+    L = api.lib()
+    assert L.lorekv_output_fidelity(None, None, 4, 128, None, None, None) == api.KVE_EINVAL
+    fake = ctypes.c_void_p(256)  # never dereferenced: the checks run first
+    assert L.lorekv_output_fidelity(fake, fake, 0, 128, fake, None, None) == api.KVE_EINVAL
+    assert L.lorekv_output_fidelity(fake, fake, 4, 0, fake, None, None) == api.KVE_EINVAL
+
+
 def test_h2o_create_validates_arguments(api):
     L = api.lib()
     h = ctypes.c_void_p()

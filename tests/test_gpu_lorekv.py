@@ -267,6 +267,50 @@ def test_layer_chunks_match_whole_pass():
                                              chunk=cfg.chunk, B=cfg.B, what=f"chunk {c} unit {ui}")
 
 
+def test_output_fidelity_matches_oracle():
+    """Attention-output fidelity of the compressed cache: held-out queries (the generator's queries
+    under another seed, seeing the whole cache) attend over the full K/V and over the compacted
+    K'/V'; each query's cosine of the two outputs matches the oracle's fp64 attention over the same
+    kept rows, and the reported mean is the mean of the cosines."""
+    import dataclasses
+    cfg = SMALL["bf16_gqa4_D"]
+    inp = synth.lorekv_inputs(cfg, "cpu")
+    held = synth.lorekv_inputs(cfg.replace(seed=cfg.seed + 1000), "cpu")
+    g = {k: v.to(_dev()) for k, v in inp.items()}
+    run = _run_pass(cfg, g)
+    pe = dataclasses.replace(api.LorekvProblem.from_config(cfg), window_causal=0)
+    pc = dataclasses.replace(pe, n_tokens=run.cap)  # the compacted cache as a cache of cap tokens
+    Qw, Ql = held["Q_W"].to(_dev()), held["Q_look"].to(_dev())
+    Qu = cfg.g * cfg.queries_per_head
+    lse = torch.empty(cfg.units, Qu, device=_dev())
+    o_full = torch.empty(cfg.units, Qu, cfg.d, device=_dev())
+    o_comp = torch.empty_like(o_full)
+    for pb, K, V, o in ((pe, g["K"], g["V"], o_full), (pc, run.K_out, run.V_out, o_comp)):
+        ws = torch.empty(api.lorekv_workspace_size(pb), dtype=torch.uint8, device=_dev())
+        api.lorekv_attention_stats(pb, K, V, Qw, Ql, lse, o, ws)
+    cos = torch.empty(cfg.units * Qu, device=_dev())
+    mean = torch.empty(1, device=_dev())
+    api.lorekv_output_fidelity(o_full.view(-1, cfg.d), o_comp.view(-1, cfg.d), cos, mean)
+    api.kve_check_device()
+    cos_g = cos.double().cpu().numpy().reshape(cfg.units, Qu)
+    kept = run.kept_idx.long().cpu().numpy()
+    eye = np.stack([np.eye(cfg.d)] * cfg.g)
+    for (s, l, kh) in _all_units(cfg):
+        ui = _unit_index(cfg, s, l, kh)
+        u, h = synth.unit_slice(cfg, inp, s, l, kh), synth.unit_slice(cfg, held, s, l, kh)
+        idx = kept[ui, :run.cap]
+        outs = []
+        for K, V in ((u["K"], u["V"]), (u["K"][idx], u["V"][idx])):
+            r = oracle.lorekv_unit(K, V, h["Q_W"], h["Q_look"], eye, np.ones(cfg.M) / cfg.M,
+                                   M=cfg.M, T=cfg.T, sink=cfg.sink, lambda_L=1.0, eps=cfg.eps,
+                                   window_causal=0, want=("o",))
+            outs.append(r["o"].reshape(-1, cfg.d))
+        of, oc = outs
+        ref = (of * oc).sum(1) / (np.linalg.norm(of, axis=1) * np.linalg.norm(oc, axis=1))
+        assert np.allclose(cos_g[ui], ref, rtol=0, atol=3e-3), (ui, float(np.abs(cos_g[ui] - ref).max()))
+    assert float(mean.item()) == pytest.approx(float(cos_g.mean()), rel=1e-5)
+
+
 def test_scores_are_deterministic():
     cfg = SMALL["bf16_gqa4_D"]
     g = {k: v.to(_dev()) for k, v in synth.lorekv_inputs(cfg, "cpu").items()}
