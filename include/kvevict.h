@@ -210,13 +210,59 @@ int h2o_length(const KveH2O *st);
 
 void h2o_state_destroy(KveH2O *st);
 
+/* ---- counter-causal surprise refresh --------------------------------------------------------- */
+
+/* Problem shape of one counter-causal refresh (review of "Back from the Future: KV Cache Management
+ * by Counter-Causal Surprise", Section 3.3: the fast variant that runs only the last layer).
+ * n_seq independent sequences of n_tokens cached tokens; query head h reads KV head
+ * h / (n_q_heads/n_kv_heads); sink = leading system-prompt slots that are never scored or evicted
+ * (design choice 4); keep_J = tokens kept per sequence (Algorithm 3, J). dtype is the element type
+ * of K, V, Q_fresh, H_last, W_O and W_U: KVE_F32 or KVE_BF16. d_head is 32, 64 or 128;
+ * 0 <= sink <= n_tokens; 1 <= keep_J <= n_tokens. */
+typedef struct {
+    int n_seq, n_q_heads, n_kv_heads, d_head, d_model, n_tokens, vocab, dtype, sink, keep_J;
+} KveCcShape;
+
+/* Bytes of workspace cc_surprise() needs: the heads' attention outputs (fp32, n_seq * n_tokens *
+ * n_q_heads * d_head floats) and per-column-tile partial logits. 0 on invalid input. */
+size_t cc_workspace_size(const KveCcShape *shape);
+
+/* Counter-causal surprise of every cached token (same review, Section 3.2 steps 1-5, Eq. 1).
+ *   K, V     [n_seq][n_kv_heads][n_tokens][d_head]  the last layer's cached keys and values
+ *   Q_fresh  [n_seq][n_q_heads][n_tokens][d_head]   fresh queries at the tokens' own positions
+ *   H_last   [n_seq][n_tokens][d_model]             the last layer's stored input activations
+ *   W_O      [d_model][n_q_heads*d_head]            the last layer's output projection (o_proj)
+ *   W_U      [vocab][d_model]                       the unembedding
+ *   tokens   [n_seq][n_tokens] int32                the cached token ids x_i, in [0, vocab)
+ *   surprise_out [n_seq][n_tokens] fp32: -logit_i with logit_i = W_U[x_i] . (h_i + W_O o_i),
+ *            o_i the heads' outputs concatenated, o_i^h = sum_{j>i} softmax_j(q_i^h.k_j/sqrt d) v_j
+ *            (strictly later tokens only; the last token's o is 0); +inf for the sink slots and
+ *            the last token.
+ * Token ids are checked on the device: an id outside [0, vocab) is read as 0 and recorded in the
+ * device error word, which kve_check_device(stream) reports as KVE_EINVAL. */
+int cc_surprise(const KveCcShape *shape, const void *K, const void *V, const void *Q_fresh,
+                const void *H_last, const void *W_O, const void *W_U, const int32_t *tokens,
+                float *surprise_out, void *workspace, size_t ws_bytes, void *stream);
+
+/* Memory refresh (same review, Algorithm 3): per sequence keep the keep_J tokens of highest
+ * surprise (equal surprise: the lower position), in ascending position order, and gather them.
+ *   surprise [n_seq][n_tokens] fp32 (from cc_surprise); K, V, tokens as in cc_surprise
+ *   kept_idx [n_seq][keep_J] int32 kept positions, ascending
+ *   K_out, V_out [n_seq][n_kv_heads][keep_J][d_head] shape->dtype: K_out[s][h][j] =
+ *            K[s][h][kept_idx[s][j]]; tokens_out [n_seq][keep_J] int32.
+ * No workspace. Outputs must not overlap the inputs. */
+int cc_select_compact(const KveCcShape *shape, const float *surprise, const void *K,
+                      const void *V, const int32_t *tokens, int32_t *kept_idx, void *K_out,
+                      void *V_out, int32_t *tokens_out, void *stream);
+
 /* ---- diagnostics ---------------------------------------------------------------------------- */
 
 /* Message of the last failing call on this thread ("" if none). Valid until the next call. */
 const char *kve_last_error(void);
 
 /* Synchronises `stream`, then reads and clears the device error word that bounded on-device
- * waits set. Returns KVE_OK, KVE_ETIMEOUT (a wait gave up) or KVE_ECUDA. */
+ * waits and device-side index checks set. Returns KVE_OK, KVE_ETIMEOUT (a wait gave up),
+ * KVE_EINVAL (cc_surprise met a token id outside [0, vocab)) or KVE_ECUDA. */
 int kve_check_device(void *stream);
 
 /* Self-test of the bounded on-device waits: launches one CTA whose thread waits, through the same

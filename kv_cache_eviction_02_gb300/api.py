@@ -26,7 +26,8 @@ EXPORTED = ("lorekv_prepare_wo", "lorekv_workspace_size", "lorekv_score",
             "h2o_state_create", "h2o_prefill", "h2o_decode_step", "h2o_export", "h2o_capacity",
             "h2o_length", "h2o_state_destroy", "kve_last_error", "kve_check_device",
             "kve_inject_failure", "kve_profile_enable", "kve_profile_report", "kve_version",
-            "kve_selftest_wait_timeout", "lorekv_score_noalloc")
+            "kve_selftest_wait_timeout", "lorekv_score_noalloc",
+            "cc_workspace_size", "cc_surprise", "cc_select_compact")
 
 
 class KveError(RuntimeError):
@@ -44,6 +45,12 @@ class KveLorekvParams(ctypes.Structure):
     _fields_ = ([(n, ctypes.c_int) for n in ("w", "M", "T", "chunk", "sink", "budget_B",
                                               "window_causal")] +
                 [(n, ctypes.c_float) for n in ("lambda_L", "beta", "gamma", "lambda_D", "eps")])
+
+
+class KveCcShape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("n_seq", "n_q_heads", "n_kv_heads", "d_head",
+                                             "d_model", "n_tokens", "vocab", "dtype", "sink",
+                                             "keep_J")]
 
 
 _lib = None
@@ -82,6 +89,11 @@ def lib():
         L.kve_profile_enable.argtypes = [I]
         L.kve_selftest_wait_timeout.argtypes = [I, P]
         L.kve_profile_report.argtypes = [ctypes.c_char_p, Z]
+        CS = ctypes.POINTER(KveCcShape)
+        L.cc_workspace_size.argtypes = [CS]
+        L.cc_workspace_size.restype = Z
+        L.cc_surprise.argtypes = [CS, P, P, P, P, P, P, P, P, P, Z, P]
+        L.cc_select_compact.argtypes = [CS, P, P, P, P, P, P, P, P, P]
         _lib = L
     return _lib
 
@@ -216,6 +228,47 @@ def lorekv_select_compact(pb, scores, K, V, kept_idx, kept_len, K_out, V_out, wo
     _check(lib().lorekv_select_compact(ctypes.byref(sh), ctypes.byref(pr), _ptr(scores), _ptr(K),
                                        _ptr(V), _ptr(kept_idx), _ptr(kept_len), _ptr(K_out),
                                        _ptr(V_out), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+@dataclass
+class CcProblem:
+    """Shape of one counter-causal refresh (the C struct KveCcShape)."""
+    n_seq: int
+    n_q_heads: int
+    n_kv_heads: int
+    d_head: int
+    d_model: int
+    n_tokens: int
+    vocab: int
+    dtype: int
+    sink: int
+    keep_J: int
+
+    def shape(self) -> KveCcShape:
+        return KveCcShape(self.n_seq, self.n_q_heads, self.n_kv_heads, self.d_head, self.d_model,
+                          self.n_tokens, self.vocab, self.dtype, self.sink, self.keep_J)
+
+
+def cc_workspace_size(pb: CcProblem) -> int:
+    sh = pb.shape()
+    return int(lib().cc_workspace_size(ctypes.byref(sh)))
+
+
+def cc_surprise(pb: CcProblem, K, V, Q_fresh, H_last, W_O, W_U, tokens, surprise_out, workspace,
+                stream=None):
+    sh = pb.shape()
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().cc_surprise(ctypes.byref(sh), _ptr(K), _ptr(V), _ptr(Q_fresh), _ptr(H_last),
+                             _ptr(W_O), _ptr(W_U), _ptr(tokens), _ptr(surprise_out),
+                             _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def cc_select_compact(pb: CcProblem, surprise, K, V, tokens, kept_idx, K_out, V_out, tokens_out,
+                      stream=None):
+    sh = pb.shape()
+    _check(lib().cc_select_compact(ctypes.byref(sh), _ptr(surprise), _ptr(K), _ptr(V),
+                                   _ptr(tokens), _ptr(kept_idx), _ptr(K_out), _ptr(V_out),
+                                   _ptr(tokens_out), _stream(stream)))
 
 
 def kve_check_device(stream=None):

@@ -299,6 +299,9 @@ int kve_check_device(void *stream) {
         cudaMemcpyToSymbol(g_kve_error_word, &zero, sizeof(zero));
         if (word & KVE_DEVERR_TIMEOUT)
             return fail(KVE_ETIMEOUT, "a bounded on-device wait gave up (error word 0x%x)", word);
+        if (word & KVE_DEVERR_BADINDEX)
+            return fail(KVE_EINVAL, "a token id outside [0, vocab) reached cc_surprise (error word 0x%x)",
+                        word);
         return fail(KVE_ECUDA, "device error word 0x%x", word);
     }
     return KVE_OK;
@@ -429,6 +432,79 @@ int lorekv_output_fidelity(const float *o_full, const float *o_comp, int rows, i
         e = launch_output_fidelity(o_full, o_comp, rows, d_head, cos_out, mean_out, st);
     }
     if (e != cudaSuccess) return cuda_fail(e, "lorekv_output_fidelity: launch");
+    return KVE_OK;
+}
+
+// ---- counter-causal surprise refresh ----------------------------------------------------------
+
+static int cc_dims(const char *fn, const KveCcShape *sh, CcDims *D) {
+    if (!sh) return fail(KVE_EINVAL, "%s: null shape", fn);
+    if (sh->dtype != KVE_F32 && sh->dtype != KVE_BF16)
+        return fail(KVE_EDTYPE, "%s: dtype must be KVE_F32 or KVE_BF16", fn);
+    if (sh->n_seq < 1 || sh->n_tokens < 1 || sh->n_q_heads < 1 || sh->n_kv_heads < 1 ||
+        sh->d_model < 1 || sh->vocab < 1)
+        return fail(KVE_EINVAL, "%s: sizes must be >= 1", fn);
+    if (sh->n_q_heads % sh->n_kv_heads != 0)
+        return fail(KVE_EINVAL, "%s: n_q_heads must be a multiple of n_kv_heads", fn);
+    if (sh->d_head != 32 && sh->d_head != 64 && sh->d_head != 128)
+        return fail(KVE_EINVAL, "%s: d_head must be 32, 64 or 128", fn);
+    if (sh->sink < 0 || sh->sink > sh->n_tokens)
+        return fail(KVE_EINVAL, "%s: sink must be in [0, n_tokens]", fn);
+    if (sh->keep_J < 1 || sh->keep_J > sh->n_tokens)
+        return fail(KVE_EINVAL, "%s: keep_J must be in [1, n_tokens]", fn);
+    // launch-grid limits: y = query heads / column tiles, z = sequences
+    if (sh->n_seq > 65535 || sh->n_q_heads > 65535 || sh->d_model > (1 << 22))
+        return fail(KVE_EINVAL, "%s: n_seq, n_q_heads or d_model too large", fn);
+    *D = CcDims{sh->n_seq, sh->n_q_heads, sh->n_kv_heads, sh->d_head, sh->d_model, sh->n_tokens,
+                sh->vocab, sh->dtype, sh->sink, sh->keep_J};
+    return KVE_OK;
+}
+
+size_t cc_workspace_size(const KveCcShape *shape) {
+    CcDims D;
+    if (cc_dims("cc_workspace_size", shape, &D) != KVE_OK) return 0;
+    return cc_workspace_bytes(D);
+}
+
+int cc_surprise(const KveCcShape *shape, const void *K, const void *V, const void *Q_fresh,
+                const void *H_last, const void *W_O, const void *W_U, const int32_t *tokens,
+                float *surprise_out, void *workspace, size_t ws_bytes, void *stream) {
+    if (int s = injected()) return s;
+    CcDims D;
+    if (int s = cc_dims("cc_surprise", shape, &D)) return s;
+    if (!K || !V || !Q_fresh || !H_last || !W_O || !W_U || !tokens || !surprise_out)
+        return fail(KVE_EINVAL, "cc_surprise: null argument");
+    if (!workspace || ws_bytes < cc_workspace_bytes(D))
+        return fail(KVE_EWORKSPACE, "cc_surprise: workspace of %zu bytes needed, %zu given",
+                    cc_workspace_bytes(D), ws_bytes);
+    unsigned *err = device_error_word();
+    if (!err) return fail(KVE_ECUDA, "cc_surprise: no device error word");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    {
+        ProfScope ps("cc_surprise", 3, st);
+        e = launch_cc_surprise(D, K, V, Q_fresh, H_last, W_O, W_U, tokens, surprise_out, workspace,
+                               err, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "cc_surprise: launch");
+    return KVE_OK;
+}
+
+int cc_select_compact(const KveCcShape *shape, const float *surprise, const void *K,
+                      const void *V, const int32_t *tokens, int32_t *kept_idx, void *K_out,
+                      void *V_out, int32_t *tokens_out, void *stream) {
+    if (int s = injected()) return s;
+    CcDims D;
+    if (int s = cc_dims("cc_select_compact", shape, &D)) return s;
+    if (!surprise || !K || !V || !tokens || !kept_idx || !K_out || !V_out || !tokens_out)
+        return fail(KVE_EINVAL, "cc_select_compact: null argument");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    {
+        ProfScope ps("cc_select_compact", 1, st);
+        e = launch_cc_select(D, surprise, K, V, tokens, kept_idx, K_out, V_out, tokens_out, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "cc_select_compact: launch");
     return KVE_OK;
 }
 

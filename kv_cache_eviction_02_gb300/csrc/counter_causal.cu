@@ -1,0 +1,343 @@
+// Counter-causal surprise refresh, fast single-layer variant (counter-causal page, "Back from the
+// Future: KV Cache Management by Counter-Causal Surprise": Section 3.2 steps 1-5, Section 3.3,
+// Algorithm 3, design choice 4).
+//
+//   cc_attn_kernel      o_i^h = sum_{j>i} softmax_j(q_i^h . k_j / sqrt d) v_j over the cached K/V
+//                       (strictly upper-triangular mask, fresh queries); one warp per query, K tiles
+//                       of 32 keys staged in padded shared memory (lane l scores key l), online
+//                       softmax, lanes hold d/32 output columns each.
+//   cc_proj_kernel      r_i = h_i + W_O o_i (o_i = the heads' outputs concatenated) as a tiled FP32
+//                       product, fused with the true token's unembedding row: each CTA writes the
+//                       partial logit sum_m W_U[x_i][m] r_i[m] over its 64 columns m.
+//   cc_finish_kernel    surprise_i = -(sum of the partial logits, fixed order); +inf for the sink
+//                       slots and the last token.
+//   cc_select_kernel    keep the J highest surprises (equal: the lower position), ascending order:
+//                       MSB-first radix select over shared-memory histograms, an ordered scan,
+//                       then 16-byte gathers of the kept K and V rows and token ids.
+#include "kve_internal.cuh"
+
+namespace kve {
+
+namespace {
+
+constexpr int kCcQueriesPerCta = 8;  // one warp per query
+constexpr int kCcKeys = 32;          // keys per staged tile
+
+template <typename T>
+__global__ void __launch_bounds__(kCcQueriesPerCta * 32) cc_attn_kernel(
+    const T *__restrict__ K, const T *__restrict__ V, const T *__restrict__ Q, int n, int hq,
+    int hkv, int d, float scale, float *__restrict__ O) {
+    __shared__ float ks[kCcKeys][129];  // padded: lane l reads row l column c conflict-free
+    __shared__ float vs[kCcKeys][128];
+    __shared__ float qs[kCcQueriesPerCta][128];
+    const int b = blockIdx.z, h = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i0 = blockIdx.x * kCcQueriesPerCta;
+    const int i = i0 + warp;
+    const int kh = h / (hq / hkv);
+    const T *Kb = K + ((size_t)b * hkv + kh) * n * d;
+    const T *Vb = V + ((size_t)b * hkv + kh) * n * d;
+    const T *Qb = Q + ((size_t)b * hq + h) * n * d;
+    for (int e = threadIdx.x; e < kCcQueriesPerCta * d; e += blockDim.x) {
+        const int r = e / d, c = e % d;
+        qs[r][c] = (i0 + r < n) ? to_f(Qb[(size_t)(i0 + r) * d + c]) * scale : 0.f;
+    }
+    const int per = d >> 5;  // output columns per lane (d = 32, 64 or 128): lane + 32 e
+    float o[4] = {0.f, 0.f, 0.f, 0.f};
+    float m = -INFINITY, l = 0.f;
+    for (int j0 = i0 + 1; j0 < n; j0 += kCcKeys) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < kCcKeys * d; e += blockDim.x) {
+            const int r = e / d, c = e % d;
+            const bool in = j0 + r < n;
+            ks[r][c] = in ? to_f(Kb[(size_t)(j0 + r) * d + c]) : 0.f;
+            vs[r][c] = in ? to_f(Vb[(size_t)(j0 + r) * d + c]) : 0.f;
+        }
+        __syncthreads();
+        if (i >= n) continue;
+        const int j = j0 + lane;
+        float s = 0.f;
+        for (int c = 0; c < d; ++c) s = fmaf(qs[warp][c], ks[lane][c], s);
+        const bool valid = j > i && j < n;
+        const float sv = valid ? s : -INFINITY;
+        const float mt = warp_max(sv);
+        if (mt == -INFINITY) continue;  // no visible key in this tile (warp-uniform)
+        const float mn = fmaxf(m, mt);
+        const float corr = __expf(m - mn);  // exp(-inf) = 0 on the first visible tile
+        const float p = valid ? __expf(s - mn) : 0.f;
+        l = l * corr + warp_sum(p);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] *= corr;
+        for (int r = 0; r < kCcKeys; ++r) {
+            const float pr = __shfl_sync(0xffffffffu, p, r);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (e < per) o[e] = fmaf(pr, vs[r][lane + 32 * e], o[e]);
+        }
+        m = mn;
+    }
+    if (i < n) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;  // the last token sees no key: o = 0
+        float *dst = O + ((size_t)b * n + i) * hq * d + (size_t)h * d + lane;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (e < per) dst[32 * e] = o[e] * inv;
+    }
+}
+
+// r = h + W_O o and the partial logits; CTA tile 64 tokens x 64 columns m, K chunks of 32.
+constexpr int kPT = 64, kPM = 64, kPK = 32;
+
+template <typename T>
+__global__ void __launch_bounds__(256) cc_proj_kernel(
+    const float *__restrict__ O, const T *__restrict__ Hres, const T *__restrict__ W_O,
+    const T *__restrict__ W_U, const int32_t *__restrict__ X, int n, int kdim, int dm, int vocab,
+    float *__restrict__ part, unsigned *err) {
+    __shared__ float as[kPT][kPK + 1];
+    __shared__ float bs[kPM][kPK + 1];
+    const int b = blockIdx.z;
+    const int t0 = blockIdx.x * kPT, m0 = blockIdx.y * kPM;
+    const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;  // 16 x 16 threads, 4 x 4 outputs
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
+    const float *Ob = O + (size_t)b * n * kdim;
+    for (int k0 = 0; k0 < kdim; k0 += kPK) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < kPT * kPK; e += 256) {
+            const int r = e / kPK, c = e % kPK;
+            const int t = t0 + r, k = k0 + c;
+            as[r][c] = (t < n && k < kdim) ? Ob[(size_t)t * kdim + k] : 0.f;
+            const int mm = m0 + r;
+            bs[r][c] = (mm < dm && k < kdim) ? to_f(W_O[(size_t)mm * kdim + k]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int c = 0; c < kPK; ++c) {
+            float av[4], bv[4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) av[a] = as[ty * 4 + a][c];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) bv[q] = bs[tx * 4 + q][c];
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[a][q] = fmaf(av[a], bv[q], acc[a][q]);
+        }
+    }
+    // epilogue: r = acc + h, partial logit over this CTA's columns for each of the 4 tokens
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int t = t0 + ty * 4 + a;
+        float z = 0.f;
+        if (t < n) {
+            int x = X[(size_t)b * n + t];
+            if (x < 0 || x >= vocab) {  // reported, and the row treated as token 0
+                if (err) atomicOr(err, KVE_DEVERR_BADINDEX);
+                x = 0;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int mm = m0 + tx * 4 + q;
+                if (mm < dm) {
+                    const float r = acc[a][q] + to_f(Hres[((size_t)b * n + t) * dm + mm]);
+                    z = fmaf(to_f(W_U[(size_t)x * dm + mm]), r, z);
+                }
+            }
+        }
+        // sum over the 16 threads (tx) that share these tokens: lanes 0-15 / 16-31 of a warp
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+        if (tx == 0 && t < n) part[((size_t)b * gridDim.y + blockIdx.y) * n + t] = z;
+    }
+}
+
+__global__ void cc_finish_kernel(const float *__restrict__ part, int n, int mtiles, int sink,
+                                 float *__restrict__ surprise) {
+    const int b = blockIdx.y;
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= n) return;
+    float z = 0.f;
+    for (int k = 0; k < mtiles; ++k) z += part[((size_t)b * mtiles + k) * n + t];
+    surprise[(size_t)b * n + t] = (t < sink || t == n - 1) ? INFINITY : -z;
+}
+
+__device__ __forceinline__ uint32_t cc_key(float f) {  // order-preserving (+inf largest)
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+constexpr int kSelT = 1024;
+
+// Exclusive block-wide scan of one value per thread; *total = the block's sum. All threads call.
+__device__ __forceinline__ int cc_scan(int v, int *warp_tot, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    int before = 0, tot = 0;
+    for (int w = 0; w < kSelT / 32; ++w) {
+        const int t = warp_tot[w];
+        before += w < warp ? t : 0;
+        tot += t;
+    }
+    __syncthreads();
+    *total = tot;
+    return before + x - v;
+}
+
+template <typename VecT>
+__global__ void __launch_bounds__(kSelT) cc_select_kernel(
+    const float *__restrict__ surprise, const VecT *__restrict__ K, const VecT *__restrict__ V,
+    const int32_t *__restrict__ X, int n, int J, int hkv, int vpr, int32_t *__restrict__ kept,
+    VecT *__restrict__ K_out, VecT *__restrict__ V_out, int32_t *__restrict__ X_out) {
+    __shared__ uint32_t hist[256];
+    __shared__ int warp_tot[32];
+    __shared__ uint32_t s_prefix;
+    __shared__ int s_krem;
+    const int b = blockIdx.x;
+    const float *S = surprise + (size_t)b * n;
+    int32_t *kb = kept + (size_t)b * J;
+    if (threadIdx.x == 0) {
+        s_prefix = 0u;
+        s_krem = J;
+    }
+    __syncthreads();
+    if (J < n) {
+        for (int pass = 0; pass < 4; ++pass) {
+            const int shift = 24 - 8 * pass;
+            const uint32_t mask = pass == 0 ? 0u : (0xffffffffu << (shift + 8));
+            for (int i = threadIdx.x; i < 256; i += kSelT) hist[i] = 0u;
+            __syncthreads();
+            const uint32_t prefix = s_prefix;
+            for (int i = threadIdx.x; i < n; i += kSelT) {
+                const uint32_t key = cc_key(S[i]);
+                if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+            }
+            __syncthreads();
+            if (threadIdx.x < 32) {  // warp 0 finds the bin of the krem-th largest key
+                const int lane = threadIdx.x;
+                uint32_t c[8];
+                int sum = 0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    c[k] = hist[255 - 8 * lane - k];
+                    sum += (int)c[k];
+                }
+                int incl = sum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const int krem = s_krem;
+                const unsigned ball = __ballot_sync(0xffffffffu, incl >= krem);
+                if (ball != 0u && lane == __ffs(ball) - 1) {
+                    int kr = krem - (incl - sum);
+                    int bsel = 248 - 8 * lane;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        if ((int)c[k] >= kr) {
+                            bsel = 255 - 8 * lane - k;
+                            break;
+                        }
+                        kr -= (int)c[k];
+                    }
+                    s_krem = kr;
+                    s_prefix = prefix | ((uint32_t)bsel << shift);
+                }
+            }
+            __syncthreads();
+        }
+    }
+    const uint32_t tau = s_prefix;
+    const int take_eq = s_krem;  // keys equal to tau that stay, lower positions first
+    int run_eq = 0, run = 0;
+    for (int base = 0; base < n; base += kSelT) {
+        const int i = base + threadIdx.x;
+        uint32_t key = 0u;
+        if (i < n) key = cc_key(S[i]);
+        const int eq = (J < n && i < n && key == tau) ? 1 : 0;
+        int tot_eq;
+        const int rank_eq = run_eq + cc_scan(eq, warp_tot, &tot_eq);
+        const int sel = (i < n && (J >= n || key > tau || (eq && rank_eq < take_eq))) ? 1 : 0;
+        int tot;
+        const int slot = run + cc_scan(sel, warp_tot, &tot);
+        if (sel) kb[slot] = i;
+        run_eq += tot_eq;
+        run += tot;
+    }
+    __syncthreads();
+    // gather: K', V' per KV head, token ids
+    for (int e = threadIdx.x; e < hkv * J * vpr; e += kSelT) {
+        const int c = e % vpr, r = (e / vpr) % J, kh = e / (vpr * J);
+        const size_t src = (((size_t)b * hkv + kh) * n + kb[r]) * vpr + c;
+        const size_t dst = (((size_t)b * hkv + kh) * J + r) * vpr + c;
+        K_out[dst] = K[src];
+        V_out[dst] = V[src];
+    }
+    for (int r = threadIdx.x; r < J; r += kSelT) X_out[(size_t)b * J + r] = X[(size_t)b * n + kb[r]];
+}
+
+template <typename T>
+cudaError_t cc_surprise_t(const CcDims &D, const void *K, const void *V, const void *Q,
+                          const void *H, const void *W_O, const void *W_U, const int32_t *X,
+                          float *surprise, void *ws, unsigned *err, cudaStream_t st) {
+    char *w = static_cast<char *>(ws);
+    float *O = reinterpret_cast<float *>(w);
+    const int kdim = D.hq * D.d;
+    const int mtiles = (D.dm + kPM - 1) / kPM;
+    float *part = reinterpret_cast<float *>(w + cc_o_bytes(D));
+    cc_attn_kernel<T><<<dim3((D.n + kCcQueriesPerCta - 1) / kCcQueriesPerCta, D.hq, D.batch),
+                        kCcQueriesPerCta * 32, 0, st>>>(
+        (const T *)K, (const T *)V, (const T *)Q, D.n, D.hq, D.hkv, D.d,
+        1.f / sqrtf((float)D.d), O);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cc_proj_kernel<T><<<dim3((D.n + kPT - 1) / kPT, mtiles, D.batch), 256, 0, st>>>(
+        O, (const T *)H, (const T *)W_O, (const T *)W_U, X, D.n, kdim, D.dm, D.vocab, part, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cc_finish_kernel<<<dim3((D.n + 255) / 256, D.batch), 256, 0, st>>>(part, D.n, mtiles, D.sink,
+                                                                      surprise);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t cc_o_bytes(const CcDims &D) {
+    return ((size_t)D.batch * D.n * D.hq * D.d * sizeof(float) + 255) & ~size_t(255);
+}
+
+size_t cc_workspace_bytes(const CcDims &D) {
+    const size_t mtiles = (size_t)(D.dm + kPM - 1) / kPM;
+    return cc_o_bytes(D) + (((size_t)D.batch * mtiles * D.n * sizeof(float) + 255) & ~size_t(255));
+}
+
+cudaError_t launch_cc_surprise(const CcDims &D, const void *K, const void *V, const void *Q,
+                               const void *H, const void *W_O, const void *W_U, const int32_t *X,
+                               float *surprise, void *ws, unsigned *err, cudaStream_t st) {
+    if (D.dtype == KVE_F32)
+        return cc_surprise_t<float>(D, K, V, Q, H, W_O, W_U, X, surprise, ws, err, st);
+    return cc_surprise_t<__nv_bfloat16>(D, K, V, Q, H, W_O, W_U, X, surprise, ws, err, st);
+}
+
+cudaError_t launch_cc_select(const CcDims &D, const float *surprise, const void *K, const void *V,
+                             const int32_t *X, int32_t *kept, void *K_out, void *V_out,
+                             int32_t *X_out, cudaStream_t st) {
+    const size_t row = (size_t)D.d * dtype_size(D.dtype);
+    if (row % 16 != 0) return cudaErrorInvalidValue;
+    cc_select_kernel<uint4><<<D.batch, kSelT, 0, st>>>(
+        surprise, (const uint4 *)K, (const uint4 *)V, X, D.n, D.J, D.hkv, (int)(row / 16), kept,
+        (uint4 *)K_out, (uint4 *)V_out, X_out);
+    return cudaGetLastError();
+}
+
+}  // namespace kve

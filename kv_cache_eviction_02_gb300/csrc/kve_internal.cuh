@@ -26,7 +26,8 @@ inline size_t dtype_size(int dt) { return dt == KVE_F32 ? 4 : 2; }
 
 // ---- device error word -------------------------------------------------------------------------
 // Bit 0: a bounded wait on an mbarrier gave up. The host reads and clears it in kve_check_device.
-enum : unsigned { KVE_DEVERR_TIMEOUT = 1u };
+// Bit 1: a token id outside [0, vocab) reached the counter-causal logit kernel.
+enum : unsigned { KVE_DEVERR_TIMEOUT = 1u, KVE_DEVERR_BADINDEX = 2u };
 unsigned *device_error_word();  // device address of the word (per device, set up lazily)
 
 // Records a message for kve_last_error() on the calling thread and returns `code`.
@@ -128,5 +129,18 @@ cudaError_t launch_h2o_step(H2OState &s, const void *q, const void *k, const voi
                             cudaStream_t st);
 cudaError_t launch_h2o_export(const H2OState &s, void *K, void *V, int32_t *pos, float *acc,
                               int32_t *count, cudaStream_t st);
+
+// Counter-causal surprise refresh, fast single-layer variant (counter_causal.cu)
+struct CcDims {
+    int batch, hq, hkv, d, dm, n, vocab, dtype, sink, J;
+};
+size_t cc_o_bytes(const CcDims &D);
+size_t cc_workspace_bytes(const CcDims &D);
+cudaError_t launch_cc_surprise(const CcDims &D, const void *K, const void *V, const void *Q,
+                               const void *H, const void *W_O, const void *W_U, const int32_t *X,
+                               float *surprise, void *ws, unsigned *err, cudaStream_t st);
+cudaError_t launch_cc_select(const CcDims &D, const float *surprise, const void *K, const void *V,
+                             const int32_t *X, int32_t *kept, void *K_out, void *V_out,
+                             int32_t *X_out, cudaStream_t st);
 
 }  // namespace kve

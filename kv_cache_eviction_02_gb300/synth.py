@@ -35,8 +35,8 @@ import math
 
 import torch
 
-__all__ = ["LorekvConfig", "H2OConfig", "LOREKV_CONFIGS", "H2O_CONFIGS", "lorekv_inputs",
-           "h2o_inputs", "unit_slice", "zipf_table"]
+__all__ = ["LorekvConfig", "H2OConfig", "CcConfig", "LOREKV_CONFIGS", "H2O_CONFIGS",
+           "CC_CONFIGS", "lorekv_inputs", "h2o_inputs", "cc_inputs", "unit_slice", "zipf_table"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -108,6 +108,32 @@ class H2OConfig:
         return dataclasses.replace(self, **kw)
 
 
+@dataclasses.dataclass(frozen=True)
+class CcConfig:
+    """One counter-causal refresh: the last layer of ``batch`` sequences of ``n`` cached tokens,
+    keeping ``J`` of them (J = floor(0.8 n): the refresh keeps J of J + h candidates with
+    h = J/4)."""
+    name: str
+    dtype: str            # "f32" | "bf16"
+    batch: int
+    Hq: int
+    Hkv: int
+    d: int
+    d_model: int
+    n: int
+    vocab: int
+    sink: int
+    J: int
+    seed: int = 0
+
+    @property
+    def g(self) -> int:
+        return self.Hq // self.Hkv
+
+    def replace(self, **kw) -> "CcConfig":
+        return dataclasses.replace(self, **kw)
+
+
 LOREKV_CONFIGS = {
     "tiny": LorekvConfig("tiny", "f32", S=1, L=1, Hq=1, Hkv=1, d=64, d_model=64, n=512,
                          vocab=1024, keys="normal"),
@@ -122,6 +148,16 @@ LOREKV_CONFIGS = {
 H2O_CONFIGS = {
     "opt30b": H2OConfig("opt30b", "f16", batch=64, L=48, H=56, d=128, prompt=512, steps=512),
     "tiny": H2OConfig("tiny", "f16", batch=1, L=1, H=2, d=64, prompt=64, steps=64),
+}
+
+CC_CONFIGS = {
+    # Qwen2.5-7B-shaped last layer: 28 query heads, 4 KV heads, d_head 128, d_model 3584
+    "qwen7b_512": CcConfig("qwen7b_512", "bf16", batch=1, Hq=28, Hkv=4, d=128, d_model=3584,
+                           n=512, vocab=152064, sink=4, J=409),
+    "qwen7b_4096": CcConfig("qwen7b_4096", "bf16", batch=1, Hq=28, Hkv=4, d=128, d_model=3584,
+                            n=4096, vocab=152064, sink=4, J=3276),
+    "tiny": CcConfig("tiny", "f32", batch=2, Hq=4, Hkv=2, d=64, d_model=96, n=203, vocab=300,
+                     sink=3, J=150),
 }
 
 _TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
@@ -283,3 +319,41 @@ def h2o_inputs(cfg: H2OConfig, device="cpu", steps=None) -> dict:
         k[t] = gk.to(dt)
         v[t] = torch.randn(Bt, L, H, d, generator=gen, device=dev).to(dt)
     return {"K": Kp, "V": Vp, "Q": Qp, "q": q, "k": k, "v": v}
+
+
+def cc_inputs(cfg: CcConfig, device="cpu") -> dict:
+    """All inputs of one counter-causal refresh, laid out as the C-ABI expects.
+
+    K, V     [batch][Hkv][n][d]     cfg.dtype (Zipf-biased keys along a per-KV-head direction mu)
+    Q_fresh  [batch][Hq][n][d]      cfg.dtype (g + 2 mu of the query head's KV head)
+    H_last   [batch][n][d_model]    cfg.dtype, N(0, 1)
+    W_O      [d_model][Hq*d]        cfg.dtype, N(0, 1/d_model)
+    W_U      [vocab][d_model]       cfg.dtype, N(0, 1/d_model)
+    tokens   [batch][n]             int32, uniform over the vocabulary
+    """
+    dt = _TORCH_DTYPE[cfg.dtype]
+    dev = torch.device(device)
+    B, Hq, Hkv, d, n, dm = cfg.batch, cfg.Hq, cfg.Hkv, cfg.d, cfg.n, cfg.d_model
+    mu = 2.0 * _unit_vectors(Hkv, d, _gen(dev, cfg.seed, cfg.name, "mu"), dev)
+    K = torch.empty(B, Hkv, n, d, dtype=dt, device=dev)
+    V = torch.empty_like(K)
+    Q = torch.empty(B, Hq, n, d, dtype=dt, device=dev)
+    H = torch.empty(B, n, dm, dtype=dt, device=dev)
+    X = torch.empty(B, n, dtype=torch.int32, device=dev)
+    for b in range(B):
+        gen = _gen(dev, cfg.seed, cfg.name, "seq", b)
+        gk = torch.randn(Hkv, n, d, generator=gen, device=dev)
+        gk += _zipf((Hkv, n), gen, dev)[..., None] * mu[:, None, :]
+        K[b] = gk.to(dt)
+        V[b] = torch.randn(Hkv, n, d, generator=gen, device=dev).to(dt)
+        Q[b] = (torch.randn(Hq, n, d, generator=gen, device=dev)
+                + 2.0 * mu.repeat_interleave(cfg.g, dim=0)[:, None, :]).to(dt)
+        H[b] = torch.randn(n, dm, generator=gen, device=dev).to(dt)
+        X[b] = torch.randint(0, cfg.vocab, (n,), generator=gen, device=dev, dtype=torch.int32)
+    gw = _gen(dev, cfg.seed, cfg.name, "weights")
+    W_O = (torch.randn(dm, Hq * d, generator=gw, device=dev) / math.sqrt(dm)).to(dt)
+    W_U = torch.empty(cfg.vocab, dm, dtype=dt, device=dev)
+    for r0 in range(0, cfg.vocab, 16384):   # bounded float32 temporaries
+        r1 = min(cfg.vocab, r0 + 16384)
+        W_U[r0:r1] = (torch.randn(r1 - r0, dm, generator=gw, device=dev) / math.sqrt(dm)).to(dt)
+    return {"K": K, "V": V, "Q_fresh": Q, "H_last": H, "W_O": W_O, "W_U": W_U, "tokens": X}

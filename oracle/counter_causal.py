@@ -32,24 +32,31 @@ def _d(a) -> np.ndarray:
     return np.asarray(a, dtype=np.float64)
 
 
-def cc_attention(K, V, Qf) -> np.ndarray:
-    """Counter-causal attention of one sequence (Section 3.2, step 1).
+def cc_attention_rows(K, V, Qf, rows) -> np.ndarray:
+    """Counter-causal attention of one sequence at the listed positions (Section 3.2, step 1).
 
     K, V [H_kv][n][d]; Qf [H_q][n][d] fresh queries. Position i attends to positions j > i only:
-    o_i^h = sum_{j>i} softmax_j(q_i^h . k_j / sqrt d) v_j. The last position sees nothing (o = 0).
-    Returns o [n][H_q][d]."""
+    o_i^h = sum_{j>i} softmax_j(q_i^h . k_j / sqrt d) v_j; query head h reads KV head
+    h // (H_q / H_kv). The last position sees nothing (o = 0). Returns o [len(rows)][H_q][d]."""
     K, V, Qf = _d(K), _d(V), _d(Qf)
     hkv, n, d = K.shape
     hq = Qf.shape[0]
     g = hq // hkv
-    o = np.zeros((n, hq, d))
-    for h in range(hq):
-        kh = h // g
-        for i in range(n - 1):
+    o = np.zeros((len(rows), hq, d))
+    for r, i in enumerate(rows):
+        if i >= n - 1:
+            continue
+        for h in range(hq):
+            kh = h // g
             s = K[kh, i + 1:] @ Qf[h, i] / math.sqrt(d)
             a = np.exp(s - s.max())
-            o[i, h] = (a / a.sum()) @ V[kh, i + 1:]
+            o[r, h] = (a / a.sum()) @ V[kh, i + 1:]
     return o
+
+
+def cc_attention(K, V, Qf) -> np.ndarray:
+    """Counter-causal attention at every position of one sequence: o [n][H_q][d]."""
+    return cc_attention_rows(K, V, Qf, range(_d(K).shape[1]))
 
 
 def cc_logits(o, Hres, W_O, W_U, X) -> np.ndarray:

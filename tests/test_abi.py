@@ -106,6 +106,50 @@ def test_fidelity_rejects_bad_arguments_before_touching_the_gpu(api):
     assert L.lorekv_output_fidelity(fake, fake, 4, 0, fake, None, None) == api.KVE_EINVAL
 
 
+def _cc(api, **kw):
+    base = dict(n_seq=2, n_q_heads=28, n_kv_heads=4, d_head=128, d_model=3584, n_tokens=512,
+                vocab=1000, dtype=api.KVE_BF16, sink=4, keep_J=410)
+    base.update(kw)
+    return api.CcProblem(**base)
+
+
+def test_cc_workspace_size_covers_the_attention_outputs(api):
+    ws = api.cc_workspace_size(_cc(api))
+    assert ws >= 2 * 512 * 28 * 128 * 4 and ws % 256 == 0
+    assert api.cc_workspace_size(_cc(api, n_tokens=1024)) > ws
+
+
+@pytest.mark.parametrize("bad", [
+    dict(n_q_heads=27),            # not a multiple of n_kv_heads
+    dict(d_head=96),               # unsupported head size
+    dict(keep_J=0), dict(keep_J=513),
+    dict(sink=-1), dict(sink=513),
+    dict(dtype=2),                 # f16 not supported here
+    dict(vocab=0),
+])
+def test_cc_invalid_shapes_are_rejected_without_a_gpu(api, bad):
+    pb = _cc(api, **bad)
+    assert api.cc_workspace_size(pb) == 0
+    L, sh, fake = api.lib(), pb.shape(), ctypes.c_void_p(256)
+    st = L.cc_surprise(ctypes.byref(sh), fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                       1 << 40, None)
+    assert st in (api.KVE_EINVAL, api.KVE_EDTYPE)
+    st = L.cc_select_compact(ctypes.byref(sh), fake, fake, fake, fake, fake, fake, fake, fake, None)
+    assert st in (api.KVE_EINVAL, api.KVE_EDTYPE)
+
+
+def test_cc_rejects_bad_arguments_before_touching_the_gpu(api):
+    L, sh, fake = api.lib(), _cc(api).shape(), ctypes.c_void_p(256)
+    st = L.cc_surprise(ctypes.byref(sh), fake, fake, fake, fake, fake, fake, fake, fake, None, 0,
+                       None)
+    assert st == api.KVE_EWORKSPACE and "workspace" in L.kve_last_error().decode()
+    st = L.cc_surprise(ctypes.byref(sh), fake, None, fake, fake, fake, fake, fake, fake, fake,
+                       1 << 40, None)
+    assert st == api.KVE_EINVAL
+    st = L.cc_select_compact(ctypes.byref(sh), fake, fake, fake, None, fake, fake, fake, fake, None)
+    assert st == api.KVE_EINVAL
+
+
 def test_h2o_create_validates_arguments(api):
     L = api.lib()
     h = ctypes.c_void_p()

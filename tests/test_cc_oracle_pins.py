@@ -94,3 +94,11 @@ def test_select_matches_exhaustive_enumeration(seed):
             best = (key, sub)
     assert cc.cc_select(s, J).tolist() == list(best[1])
     assert cc.cc_select(s, n).tolist() == list(range(n))
+
+
+def test_row_evaluation_matches_the_whole_sequence():
+    """Evaluating selected positions (used at full sizes) gives the same rows as the whole pass."""
+    rng = np.random.default_rng(6)
+    K, V, Q = _rand(rng, 2, 15, 8), _rand(rng, 2, 15, 8), _rand(rng, 6, 15, 8)
+    rows = [14, 0, 7, 13, 3]
+    assert np.array_equal(cc.cc_attention_rows(K, V, Q, rows), cc.cc_attention(K, V, Q)[rows])
