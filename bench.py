@@ -55,6 +55,7 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-fidelity", action="store_true")
+    p.add_argument("--no-cc", action="store_true", help="skip the counter-causal refresh")
     p.add_argument("--workload", default=WORKLOAD)
     p.add_argument("--h2o-batch", type=int, default=64, help="H2O batch (64 = OPT-30B workload)")
     p.add_argument("--h2o-steps", type=int, default=512, help="H2O decode steps")
@@ -409,6 +410,8 @@ def run_native(args):
 
     if not args.no_h2o:
         line["h2o"] = bench_h2o(dev, stream, pg, world, args, pk)
+    if not args.no_cc:
+        line["cc_refresh"] = bench_cc(dev, stream, pg, args)
     if rank == 0 and not args.no_cpu:
         try:
             cb = cpu_baseline(cfg)
@@ -662,6 +665,98 @@ def bench_h2o(dev, stream, pg, world, args, pk):
             "roofline": {"kernel": "h2o_step", "bound": "hbm", "achieved": ach,
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
                          "traffic": None, "bytes_per_launch": per_step_bytes}}
+
+
+# Counter-causal refresh latency of the fast single-layer variant on the page's own setup (Qwen2.5-
+# 7B, fp16, RTX 4090; review of "Back from the Future", Table 1): context, not a target.
+CC_PAGE_MS = {"qwen7b_512": 7.9, "qwen7b_4096": 52.6}
+
+
+def cc_attention_flops(cfg) -> int:
+    """Counter-causal attention: per query head and visible (i, j > i) pair, q.k and p v."""
+    return cfg.batch * cfg.Hq * (cfg.n * (cfg.n - 1) // 2) * 4 * cfg.d
+
+
+def cc_logits_flops(cfg) -> int:
+    """r = h + W_O o over all tokens, then the true token's logit W_U[x] . r."""
+    return cfg.batch * cfg.n * (2 * cfg.d_model * cfg.Hq * cfg.d + 2 * cfg.d_model)
+
+
+def bench_cc(dev, stream, pg, args):
+    """Counter-causal surprise refresh (fast single-layer variant): cc_surprise +
+    cc_select_compact on the Qwen2.5-7B-shaped last layer at n = 512 and 4096. Each refresh is
+    timed alone with CUDA events after a 256 MB write that flushes L2 (the inputs fit in it)."""
+    import torch
+    from kv_cache_eviction_02_gb300 import api, synth
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+    for name in ("qwen7b_512", "qwen7b_4096"):
+        cfg = synth.CC_CONFIGS[name]
+        inp = synth.cc_inputs(cfg, dev)
+        pb = api.CcProblem(cfg.batch, cfg.Hq, cfg.Hkv, cfg.d, cfg.d_model, cfg.n, cfg.vocab,
+                           api.KVE_BF16, cfg.sink, cfg.J)
+        ws = torch.empty(api.cc_workspace_size(pb), dtype=torch.uint8, device=dev)
+        s = torch.empty(cfg.batch, cfg.n, dtype=torch.float32, device=dev)
+        kept = torch.empty(cfg.batch, cfg.J, dtype=torch.int32, device=dev)
+        Ko = torch.empty(cfg.batch, cfg.Hkv, cfg.J, cfg.d, dtype=torch.bfloat16, device=dev)
+        Vo = torch.empty_like(Ko)
+        Xo = torch.empty(cfg.batch, cfg.J, dtype=torch.int32, device=dev)
+
+        def refresh():
+            api.cc_surprise(pb, inp["K"], inp["V"], inp["Q_fresh"], inp["H_last"], inp["W_O"],
+                            inp["W_U"], inp["tokens"], s, ws, stream)
+            api.cc_select_compact(pb, s, inp["K"], inp["V"], inp["tokens"], kept, Ko, Vo, Xo,
+                                  stream)
+
+        for _ in range(max(args.warmup, 3)):
+            refresh()
+        api.kve_check_device()
+        steps = max(1, min(args.steps, 20))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        barrier(pg)
+        torch.cuda.synchronize(dev)
+        api.kve_profile_enable(True)
+        with ClockSampler(dev.index) as clk:
+            for e0, e1 in ev:
+                with torch.cuda.stream(stream):
+                    flush.zero_()
+                e0.record(stream)
+                refresh()
+                e1.record(stream)
+            torch.cuda.synchronize(dev)
+        api.kve_profile_enable(False)
+        prof = api.kve_profile_report()
+        api.kve_check_device()
+        ms = max_over_ranks(pg, sum(a.elapsed_time(b) for a, b in ev) / steps, dev)
+        stages = {k: v["ms"] / v["groups"] for k, v in prof.items()}
+        ck = clk.summary()
+        mhz = ck["sm_mhz"] or 2070.0
+        alu_peak = 152 * 128 * 2 * mhz * 1e6 / 1e12
+        att_ms = stages.get("cc_attention")
+        ach = cc_attention_flops(cfg) / (att_ms / 1e3) / 1e12 if att_ms else None
+        out[name] = {
+            "ms_per_refresh": ms, "steps": steps,
+            "config": f"{name}: batch {cfg.batch}, {cfg.Hq}/{cfg.Hkv} heads, d_head {cfg.d}, "
+                      f"d_model {cfg.d_model}, vocab {cfg.vocab}, n {cfg.n}, keep J {cfg.J}, "
+                      f"sink {cfg.sink}, bf16; L2 flushed before each refresh",
+            "stages_ms": stages,
+            "gpu_launches_per_refresh": sum(v["kernels"] for v in prof.values()) // steps,
+            "page_ms_rtx4090_fp16": CC_PAGE_MS[name],
+            "roofline": {"kernel": "cc_attention", "bound": "alu", "achieved": ach,
+                         "peak": alu_peak, "unit": "TFLOP/s",
+                         "frac": ach / alu_peak if ach else None, "traffic": None,
+                         "peak_source": f"FP32 FMA: 152 SMs x 128 lanes x 2 flop x {mhz:.0f} MHz "
+                                        "(median sampled SM clock)",
+                         "flops": cc_attention_flops(cfg)},
+            "logits_tflops": (cc_logits_flops(cfg) / (stages["cc_logits"] / 1e3) / 1e12
+                              if stages.get("cc_logits") else None),
+            "clocks": ck}
+        del inp, ws, s, kept, Ko, Vo, Xo
+        torch.cuda.empty_cache()
+    del flush
+    torch.cuda.empty_cache()
+    return out
 
 
 def main():

@@ -482,9 +482,12 @@ int cc_surprise(const KveCcShape *shape, const void *K, const void *V, const voi
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     {
-        ProfScope ps("cc_surprise", 3, st);
-        e = launch_cc_surprise(D, K, V, Q_fresh, H_last, W_O, W_U, tokens, surprise_out, workspace,
-                               err, st);
+        ProfScope ps("cc_attention", 1, st);
+        e = launch_cc_attention(D, K, V, Q_fresh, workspace, st);
+    }
+    if (e == cudaSuccess) {
+        ProfScope ps("cc_logits", 2, st);
+        e = launch_cc_logits(D, H_last, W_O, W_U, tokens, surprise_out, workspace, err, st);
     }
     if (e != cudaSuccess) return cuda_fail(e, "cc_surprise: launch");
     return KVE_OK;

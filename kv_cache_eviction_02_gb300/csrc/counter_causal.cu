@@ -287,23 +287,24 @@ __global__ void __launch_bounds__(kSelT) cc_select_kernel(
 }
 
 template <typename T>
-cudaError_t cc_surprise_t(const CcDims &D, const void *K, const void *V, const void *Q,
-                          const void *H, const void *W_O, const void *W_U, const int32_t *X,
-                          float *surprise, void *ws, unsigned *err, cudaStream_t st) {
-    char *w = static_cast<char *>(ws);
-    float *O = reinterpret_cast<float *>(w);
-    const int kdim = D.hq * D.d;
-    const int mtiles = (D.dm + kPM - 1) / kPM;
-    float *part = reinterpret_cast<float *>(w + cc_o_bytes(D));
+cudaError_t cc_attention_t(const CcDims &D, const void *K, const void *V, const void *Q, float *O,
+                           cudaStream_t st) {
     cc_attn_kernel<T><<<dim3((D.n + kCcQueriesPerCta - 1) / kCcQueriesPerCta, D.hq, D.batch),
                         kCcQueriesPerCta * 32, 0, st>>>(
         (const T *)K, (const T *)V, (const T *)Q, D.n, D.hq, D.hkv, D.d,
         1.f / sqrtf((float)D.d), O);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t cc_logits_t(const CcDims &D, const float *O, const void *H, const void *W_O,
+                        const void *W_U, const int32_t *X, float *part, float *surprise,
+                        unsigned *err, cudaStream_t st) {
+    const int mtiles = (D.dm + kPM - 1) / kPM;
     cc_proj_kernel<T><<<dim3((D.n + kPT - 1) / kPT, mtiles, D.batch), 256, 0, st>>>(
-        O, (const T *)H, (const T *)W_O, (const T *)W_U, X, D.n, kdim, D.dm, D.vocab, part, err);
-    e = cudaGetLastError();
+        O, (const T *)H, (const T *)W_O, (const T *)W_U, X, D.n, D.hq * D.d, D.dm, D.vocab, part,
+        err);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     cc_finish_kernel<<<dim3((D.n + 255) / 256, D.batch), 256, 0, st>>>(part, D.n, mtiles, D.sink,
                                                                       surprise);
@@ -321,12 +322,21 @@ size_t cc_workspace_bytes(const CcDims &D) {
     return cc_o_bytes(D) + (((size_t)D.batch * mtiles * D.n * sizeof(float) + 255) & ~size_t(255));
 }
 
-cudaError_t launch_cc_surprise(const CcDims &D, const void *K, const void *V, const void *Q,
-                               const void *H, const void *W_O, const void *W_U, const int32_t *X,
-                               float *surprise, void *ws, unsigned *err, cudaStream_t st) {
+cudaError_t launch_cc_attention(const CcDims &D, const void *K, const void *V, const void *Q,
+                                void *ws, cudaStream_t st) {
+    float *O = static_cast<float *>(ws);
+    if (D.dtype == KVE_F32) return cc_attention_t<float>(D, K, V, Q, O, st);
+    return cc_attention_t<__nv_bfloat16>(D, K, V, Q, O, st);
+}
+
+cudaError_t launch_cc_logits(const CcDims &D, const void *H, const void *W_O, const void *W_U,
+                             const int32_t *X, float *surprise, void *ws, unsigned *err,
+                             cudaStream_t st) {
+    const float *O = static_cast<const float *>(ws);
+    float *part = reinterpret_cast<float *>(static_cast<char *>(ws) + cc_o_bytes(D));
     if (D.dtype == KVE_F32)
-        return cc_surprise_t<float>(D, K, V, Q, H, W_O, W_U, X, surprise, ws, err, st);
-    return cc_surprise_t<__nv_bfloat16>(D, K, V, Q, H, W_O, W_U, X, surprise, ws, err, st);
+        return cc_logits_t<float>(D, O, H, W_O, W_U, X, part, surprise, err, st);
+    return cc_logits_t<__nv_bfloat16>(D, O, H, W_O, W_U, X, part, surprise, err, st);
 }
 
 cudaError_t launch_cc_select(const CcDims &D, const float *surprise, const void *K, const void *V,

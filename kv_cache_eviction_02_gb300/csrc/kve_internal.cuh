@@ -136,9 +136,13 @@ struct CcDims {
 };
 size_t cc_o_bytes(const CcDims &D);
 size_t cc_workspace_bytes(const CcDims &D);
-cudaError_t launch_cc_surprise(const CcDims &D, const void *K, const void *V, const void *Q,
-                               const void *H, const void *W_O, const void *W_U, const int32_t *X,
-                               float *surprise, void *ws, unsigned *err, cudaStream_t st);
+// attention outputs O [batch][n][hq*d] fp32 at the start of the workspace
+cudaError_t launch_cc_attention(const CcDims &D, const void *K, const void *V, const void *Q,
+                                void *ws, cudaStream_t st);
+// surprise from O, h, W_O, W_U[x] (partial logits after O in the workspace)
+cudaError_t launch_cc_logits(const CcDims &D, const void *H, const void *W_O, const void *W_U,
+                             const int32_t *X, float *surprise, void *ws, unsigned *err,
+                             cudaStream_t st);
 cudaError_t launch_cc_select(const CcDims &D, const float *surprise, const void *K, const void *V,
                              const int32_t *X, int32_t *kept, void *K_out, void *V_out,
                              int32_t *X_out, cudaStream_t st);
