@@ -411,7 +411,7 @@ def run_native(args):
     if not args.no_h2o:
         line["h2o"] = bench_h2o(dev, stream, pg, world, args, pk)
     if not args.no_cc:
-        line["cc_refresh"] = bench_cc(dev, stream, pg, args)
+        line["cc_refresh"] = bench_cc(dev, stream, pg, args, pk)
     if rank == 0 and not args.no_cpu:
         try:
             cb = cpu_baseline(cfg)
@@ -682,7 +682,7 @@ def cc_logits_flops(cfg) -> int:
     return cfg.batch * cfg.n * (2 * cfg.d_model * cfg.Hq * cfg.d + 2 * cfg.d_model)
 
 
-def bench_cc(dev, stream, pg, args):
+def bench_cc(dev, stream, pg, args, pk):
     """Counter-causal surprise refresh (fast single-layer variant): cc_surprise +
     cc_select_compact on the Qwen2.5-7B-shaped last layer at n = 512 and 4096. Each refresh is
     timed alone with CUDA events after a 256 MB write that flushes L2 (the inputs fit in it)."""
@@ -731,10 +731,14 @@ def bench_cc(dev, stream, pg, args):
         ms = max_over_ranks(pg, sum(a.elapsed_time(b) for a, b in ev) / steps, dev)
         stages = {k: v["ms"] / v["groups"] for k, v in prof.items()}
         ck = clk.summary()
-        mhz = ck["sm_mhz"] or 2070.0
-        alu_peak = 152 * 128 * 2 * mhz * 1e6 / 1e12
         att_ms = stages.get("cc_attention")
         ach = cc_attention_flops(cfg) / (att_ms / 1e3) / 1e12 if att_ms else None
+        # bf16 with d_head 128 runs on the tensor cores: a kernel timed alone, the burst peak
+        att_roof = {"kernel": "cc_attention", "bound": "tensor", "achieved": ach,
+                    "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": ach / pk["bf16_tflops"] if ach else None, "traffic": None,
+                    "peak_source": f"bf16 dense burst, {pk['source']}",
+                    "flops": cc_attention_flops(cfg), "ms_per_launch": att_ms}
         out[name] = {
             "ms_per_refresh": ms, "steps": steps,
             "config": f"{name}: batch {cfg.batch}, {cfg.Hq}/{cfg.Hkv} heads, d_head {cfg.d}, "
@@ -743,12 +747,7 @@ def bench_cc(dev, stream, pg, args):
             "stages_ms": stages,
             "gpu_launches_per_refresh": sum(v["kernels"] for v in prof.values()) // steps,
             "page_ms_rtx4090_fp16": CC_PAGE_MS[name],
-            "roofline": {"kernel": "cc_attention", "bound": "alu", "achieved": ach,
-                         "peak": alu_peak, "unit": "TFLOP/s",
-                         "frac": ach / alu_peak if ach else None, "traffic": None,
-                         "peak_source": f"FP32 FMA: 152 SMs x 128 lanes x 2 flop x {mhz:.0f} MHz "
-                                        "(median sampled SM clock)",
-                         "flops": cc_attention_flops(cfg)},
+            "roofline": att_roof,
             "logits_tflops": (cc_logits_flops(cfg) / (stages["cc_logits"] / 1e3) / 1e12
                               if stages.get("cc_logits") else None),
             "clocks": ck}

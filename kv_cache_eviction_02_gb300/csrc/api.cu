@@ -483,7 +483,7 @@ int cc_surprise(const KveCcShape *shape, const void *K, const void *V, const voi
     cudaError_t e;
     {
         ProfScope ps("cc_attention", 1, st);
-        e = launch_cc_attention(D, K, V, Q_fresh, workspace, st);
+        e = launch_cc_attention(D, K, V, Q_fresh, workspace, err, st);
     }
     if (e == cudaSuccess) {
         ProfScope ps("cc_logits", 2, st);

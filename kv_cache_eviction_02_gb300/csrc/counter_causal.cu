@@ -5,7 +5,9 @@
 //   cc_attn_kernel      o_i^h = sum_{j>i} softmax_j(q_i^h . k_j / sqrt d) v_j over the cached K/V
 //                       (strictly upper-triangular mask, fresh queries); one warp per query, K tiles
 //                       of 32 keys staged in padded shared memory (lane l scores key l), online
-//                       softmax, lanes hold d/32 output columns each.
+//                       softmax, lanes hold d/32 output columns each. Used for fp32 and for head
+//                       sizes other than 128; bf16 with d_head 128 runs on the tensor cores
+//                       (cc_tc.cu).
 //   cc_proj_kernel      r_i = h_i + W_O o_i (o_i = the heads' outputs concatenated) as a tiled FP32
 //                       product, fused with the true token's unembedding row: each CTA writes the
 //                       partial logit sum_m W_U[x_i][m] r_i[m] over its 64 columns m.
@@ -323,8 +325,9 @@ size_t cc_workspace_bytes(const CcDims &D) {
 }
 
 cudaError_t launch_cc_attention(const CcDims &D, const void *K, const void *V, const void *Q,
-                                void *ws, cudaStream_t st) {
+                                void *ws, unsigned *err, cudaStream_t st) {
     float *O = static_cast<float *>(ws);
+    if (cc_attention_tc_supported(D)) return launch_cc_attention_tc(D, K, V, Q, O, err, st);
     if (D.dtype == KVE_F32) return cc_attention_t<float>(D, K, V, Q, O, st);
     return cc_attention_t<__nv_bfloat16>(D, K, V, Q, O, st);
 }

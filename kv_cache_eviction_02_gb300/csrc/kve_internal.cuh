@@ -138,7 +138,11 @@ size_t cc_o_bytes(const CcDims &D);
 size_t cc_workspace_bytes(const CcDims &D);
 // attention outputs O [batch][n][hq*d] fp32 at the start of the workspace
 cudaError_t launch_cc_attention(const CcDims &D, const void *K, const void *V, const void *Q,
-                                void *ws, cudaStream_t st);
+                                void *ws, unsigned *err, cudaStream_t st);
+// tensor-core attention (cc_tc.cu): bf16, d_head 128, at least 128 K/V rows in all
+bool cc_attention_tc_supported(const CcDims &D);
+cudaError_t launch_cc_attention_tc(const CcDims &D, const void *K, const void *V, const void *Q,
+                                   float *O, unsigned *err, cudaStream_t st);
 // surprise from O, h, W_O, W_U[x] (partial logits after O in the workspace)
 cudaError_t launch_cc_logits(const CcDims &D, const void *H, const void *W_O, const void *W_U,
                              const int32_t *X, float *surprise, void *ws, unsigned *err,
