@@ -13,7 +13,8 @@
 //   warps 4-11   two softmax groups (one per query tile, one TMEM lane = one query row): mask to
 //                i < j < n, online softmax in the log2 domain with the rescale of O deferred until
 //                the row maximum grew by more than 2^8, P as bf16 pairs into TMEM; at the end
-//                o = O / l is written as fp32.
+//                o = O / l is written as fp32, or as bf16 when the tensor-core projection below
+//                consumes it.
 // Every wait is bounded (tc::mbar_wait), a warp gives up as a whole before warp-collective TMEM
 // instructions, and roles drain their copies and products in flight before TMEM is freed.
 #include <cudaTypedefs.h>
@@ -35,7 +36,8 @@ constexpr float kCaNoMax = -1e30f;     // running maximum before any visible tok
 struct CcAttnArgs {
     int n, hq, hkv, g, nblk, units;  // units = batch * hkv
     float k1;                        // log2(e) / sqrt(d)
-    float *O;                        // [batch][n][hq * 128] fp32
+    float *O;                        // [batch][n][hq * 128] fp32, or
+    __nv_bfloat16 *Ob;               // the same in bf16 (the tensor-core projection's operand)
     unsigned *err;
 };
 
@@ -283,14 +285,27 @@ __global__ void __launch_bounds__(kCaThreads, 1)
                        ok && tc::mbar_wait(&o_done[t], (ntl - 1) & 1, abort_flag, A.err))) {
             tc::fence_after_sync();
             const float inv = l > 0.f ? 1.f / l : 0.f;  // the last token sees no key: o = 0
-            float *dst = A.O + ((size_t)(b * A.n + i) * A.hq + kh * A.g + qt.hh) * 128;
+            const size_t off = ((size_t)(b * A.n + i) * A.hq + kh * A.g + qt.hh) * 128;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 float o[32];
                 tc::tmem_ld32(o_col + c * 32, o);
                 tc::tmem_wait_ld();
-                if (valid_row) {
-                    float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+                if (valid_row && A.Ob) {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(A.Ob + off + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const __nv_bfloat162 h2 = __floats2bfloat162_rn(
+                                o[8 * e + 2 * k] * inv, o[8 * e + 2 * k + 1] * inv);
+                            w[k] = *reinterpret_cast<const uint32_t *>(&h2);
+                        }
+                        d4[e] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                } else if (valid_row) {
+                    float4 *d4 = reinterpret_cast<float4 *>(A.O + off + c * 32);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         d4[e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv,
@@ -306,14 +321,227 @@ __global__ void __launch_bounds__(kCaThreads, 1)
     }
 }
 
+// ---- r = h + W_O o and the true token's logit, on the tensor cores -------------------------------
+//
+// cc_logits_tc_kernel: CTA tile of 128 tokens x 256 output columns m of d_model; the K loop runs
+// over o's H_q * 128 entries in steps of 64 (one 128-byte-swizzled TMA box of each operand per
+// step, 4-stage ring), one thread issues D += O W_O^T (M = 128, N = 256, K = 16 per instruction)
+// into 256 TMEM columns. The logit is linear in r, so the K loop may be split over CTAs: each split
+// contributes sum_m W_U[x_t][m] (its part of W_O o)_m, the first one also adds h. Epilogue: warps
+// 2-9, one TMEM lane (token) and 128 columns each, write one partial logit per (column tile,
+// split, column half); a fixed-order sum of the partials gives the logit.
+constexpr int kLgThreads = 320;  // TMA, MMA issuer, 8 epilogue warps
+constexpr int LG_STAGES = 4;
+constexpr uint32_t LG_A = 16384, LG_STAGE = LG_A + 32768;  // O: 128 x 64, W_O: 256 x 64 (bf16)
+constexpr uint32_t LG_BAR = LG_STAGES * LG_STAGE;
+constexpr size_t LG_SMEM = LG_BAR + 256 + 1024;
+
+struct CcLogitsArgs {
+    int n, dm, vocab, mtiles, ntiles, ksplit, ksteps, ksteps_per;
+    const __nv_bfloat16 *H, *W_U;
+    const int32_t *X;
+    float *part;  // [batch][ntiles * ksplit * 2][n]
+    unsigned *err;
+};
+
+__global__ void __launch_bounds__(kLgThreads, 1)
+    cc_logits_tc_kernel(const __grid_constant__ CUtensorMap tm_o,
+                        const __grid_constant__ CUtensorMap tm_w, CcLogitsArgs A) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int bx = blockIdx.x;
+    const int ks = bx % A.ksplit;
+    bx /= A.ksplit;
+    const int mt = bx % A.mtiles;
+    bx /= A.mtiles;
+    const int nt = bx % A.ntiles;
+    const int b = bx / A.ntiles;
+    const int kb = ks * A.ksteps_per;
+    const int nk = min(A.ksteps, kb + A.ksteps_per) - kb;  // >= 1 (host sizes the splits)
+    const int m0 = mt * 128, n0 = nt * 256;
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + LG_BAR);
+    uint64_t *full = bars, *empty = bars + LG_STAGES, *acc_full = bars + 2 * LG_STAGES,
+             *drain = bars + 2 * LG_STAGES + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * LG_STAGES + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * LG_STAGES + 3);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < LG_STAGES; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        tc::mbar_init(acc_full, 1);
+        tc::mbar_init(drain, 1);
+        *abort_flag = 0;
+        tc::mbar_fence_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 256);
+        tc::fence_before_sync();
+    }
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {  // ---- TMA producer ----
+            int issued = 0;
+            for (int s = 0; s < nk; ++s) {
+                const int slot = s % LG_STAGES;
+                if (!tc::mbar_wait(&empty[slot], ((s / LG_STAGES) & 1) ^ 1, abort_flag, A.err))
+                    break;
+                tc::mbar_expect_tx(&full[slot], LG_STAGE);
+                uint8_t *dst = sm + slot * LG_STAGE;
+                const int x = (kb + s) * 64;
+                tc::tma_load_2d(dst, &tm_o, x, b * A.n + m0, &full[slot]);
+                tc::tma_load_2d(dst + LG_A, &tm_w, x, n0, &full[slot]);
+                issued = s + 1;
+            }
+            for (int s = issued - LG_STAGES < 0 ? 0 : issued - LG_STAGES; s < issued; ++s)
+                tc::mbar_drain(&full[s % LG_STAGES], (s / LG_STAGES) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // ---- MMA issuer ----
+            constexpr uint32_t id = tc::idesc_bf16(128, 256, 0);
+            const uint32_t base = tc::smem_u32(sm);
+            bool ok = true;
+            for (int s = 0; s < nk; ++s) {
+                const int slot = s % LG_STAGES;
+                if (!tc::mbar_wait(&full[slot], (s / LG_STAGES) & 1, abort_flag, A.err)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint32_t a = base + slot * LG_STAGE, w = a + LG_A;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    tc::mma_bf16(tmem, tc::sdesc_sw128(a + k * 32, 16, 1024),
+                                 tc::sdesc_sw128(w + k * 32, 16, 1024), id, (s > 0 || k > 0));
+                tc::mma_commit(&empty[slot]);
+            }
+            if (ok) tc::mma_commit(acc_full);
+            tc::mma_commit(drain);  // every product issued has completed before TMEM is freed
+            tc::mbar_drain(drain, 0);
+        }
+    } else {  // ---- epilogue: warps 2-9 ----
+        const int lg = warp & 3, half = (warp - 2) >> 2;
+        const int t = m0 + lg * 32 + lane;
+        const bool valid = t < A.n;
+        int x = 0;
+        if (valid) {
+            x = A.X[(size_t)b * A.n + t];
+            if (x < 0 || x >= A.vocab) {  // reported, and the row read as token 0
+                if (A.err) atomicOr(A.err, KVE_DEVERR_BADINDEX);
+                x = 0;
+            }
+        }
+        if (tc::mbar_wait_warp(acc_full, 0, abort_flag, A.err)) {
+            tc::fence_after_sync();
+            const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
+            const __nv_bfloat16 *wu = A.W_U + (size_t)x * A.dm;
+            const __nv_bfloat16 *hr = A.H + ((size_t)b * A.n + (valid ? t : 0)) * A.dm;
+            float z = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                const int col = half * 128 + c * 32;
+                float acc[32];
+                tc::tmem_ld32(tmem + lane_off + col, acc);
+                tc::tmem_wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        const int m = n0 + col + e;
+                        if (m < A.dm) {  // d_model is a multiple of 8
+                            const uint4 wv = *reinterpret_cast<const uint4 *>(wu + m);
+                            uint4 hv = make_uint4(0u, 0u, 0u, 0u);
+                            if (ks == 0) hv = *reinterpret_cast<const uint4 *>(hr + m);
+                            const __nv_bfloat162 *w2 = reinterpret_cast<const __nv_bfloat162 *>(&wv);
+                            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&hv);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const float2 wf = __bfloat1622float2(w2[k]);
+                                const float2 hf = __bfloat1622float2(h2[k]);
+                                z = fmaf(wf.x, acc[e + 2 * k] + hf.x, z);
+                                z = fmaf(wf.y, acc[e + 2 * k + 1] + hf.y, z);
+                            }
+                        }
+                    }
+                }
+            }
+            if (valid)
+                A.part[((size_t)b * (A.ntiles * A.ksplit * 2) + (nt * A.ksplit + ks) * 2 + half) *
+                           A.n + t] = z;
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 256);
+    }
+}
+
 }  // namespace
+
+int cc_logits_tc_split(const CcDims &D) {
+    const long ctas = (long)D.batch * ((D.n + 127) / 128) * ((D.dm + 255) / 256);
+    const int ksteps = D.hq * D.d / 64;
+    int best = 1;
+    long best_cost = -1;
+    for (int p = 1; p <= kCcMaxKSplit && p <= ksteps; ++p) {
+        const int per = (ksteps + p - 1) / p;
+        const int used = (ksteps + per - 1) / per;  // splits that get at least one step
+        const long cost = ((ctas * used + 151) / 152) * per;
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = used;
+        }
+    }
+    return best;
+}
+
+bool cc_logits_tc_supported(const CcDims &D) {
+    return cc_attention_tc_supported(D) && D.dm % 8 == 0;
+}
+
+cudaError_t launch_cc_logits_tc(const CcDims &D, const __nv_bfloat16 *Ob, const void *H,
+                                const void *W_O, const void *W_U, const int32_t *X, float *part,
+                                int ksplit, unsigned *err, cudaStream_t st) {
+    const int kdim = D.hq * D.d;
+    CUtensorMap to, tw;
+    if (!make_tmap_bf16_2d(&to, Ob, kdim, (uint64_t)D.batch * D.n, 64, 128) ||
+        !make_tmap_bf16_2d(&tw, W_O, kdim, D.dm, 64, 256))
+        return cudaErrorInvalidValue;
+    CcLogitsArgs A;
+    A.n = D.n;
+    A.dm = D.dm;
+    A.vocab = D.vocab;
+    A.mtiles = (D.n + 127) / 128;
+    A.ntiles = (D.dm + 255) / 256;
+    A.ksteps = kdim / 64;
+    A.ksteps_per = (A.ksteps + ksplit - 1) / ksplit;
+    A.ksplit = (A.ksteps + A.ksteps_per - 1) / A.ksteps_per;
+    A.H = static_cast<const __nv_bfloat16 *>(H);
+    A.W_U = static_cast<const __nv_bfloat16 *>(W_U);
+    A.X = X;
+    A.part = part;
+    A.err = err;
+    const long grid = (long)D.batch * A.mtiles * A.ntiles * A.ksplit;
+    if (grid > 0x7fffffffL) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(cc_logits_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LG_SMEM);
+    if (e != cudaSuccess) return e;
+    cc_logits_tc_kernel<<<(unsigned)grid, kLgThreads, LG_SMEM, st>>>(to, tw, A);
+    return cudaGetLastError();
+}
 
 bool cc_attention_tc_supported(const CcDims &D) {
     return D.dtype == KVE_BF16 && D.d == 128 && (long)D.batch * D.hkv * D.n >= 128;
 }
 
 cudaError_t launch_cc_attention_tc(const CcDims &D, const void *K, const void *V, const void *Q,
-                                   float *O, unsigned *err, cudaStream_t st) {
+                                   float *O, __nv_bfloat16 *Ob, unsigned *err, cudaStream_t st) {
     CUtensorMap tk, tv, tq;
     const uint64_t kv_rows = (uint64_t)D.batch * D.hkv * D.n;
     const uint64_t q_rows = (uint64_t)D.batch * D.hq * D.n;
@@ -330,6 +558,7 @@ cudaError_t launch_cc_attention_tc(const CcDims &D, const void *K, const void *V
     A.units = D.batch * D.hkv;
     A.k1 = kLog2e / sqrtf(128.f);
     A.O = O;
+    A.Ob = Ob;
     A.err = err;
     const long pairs = ((long)A.g * A.nblk + 1) / 2;
     const long grid = pairs * A.units;

@@ -16,6 +16,8 @@
 //   cc_select_kernel    keep the J highest surprises (equal: the lower position), ascending order:
 //                       MSB-first radix select over shared-memory histograms, an ordered scan,
 //                       then 16-byte gathers of the kept K and V rows and token ids.
+#include <algorithm>
+
 #include "kve_internal.cuh"
 
 namespace kve {
@@ -156,13 +158,13 @@ __global__ void __launch_bounds__(256) cc_proj_kernel(
     }
 }
 
-__global__ void cc_finish_kernel(const float *__restrict__ part, int n, int mtiles, int sink,
+__global__ void cc_finish_kernel(const float *__restrict__ part, int n, int parts, int sink,
                                  float *__restrict__ surprise) {
     const int b = blockIdx.y;
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= n) return;
     float z = 0.f;
-    for (int k = 0; k < mtiles; ++k) z += part[((size_t)b * mtiles + k) * n + t];
+    for (int k = 0; k < parts; ++k) z += part[((size_t)b * parts + k) * n + t];
     surprise[(size_t)b * n + t] = (t < sink || t == n - 1) ? INFINITY : -z;
 }
 
@@ -320,14 +322,20 @@ size_t cc_o_bytes(const CcDims &D) {
 }
 
 size_t cc_workspace_bytes(const CcDims &D) {
-    const size_t mtiles = (size_t)(D.dm + kPM - 1) / kPM;
-    return cc_o_bytes(D) + (((size_t)D.batch * mtiles * D.n * sizeof(float) + 255) & ~size_t(255));
+    // partial logits: ceil(d_model/64) column tiles (CUDA cores) or ceil(d_model/256) column
+    // tiles x K splits x 2 column halves (tensor cores)
+    const size_t parts = std::max<size_t>((D.dm + kPM - 1) / kPM,
+                                          (size_t)((D.dm + 255) / 256) * kCcMaxKSplit * 2);
+    return cc_o_bytes(D) + (((size_t)D.batch * parts * D.n * sizeof(float) + 255) & ~size_t(255));
 }
 
 cudaError_t launch_cc_attention(const CcDims &D, const void *K, const void *V, const void *Q,
                                 void *ws, unsigned *err, cudaStream_t st) {
     float *O = static_cast<float *>(ws);
-    if (cc_attention_tc_supported(D)) return launch_cc_attention_tc(D, K, V, Q, O, err, st);
+    if (cc_attention_tc_supported(D))
+        return launch_cc_attention_tc(
+            D, K, V, Q, O, cc_logits_tc_supported(D) ? static_cast<__nv_bfloat16 *>(ws) : nullptr,
+            err, st);
     if (D.dtype == KVE_F32) return cc_attention_t<float>(D, K, V, Q, O, st);
     return cc_attention_t<__nv_bfloat16>(D, K, V, Q, O, st);
 }
@@ -337,6 +345,17 @@ cudaError_t launch_cc_logits(const CcDims &D, const void *H, const void *W_O, co
                              cudaStream_t st) {
     const float *O = static_cast<const float *>(ws);
     float *part = reinterpret_cast<float *>(static_cast<char *>(ws) + cc_o_bytes(D));
+    if (cc_logits_tc_supported(D)) {
+        const int ksplit = cc_logits_tc_split(D);
+        cudaError_t e = launch_cc_logits_tc(D, static_cast<const __nv_bfloat16 *>(ws), H, W_O,
+                                            W_U, X, part, ksplit, err, st);
+        if (e != cudaSuccess) return e;
+        const int ksteps = D.hq * D.d / 64, per = (ksteps + ksplit - 1) / ksplit;
+        const int parts = ((D.dm + 255) / 256) * ((ksteps + per - 1) / per) * 2;
+        cc_finish_kernel<<<dim3((D.n + 255) / 256, D.batch), 256, 0, st>>>(part, D.n, parts,
+                                                                          D.sink, surprise);
+        return cudaGetLastError();
+    }
     if (D.dtype == KVE_F32)
         return cc_logits_t<float>(D, O, H, W_O, W_U, X, part, surprise, err, st);
     return cc_logits_t<__nv_bfloat16>(D, O, H, W_O, W_U, X, part, surprise, err, st);

@@ -139,10 +139,19 @@ size_t cc_workspace_bytes(const CcDims &D);
 // attention outputs O [batch][n][hq*d] fp32 at the start of the workspace
 cudaError_t launch_cc_attention(const CcDims &D, const void *K, const void *V, const void *Q,
                                 void *ws, unsigned *err, cudaStream_t st);
-// tensor-core attention (cc_tc.cu): bf16, d_head 128, at least 128 K/V rows in all
+// tensor-core attention (cc_tc.cu): bf16, d_head 128, at least 128 K/V rows in all; writes O as
+// fp32 into O, or as bf16 into Ob when Ob is not null
 bool cc_attention_tc_supported(const CcDims &D);
 cudaError_t launch_cc_attention_tc(const CcDims &D, const void *K, const void *V, const void *Q,
-                                   float *O, unsigned *err, cudaStream_t st);
+                                   float *O, __nv_bfloat16 *Ob, unsigned *err, cudaStream_t st);
+// tensor-core projection + logit (cc_tc.cu): also needs d_model % 8 == 0; partial logits
+// [batch][ceil(d_model/256) * ksplit * 2][n], ksplit from cc_logits_tc_split (<= kCcMaxKSplit)
+constexpr int kCcMaxKSplit = 4;
+bool cc_logits_tc_supported(const CcDims &D);
+int cc_logits_tc_split(const CcDims &D);
+cudaError_t launch_cc_logits_tc(const CcDims &D, const __nv_bfloat16 *Ob, const void *H,
+                                const void *W_O, const void *W_U, const int32_t *X, float *part,
+                                int ksplit, unsigned *err, cudaStream_t st);
 // surprise from O, h, W_O, W_U[x] (partial logits after O in the workspace)
 cudaError_t launch_cc_logits(const CcDims &D, const void *H, const void *W_O, const void *W_U,
                              const int32_t *X, float *surprise, void *ws, unsigned *err,

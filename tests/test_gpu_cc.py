@@ -13,8 +13,9 @@ On the tensor-core path (bf16, d_head 128) the softmax numerators p_j are rounde
 the product with V, while their sum l stays fp32: o_h carries sum_j a_j eps_j v_j with a_j the
 attention weights and eps_j the relative rounding errors (independent, zero mean, standard
 deviation at most 2^-8 / sqrt 3). Through the logit weights c = W_O^T W_U[x_i] that gives a
-standard deviation sigma_P = 2^-8/sqrt(3) * sqrt(sum_h sum_j a_j^2 (c_h . v_j)^2), and the bound
-there adds 6 sigma_P.
+standard deviation sigma_P = 2^-8/sqrt(3) * sqrt(sum_h sum_j a_j^2 (c_h . v_j)^2). The projection
+W_O o then runs on the tensor cores from o rounded to bf16, which adds
+sigma_O = 2^-8/sqrt(3) * sqrt(sum_k c_k^2 o_k^2). The bound there adds 6 sqrt(sigma_P^2 + sigma_O^2).
 
 Selection: integer work, compared bit-exactly on the GPU's own surprise vector (the oracle selects
 from the same fp32 values); the gathers are byte-exact.
@@ -95,7 +96,11 @@ def _oracle_rows(inp, b, rows, hkv, bf16_p):
     z = cc.cc_logits(o, H, W_O, W_U, inv)
     r_abs = np.abs(H) + np.abs(o.reshape(len(rows), -1)) @ np.abs(W_O).T
     scale = np.einsum("nm,nm->n", np.abs(W_U[inv]), r_abs)
-    sig = _sigma_p(K, V, Q, rows, W_U[inv] @ W_O, hkv) if bf16_p else np.zeros(len(rows))
+    sig = np.zeros(len(rows))
+    if bf16_p:
+        c = W_U[inv] @ W_O
+        sig_o = BF16_REL_SD * np.sqrt(np.sum((c * o.reshape(len(rows), -1)) ** 2, axis=1))
+        sig = np.sqrt(_sigma_p(K, V, Q, rows, c, hkv) ** 2 + sig_o ** 2)
     return -z, scale, sig
 
 
