@@ -504,7 +504,7 @@ int cc_select_compact(const KveCcShape *shape, const float *surprise, const void
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     {
-        ProfScope ps("cc_select_compact", 1, st);
+        ProfScope ps("cc_select_compact", 2, st);
         e = launch_cc_select(D, surprise, K, V, tokens, kept_idx, K_out, V_out, tokens_out, st);
     }
     if (e != cudaSuccess) return cuda_fail(e, "cc_select_compact: launch");

@@ -15,7 +15,8 @@
 //                       slots and the last token.
 //   cc_select_kernel    keep the J highest surprises (equal: the lower position), ascending order:
 //                       MSB-first radix select over shared-memory histograms, an ordered scan,
-//                       then 16-byte gathers of the kept K and V rows and token ids.
+//                       kept positions and token ids (one CTA per sequence);
+//   cc_gather_kernel    16-byte copies of the kept K and V rows over the whole GPU.
 #include <algorithm>
 
 #include "kve_internal.cuh"
@@ -197,11 +198,10 @@ __device__ __forceinline__ int cc_scan(int v, int *warp_tot, int *total) {
     return before + x - v;
 }
 
-template <typename VecT>
-__global__ void __launch_bounds__(kSelT) cc_select_kernel(
-    const float *__restrict__ surprise, const VecT *__restrict__ K, const VecT *__restrict__ V,
-    const int32_t *__restrict__ X, int n, int J, int hkv, int vpr, int32_t *__restrict__ kept,
-    VecT *__restrict__ K_out, VecT *__restrict__ V_out, int32_t *__restrict__ X_out) {
+__global__ void __launch_bounds__(kSelT) cc_select_kernel(const float *__restrict__ surprise,
+                                                          const int32_t *__restrict__ X, int n,
+                                                          int J, int32_t *__restrict__ kept,
+                                                          int32_t *__restrict__ X_out) {
     __shared__ uint32_t hist[256];
     __shared__ int warp_tot[32];
     __shared__ uint32_t s_prefix;
@@ -279,15 +279,24 @@ __global__ void __launch_bounds__(kSelT) cc_select_kernel(
         run += tot;
     }
     __syncthreads();
-    // gather: K', V' per KV head, token ids
-    for (int e = threadIdx.x; e < hkv * J * vpr; e += kSelT) {
-        const int c = e % vpr, r = (e / vpr) % J, kh = e / (vpr * J);
-        const size_t src = (((size_t)b * hkv + kh) * n + kb[r]) * vpr + c;
-        const size_t dst = (((size_t)b * hkv + kh) * J + r) * vpr + c;
-        K_out[dst] = K[src];
-        V_out[dst] = V[src];
-    }
     for (int r = threadIdx.x; r < J; r += kSelT) X_out[(size_t)b * J + r] = X[(size_t)b * n + kb[r]];
+}
+
+// K', V' rows of every sequence and KV head: 16-byte words, grid-stride over all of them.
+__global__ void cc_gather_kernel(const uint4 *__restrict__ K, const uint4 *__restrict__ V,
+                                 const int32_t *__restrict__ kept, int n, int J, int hkv, int vpr,
+                                 long total, uint4 *__restrict__ K_out, uint4 *__restrict__ V_out) {
+    for (long e = (long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (long)gridDim.x * blockDim.x) {
+        const int c = (int)(e % vpr);
+        const long row = e / vpr;  // (b * hkv + kh) * J + r
+        const int r = (int)(row % J);
+        const long bh = row / J;
+        const int b = (int)(bh / hkv);
+        const size_t src = ((size_t)bh * n + kept[(size_t)b * J + r]) * vpr + c;
+        K_out[e] = K[src];
+        V_out[e] = V[src];
+    }
 }
 
 template <typename T>
@@ -366,9 +375,15 @@ cudaError_t launch_cc_select(const CcDims &D, const float *surprise, const void 
                              int32_t *X_out, cudaStream_t st) {
     const size_t row = (size_t)D.d * dtype_size(D.dtype);
     if (row % 16 != 0) return cudaErrorInvalidValue;
-    cc_select_kernel<uint4><<<D.batch, kSelT, 0, st>>>(
-        surprise, (const uint4 *)K, (const uint4 *)V, X, D.n, D.J, D.hkv, (int)(row / 16), kept,
-        (uint4 *)K_out, (uint4 *)V_out, X_out);
+    cc_select_kernel<<<D.batch, kSelT, 0, st>>>(surprise, X, D.n, D.J, kept, X_out);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int vpr = (int)(row / 16);
+    const long total = (long)D.batch * D.hkv * D.J * vpr;
+    const long blocks = std::min<long>((total + 255) / 256, 152L * 8);
+    cc_gather_kernel<<<(unsigned)blocks, 256, 0, st>>>((const uint4 *)K, (const uint4 *)V, kept,
+                                                      D.n, D.J, D.hkv, vpr, total,
+                                                      (uint4 *)K_out, (uint4 *)V_out);
     return cudaGetLastError();
 }
 
