@@ -43,6 +43,9 @@ WORKLOAD = "llama"        # the 128K-context configuration the metric is quoted 
 # (n = 16384, ncu --set full), scaled by the 8x token count of the 128K workload (every term of the
 # traffic is proportional to the tokens scored).
 NCU_TRAFFIC = {"scores": (8 * (2.207942e9 + 0.068139e9), "51c7588533720f67")}
+# cc_attn_tc_kernel on the n = 4096 counter-causal workload (ncu --set full, one launch):
+# 37.807 MB read + 0.280 MB written
+NCU_TRAFFIC_CC = {("cc_attention", "qwen7b_4096"): (37.806592e6 + 0.280064e6, "b05a084158277b0c")}
 
 
 def parse():
@@ -56,6 +59,10 @@ def parse():
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-fidelity", action="store_true")
     p.add_argument("--no-cc", action="store_true", help="skip the counter-causal refresh")
+    p.add_argument("--only-cc", action="store_true",
+                   help="run only the counter-causal refresh and print its JSON (profiling)")
+    p.add_argument("--cc-configs", default="qwen7b_512,qwen7b_4096",
+                   help="counter-causal workloads (comma-separated names)")
     p.add_argument("--workload", default=WORKLOAD)
     p.add_argument("--h2o-batch", type=int, default=64, help="H2O batch (64 = OPT-30B workload)")
     p.add_argument("--h2o-steps", type=int, default=512, help="H2O decode steps")
@@ -690,7 +697,7 @@ def bench_cc(dev, stream, pg, args, pk):
     from kv_cache_eviction_02_gb300 import api, synth
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     out = {}
-    for name in ("qwen7b_512", "qwen7b_4096"):
+    for name in args.cc_configs.split(","):
         cfg = synth.CC_CONFIGS[name]
         inp = synth.cc_inputs(cfg, dev)
         pb = api.CcProblem(cfg.batch, cfg.Hq, cfg.Hkv, cfg.d, cfg.d_model, cfg.n, cfg.vocab,
@@ -734,9 +741,14 @@ def bench_cc(dev, stream, pg, args, pk):
         att_ms = stages.get("cc_attention")
         ach = cc_attention_flops(cfg) / (att_ms / 1e3) / 1e12 if att_ms else None
         # bf16 with d_head 128 runs on the tensor cores: a kernel timed alone, the burst peak
+        traffic = None
+        key = ("cc_attention", name)
+        if key in NCU_TRAFFIC_CC and NCU_TRAFFIC_CC[key][1] == src_hash(
+                "kv_cache_eviction_02_gb300/csrc/cc_tc.cu"):
+            traffic = NCU_TRAFFIC_CC[key][0]
         att_roof = {"kernel": "cc_attention", "bound": "tensor", "achieved": ach,
                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": ach / pk["bf16_tflops"] if ach else None, "traffic": None,
+                    "frac": ach / pk["bf16_tflops"] if ach else None, "traffic": traffic,
                     "peak_source": f"bf16 dense burst, {pk['source']}",
                     "flops": cc_attention_flops(cfg), "ms_per_launch": att_ms}
         out[name] = {
@@ -758,8 +770,22 @@ def bench_cc(dev, stream, pg, args, pk):
     return out
 
 
+def run_cc_only(args):
+    import torch
+    rank, world, local, pg = dist_init(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    out = bench_cc(dev, torch.cuda.current_stream(dev), pg, args, peaks())
+    if rank == 0:
+        print(json.dumps({"cc_refresh": out}), flush=True)
+    barrier(pg)
+
+
 def main():
     args = parse()
+    if args.only_cc and args.impl != "reference":
+        run_cc_only(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
