@@ -10,6 +10,7 @@ Counter-causal page ("Back from the Future: KV Cache Management by Counter-Causa
   gets the maximum surprise (step 5);
 * Section 3.3: the fast variant runs only the last layer, from its stored input activations;
 * Algorithm 3 (memory refresh): keep the J highest-surprise entries of the J + h candidates;
+* Algorithm 1 (driver): a refresh after every h-th token, the recent chunk cleared after it;
 * Design choice 4: system-prompt sink slots are never scored or evicted.
 
 Readings (the page leaves them open): the fresh queries, the last layer's input residual stream
@@ -87,3 +88,35 @@ def cc_select(s, J: int) -> np.ndarray:
         return np.arange(n, dtype=np.int32)
     order = sorted(range(n), key=lambda i: (-s[i], i))
     return np.sort(np.asarray(order[:J], dtype=np.int32))
+
+
+def cc_refresh(K, V, Qf, Hres, W_O, W_U, X, cand, J: int, sink: int) -> np.ndarray:
+    """Algorithm 3 over the candidate positions `cand` (ascending: the memory, then the recent
+    chunk): score the candidates as one sequence (cc_surprise; the candidates with position < sink
+    are the system-prompt slots) and keep the J most surprising, ascending. All are kept when there
+    are J or fewer. K, V [H_kv][T][d], Qf [H_q][T][d], Hres [T][d_model], X [T] hold every token
+    seen so far, indexed by position."""
+    cand = np.asarray(cand, dtype=np.int64)
+    if len(cand) <= J:
+        return cand
+    K, V, Qf, Hres = _d(K), _d(V), _d(Qf), _d(Hres)
+    X = np.asarray(X, dtype=np.int64)
+    s = cc_surprise(K[:, cand], V[:, cand], Qf[:, cand], Hres[cand], W_O, W_U, X[cand],
+                    int(np.sum(cand < sink)))
+    return cand[cc_select(s, J)]
+
+
+def cc_cycle(K, V, Qf, Hres, W_O, W_U, X, J: int, h: int, sink: int, chunks) -> list:
+    """Algorithm 1 without the model: tokens 0, 1, ... arrive in appends of the given sizes (each
+    at most the free rows of the current chunk); after every h-th token the memory plus the chunk
+    is refreshed (cc_refresh) and the chunk is cleared. Returns the memory after each refresh."""
+    mem, recent, t, out = [], [], 0, []
+    for c in chunks:
+        assert 1 <= c <= h - len(recent)
+        recent.extend(range(t, t + c))
+        t += c
+        if len(recent) == h:
+            mem = list(cc_refresh(K, V, Qf, Hres, W_O, W_U, X, mem + recent, J, sink))
+            recent = []
+            out.append(np.asarray(mem))
+    return out

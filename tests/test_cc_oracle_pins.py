@@ -102,3 +102,52 @@ def test_row_evaluation_matches_the_whole_sequence():
     K, V, Q = _rand(rng, 2, 15, 8), _rand(rng, 2, 15, 8), _rand(rng, 6, 15, 8)
     rows = [14, 0, 7, 13, 3]
     assert np.array_equal(cc.cc_attention_rows(K, V, Q, rows), cc.cc_attention(K, V, Q)[rows])
+
+
+def _stream(rng, T, hkv=1, hq=2, d=8, dm=12, vocab=40, zero_v=False):
+    K, Q = _rand(rng, hkv, T, d), _rand(rng, hq, T, d)
+    V = np.zeros((hkv, T, d)) if zero_v else _rand(rng, hkv, T, d)
+    return (K, V, Q, _rand(rng, T, dm), _rand(rng, dm, hq * d), _rand(rng, vocab, dm),
+            rng.integers(0, vocab, size=T))
+
+
+@pytest.mark.parametrize("seed,J,h,sink,chunks", [
+    (0, 6, 3, 1, [1, 2] * 10 + [3] * 4),      # 42 tokens, refreshes after every 3rd
+    (1, 9, 4, 2, [4] * 12),
+    (2, 5, 1, 0, [1] * 30),
+    (3, 12, 6, 3, [2, 1, 3] * 10),
+])
+def test_cycle_with_context_free_surprise_keeps_the_global_best(seed, J, h, sink, chunks):
+    """V = 0 makes every attention output 0, so each token's surprise is the fixed
+    -W_U[x_i].h_i. A token evicted at some refresh was beaten by J - 1 - sink kept tokens, which
+    only ever make way for better ones, so the final memory is: the sinks, the final refresh's
+    last token, and the J - 1 - sink best of the other tokens (equal: the lower position)."""
+    rng = np.random.default_rng(40 + seed)
+    T = sum(chunks)
+    K, V, Q, H, W_O, W_U, X = _stream(rng, T, zero_v=True)
+    mems = cc.cc_cycle(K, V, Q, H, W_O, W_U, X, J, h, sink, chunks)
+    assert len(mems) == T // h
+    last = T - 1 - (T % h)                              # the last token of the final refresh
+    seen = last + 1
+    score = -np.einsum("tm,tm->t", W_U[X[:seen]], H[:seen])
+    others = [i for i in range(sink, seen) if i != last]
+    best = sorted(others, key=lambda i: (-score[i], i))[:J - 1 - sink]
+    assert mems[-1].tolist() == sorted(list(range(sink)) + [last] + best)
+
+
+def test_cycle_invariants_and_no_eviction_below_the_budget():
+    rng = np.random.default_rng(50)
+    J, h, sink = 7, 3, 2
+    chunks = [1, 2, 3, 1, 1, 1, 2, 1, 3, 3, 3]
+    K, V, Q, H, W_O, W_U, X = _stream(rng, sum(chunks))
+    mems = cc.cc_cycle(K, V, Q, H, W_O, W_U, X, J, h, sink, chunks)
+    t = 0
+    for k, m in enumerate(mems):
+        t = (k + 1) * h
+        assert len(m) == min(J, t)
+        assert np.all(np.diff(m) > 0)                   # ascending, distinct
+        assert set(range(sink)) <= set(m.tolist())      # system-prompt slots never evicted
+        assert t - 1 in m                               # the refresh's last token always kept
+    # a budget that holds everything evicts nothing
+    all_mems = cc.cc_cycle(K, V, Q, H, W_O, W_U, X, 100, h, sink, chunks)
+    assert all_mems[-1].tolist() == list(range(len(mems) * h))
