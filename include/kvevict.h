@@ -255,6 +255,54 @@ int cc_select_compact(const KveCcShape *shape, const float *surprise, const void
                       const void *V, const int32_t *tokens, int32_t *kept_idx, void *K_out,
                       void *V_out, int32_t *tokens_out, void *stream);
 
+/* Refresh-cycle cache (same review, Algorithms 1 and 3; Section 5, design choice 3: refresh every
+ * h tokens). Per sequence it holds the memory M = (K', V') of at most keep_J tokens followed by the
+ * recent chunk of up to h = n_tokens - keep_J tokens, with each token's fresh queries, stored
+ * last-layer input activation, id and original position (a token's fresh query depends only on
+ * its own activation and position, so it is stored with it). A refresh scores the mem + recent
+ * candidates with cc_surprise's arithmetic and keeps the keep_J most surprising (cc_select_compact's
+ * rule), in ascending position order; with keep_J or fewer candidates it keeps them all and
+ * launches nothing. The cache owns its device memory: two buffers of n_tokens rows per sequence
+ * and head (a refresh gathers into the other buffer and swaps) plus the scoring workspace.
+ * Requirements: those of cc_surprise, keep_J < n_tokens, keep_J >= sink + 1, d_model rows a
+ * multiple of 16 bytes. */
+typedef struct KveCcCache KveCcCache;
+
+/* Allocates a cache for shape (n_tokens = keep_J + h, the candidates of a full refresh).
+ * Synchronises the device once. *out receives the handle. */
+int cc_cache_create(KveCcCache **out, const KveCcShape *shape);
+
+/* Appends `count` tokens to the recent chunk (Algorithm 2, lines 3-5), 1 <= count <= h minus the
+ * tokens already in the chunk. Device pointers:
+ *   K_new, V_new [n_seq][n_kv_heads][count][d_head]; Q_new [n_seq][n_q_heads][count][d_head];
+ *   H_new [n_seq][count][d_model] (all shape->dtype); tokens_new [n_seq][count] int32.
+ * Their original positions are the number of tokens appended before them. */
+int cc_cache_append(KveCcCache *c, const void *K_new, const void *V_new, const void *Q_new,
+                    const void *H_new, const int32_t *tokens_new, int count, void *stream);
+
+/* Memory refresh (Algorithm 3) over the current candidates, then the chunk is empty. W_O
+ * [d_model][n_q_heads*d_head] and W_U [vocab][d_model] as in cc_surprise. Token ids outside
+ * [0, vocab) are reported by kve_check_device. */
+int cc_cache_refresh(KveCcCache *c, const void *W_O, const void *W_U, void *stream);
+
+/* One step of Algorithm 1's loop without the model: cc_cache_append, then cc_cache_refresh if the
+ * chunk now holds h tokens. *refreshed (host, may be NULL) tells whether the refresh ran. */
+int cc_cache_step(KveCcCache *c, const void *K_new, const void *V_new, const void *Q_new,
+                  const void *H_new, const int32_t *tokens_new, int count, const void *W_O,
+                  const void *W_U, int *refreshed, void *stream);
+
+/* Copies the held tokens out, memory then chunk (len = cc_cache_length rows, ascending original
+ * positions): K, V [n_seq][n_kv_heads][len][d_head]; Q [n_seq][n_q_heads][len][d_head];
+ * H [n_seq][len][d_model]; tokens, pos [n_seq][len] int32. Any pointer may be NULL. */
+int cc_cache_export(const KveCcCache *c, void *K, void *V, void *Q, void *H, int32_t *tokens,
+                    int32_t *pos, void *stream);
+
+/* Tokens held (memory + chunk) and tokens appended so far. */
+int cc_cache_length(const KveCcCache *c);
+int cc_cache_seen(const KveCcCache *c);
+
+void cc_cache_destroy(KveCcCache *c);
+
 /* ---- diagnostics ---------------------------------------------------------------------------- */
 
 /* Message of the last failing call on this thread ("" if none). Valid until the next call. */

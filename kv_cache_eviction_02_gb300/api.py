@@ -27,7 +27,9 @@ EXPORTED = ("lorekv_prepare_wo", "lorekv_workspace_size", "lorekv_score",
             "h2o_length", "h2o_state_destroy", "kve_last_error", "kve_check_device",
             "kve_inject_failure", "kve_profile_enable", "kve_profile_report", "kve_version",
             "kve_selftest_wait_timeout", "lorekv_score_noalloc",
-            "cc_workspace_size", "cc_surprise", "cc_select_compact")
+            "cc_workspace_size", "cc_surprise", "cc_select_compact", "cc_cache_create",
+            "cc_cache_append", "cc_cache_refresh", "cc_cache_step", "cc_cache_export",
+            "cc_cache_length", "cc_cache_seen", "cc_cache_destroy")
 
 
 class KveError(RuntimeError):
@@ -94,6 +96,15 @@ def lib():
         L.cc_workspace_size.restype = Z
         L.cc_surprise.argtypes = [CS, P, P, P, P, P, P, P, P, P, Z, P]
         L.cc_select_compact.argtypes = [CS, P, P, P, P, P, P, P, P, P]
+        L.cc_cache_create.argtypes = [ctypes.POINTER(P), CS]
+        L.cc_cache_append.argtypes = [P, P, P, P, P, P, I, P]
+        L.cc_cache_refresh.argtypes = [P, P, P, P]
+        L.cc_cache_step.argtypes = [P, P, P, P, P, P, I, P, P, ctypes.POINTER(I), P]
+        L.cc_cache_export.argtypes = [P, P, P, P, P, P, P, P]
+        L.cc_cache_length.argtypes = [P]
+        L.cc_cache_seen.argtypes = [P]
+        L.cc_cache_destroy.argtypes = [P]
+        L.cc_cache_destroy.restype = None
         _lib = L
     return _lib
 
@@ -269,6 +280,66 @@ def cc_select_compact(pb: CcProblem, surprise, K, V, tokens, kept_idx, K_out, V_
     _check(lib().cc_select_compact(ctypes.byref(sh), _ptr(surprise), _ptr(K), _ptr(V),
                                    _ptr(tokens), _ptr(kept_idx), _ptr(K_out), _ptr(V_out),
                                    _ptr(tokens_out), _stream(stream)))
+
+
+class CcCache:
+    """Owns a KveCcCache handle (cc_cache_create / cc_cache_destroy): the counter-causal refresh
+    cycle with memory keep_J and chunk h = n_tokens - keep_J."""
+
+    def __init__(self, pb: CcProblem):
+        h = ctypes.c_void_p()
+        sh = pb.shape()
+        _check(lib().cc_cache_create(ctypes.byref(h), ctypes.byref(sh)))
+        self.h = h
+        self.pb = pb
+
+    @property
+    def length(self) -> int:
+        return lib().cc_cache_length(self.h)
+
+    @property
+    def seen(self) -> int:
+        return lib().cc_cache_seen(self.h)
+
+    def append(self, K_new, V_new, Q_new, H_new, tokens_new, stream=None):
+        _check(lib().cc_cache_append(self.h, _ptr(K_new), _ptr(V_new), _ptr(Q_new), _ptr(H_new),
+                                     _ptr(tokens_new), int(K_new.shape[-2]), _stream(stream)))
+
+    def refresh(self, W_O, W_U, stream=None):
+        _check(lib().cc_cache_refresh(self.h, _ptr(W_O), _ptr(W_U), _stream(stream)))
+
+    def step(self, K_new, V_new, Q_new, H_new, tokens_new, W_O, W_U, stream=None) -> bool:
+        r = ctypes.c_int(0)
+        _check(lib().cc_cache_step(self.h, _ptr(K_new), _ptr(V_new), _ptr(Q_new), _ptr(H_new),
+                                   _ptr(tokens_new), int(K_new.shape[-2]), _ptr(W_O), _ptr(W_U),
+                                   ctypes.byref(r), _stream(stream)))
+        return bool(r.value)
+
+    def export(self, stream=None) -> dict:
+        pb, n, dev = self.pb, self.length, torch.device("cuda")
+        dt = {KVE_F32: torch.float32, KVE_BF16: torch.bfloat16}[pb.dtype]
+        out = {"K": torch.empty(pb.n_seq, pb.n_kv_heads, n, pb.d_head, dtype=dt, device=dev),
+               "Q": torch.empty(pb.n_seq, pb.n_q_heads, n, pb.d_head, dtype=dt, device=dev),
+               "H": torch.empty(pb.n_seq, n, pb.d_model, dtype=dt, device=dev),
+               "tokens": torch.empty(pb.n_seq, n, dtype=torch.int32, device=dev),
+               "pos": torch.empty(pb.n_seq, n, dtype=torch.int32, device=dev)}
+        out["V"] = torch.empty_like(out["K"])
+        if n > 0:
+            _check(lib().cc_cache_export(self.h, _ptr(out["K"]), _ptr(out["V"]), _ptr(out["Q"]),
+                                         _ptr(out["H"]), _ptr(out["tokens"]), _ptr(out["pos"]),
+                                         _stream(stream)))
+        return out
+
+    def close(self):
+        if self.h:
+            lib().cc_cache_destroy(self.h)
+            self.h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def kve_check_device(stream=None):

@@ -227,6 +227,24 @@ struct KveH2O {
     H2OState s;
 };
 
+// Refresh-cycle cache of the counter-causal method: two buffers of J + h rows per sequence (and
+// head) for K, V, fresh queries, stored activations, token ids and original positions. Rows
+// [0, mem) hold the memory M, rows [mem, mem + recent) the recent chunk; a refresh gathers the
+// kept rows into the other buffer and swaps, so no row is overwritten while it is still read.
+struct KveCcCache {
+    CcDims D;  // n = J + h, ld = J + h
+    int h;     // chunk size
+    int mem = 0, recent = 0, seen = 0, cur = 0;
+    struct Buf {
+        void *K = nullptr, *V = nullptr, *Q = nullptr, *H = nullptr;
+        int32_t *X = nullptr, *pos = nullptr;
+    } buf[2];
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+    float *surprise = nullptr;
+    int32_t *kept = nullptr;
+};
+
 extern "C" {
 
 const char *kve_last_error(void) { return g_err.c_str(); }
@@ -456,7 +474,7 @@ static int cc_dims(const char *fn, const KveCcShape *sh, CcDims *D) {
     if (sh->n_seq > 65535 || sh->n_q_heads > 65535 || sh->d_model > (1 << 22))
         return fail(KVE_EINVAL, "%s: n_seq, n_q_heads or d_model too large", fn);
     *D = CcDims{sh->n_seq, sh->n_q_heads, sh->n_kv_heads, sh->d_head, sh->d_model, sh->n_tokens,
-                sh->vocab, sh->dtype, sh->sink, sh->keep_J};
+                sh->vocab, sh->dtype, sh->sink, sh->keep_J, sh->n_tokens};
     return KVE_OK;
 }
 
@@ -575,6 +593,205 @@ int lorekv_select_compact(const KveShape *shape, const KveLorekvParams *params,
     }
     if (e != cudaSuccess) return cuda_fail(e, "lorekv_select_compact: launch");
     return KVE_OK;
+}
+
+// ---- counter-causal refresh cycle ------------------------------------------------------------------
+static size_t cc_row_bytes(const CcDims &D, int which) {  // 0 K/V, 1 Q, 2 H
+    const size_t es = dtype_size(D.dtype);
+    return which == 2 ? (size_t)D.dm * es : (size_t)D.d * es;
+}
+
+int cc_cache_create(KveCcCache **out, const KveCcShape *shape) {
+    if (int s = injected()) return s;
+    if (!out) return fail(KVE_EINVAL, "cc_cache_create: null out");
+    *out = nullptr;
+    CcDims D;
+    if (int s = cc_dims("cc_cache_create", shape, &D)) return s;
+    if (D.J >= D.n) return fail(KVE_EINVAL, "cc_cache_create: n_tokens must exceed keep_J (h = n_tokens - keep_J >= 1)");
+    if (D.J < D.sink + 1) return fail(KVE_EINVAL, "cc_cache_create: keep_J must be at least sink + 1");
+    if ((D.dm * dtype_size(D.dtype)) % 16 != 0)
+        return fail(KVE_EINVAL, "cc_cache_create: d_model rows must be a multiple of 16 bytes");
+    KveCcCache *c = new KveCcCache();
+    c->D = D;
+    c->h = D.n - D.J;
+    const size_t rows = (size_t)D.batch * D.n;
+    cudaError_t e = cudaSuccess;
+    for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
+        KveCcCache::Buf &b = c->buf[k];
+        const size_t kv = rows * D.hkv * cc_row_bytes(D, 0), q = rows * D.hq * cc_row_bytes(D, 1),
+                     hb = rows * cc_row_bytes(D, 2);
+        // zero-filled: rows past the scored ones are read (and multiplied by 0) by the tensor-core
+        // attention, so they must hold finite values
+        if (e == cudaSuccess) e = cudaMalloc(&b.K, kv);
+        if (e == cudaSuccess) e = cudaMemset(b.K, 0, kv);
+        if (e == cudaSuccess) e = cudaMalloc(&b.V, kv);
+        if (e == cudaSuccess) e = cudaMemset(b.V, 0, kv);
+        if (e == cudaSuccess) e = cudaMalloc(&b.Q, q);
+        if (e == cudaSuccess) e = cudaMemset(b.Q, 0, q);
+        if (e == cudaSuccess) e = cudaMalloc(&b.H, hb);
+        if (e == cudaSuccess) e = cudaMemset(b.H, 0, hb);
+        if (e == cudaSuccess) e = cudaMalloc(&b.X, rows * sizeof(int32_t));
+        if (e == cudaSuccess) e = cudaMemset(b.X, 0, rows * sizeof(int32_t));
+        if (e == cudaSuccess) e = cudaMalloc(&b.pos, rows * sizeof(int32_t));
+        if (e == cudaSuccess) e = cudaMemset(b.pos, 0xff, rows * sizeof(int32_t));
+    }
+    c->ws_bytes = cc_workspace_bytes(D);
+    if (e == cudaSuccess) e = cudaMalloc(&c->ws, c->ws_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&c->surprise, rows * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&c->kept, (size_t)D.batch * D.J * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        cc_cache_destroy(c);
+        return cuda_fail(e, "cc_cache_create: allocate");
+    }
+    *out = c;
+    return KVE_OK;
+}
+
+int cc_cache_append(KveCcCache *c, const void *K_new, const void *V_new, const void *Q_new,
+                    const void *H_new, const int32_t *tokens_new, int count, void *stream) {
+    if (int s = injected()) return s;
+    if (!c || !K_new || !V_new || !Q_new || !H_new || !tokens_new)
+        return fail(KVE_EINVAL, "cc_cache_append: null argument");
+    if (count < 1 || count > c->h - c->recent)
+        return fail(KVE_EINVAL, "cc_cache_append: count must be in [1, %d] (free rows of the chunk)",
+                    c->h - c->recent);
+    const CcDims &D = c->D;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    KveCcCache::Buf &b = c->buf[c->cur];
+    const int at = c->mem + c->recent;
+    cudaError_t e;
+    {
+        ProfScope ps("cc_append", 6, st);
+        const size_t rk = cc_row_bytes(D, 0), rq = cc_row_bytes(D, 1), rh = cc_row_bytes(D, 2);
+        const size_t ld = (size_t)D.ld;
+        e = cudaMemcpy2DAsync(static_cast<char *>(b.K) + at * rk, ld * rk, K_new, count * rk,
+                              count * rk, (size_t)D.batch * D.hkv, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(static_cast<char *>(b.V) + at * rk, ld * rk, V_new, count * rk,
+                                  count * rk, (size_t)D.batch * D.hkv, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(static_cast<char *>(b.Q) + at * rq, ld * rq, Q_new, count * rq,
+                                  count * rq, (size_t)D.batch * D.hq, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(static_cast<char *>(b.H) + at * rh, ld * rh, H_new, count * rh,
+                                  count * rh, (size_t)D.batch, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(b.X + at, ld * sizeof(int32_t), tokens_new,
+                                  count * sizeof(int32_t), count * sizeof(int32_t), D.batch,
+                                  cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess) e = launch_cc_fill_pos(b.pos + at, D.ld, D.batch, count, c->seen, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "cc_cache_append: copy");
+    c->recent += count;
+    c->seen += count;
+    return KVE_OK;
+}
+
+int cc_cache_refresh(KveCcCache *c, const void *W_O, const void *W_U, void *stream) {
+    if (int s = injected()) return s;
+    if (!c || !W_O || !W_U) return fail(KVE_EINVAL, "cc_cache_refresh: null argument");
+    const int cand = c->mem + c->recent;
+    if (cand <= c->D.J) {  // nothing to evict: every candidate is kept, in place and in order
+        c->mem = cand;
+        c->recent = 0;
+        return KVE_OK;
+    }
+    unsigned *err = device_error_word();
+    if (!err) return fail(KVE_ECUDA, "cc_cache_refresh: no device error word");
+    CcDims D = c->D;
+    D.n = cand;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const KveCcCache::Buf &a = c->buf[c->cur];
+    KveCcCache::Buf &b = c->buf[c->cur ^ 1];
+    cudaError_t e;
+    {
+        ProfScope ps("cc_attention", 1, st);
+        e = launch_cc_attention(D, a.K, a.V, a.Q, c->ws, err, st);
+    }
+    if (e == cudaSuccess) {
+        ProfScope ps("cc_logits", 2, st);
+        e = launch_cc_logits(D, a.H, W_O, W_U, a.X, c->surprise, c->ws, err, st);
+    }
+    if (e == cudaSuccess) {
+        ProfScope ps("cc_select_compact", 2, st);
+        e = launch_cc_select_idx(D, c->surprise, a.X, a.pos, c->kept, b.X, b.pos, D.ld, st);
+        if (e == cudaSuccess) {
+            CcGatherSet G{};
+            cc_gather_add(&G, a.K, b.K, D.batch, D.hkv, cc_row_bytes(D, 0), D.J);
+            cc_gather_add(&G, a.V, b.V, D.batch, D.hkv, cc_row_bytes(D, 0), D.J);
+            cc_gather_add(&G, a.Q, b.Q, D.batch, D.hq, cc_row_bytes(D, 1), D.J);
+            cc_gather_add(&G, a.H, b.H, D.batch, 1, cc_row_bytes(D, 2), D.J);
+            e = launch_cc_gather(G, c->kept, D.J, D.ld, D.ld, st);
+        }
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "cc_cache_refresh: launch");
+    c->cur ^= 1;
+    c->mem = D.J;
+    c->recent = 0;
+    return KVE_OK;
+}
+
+int cc_cache_step(KveCcCache *c, const void *K_new, const void *V_new, const void *Q_new,
+                  const void *H_new, const int32_t *tokens_new, int count, const void *W_O,
+                  const void *W_U, int *refreshed, void *stream) {
+    if (refreshed) *refreshed = 0;
+    if (!c || !W_O || !W_U) return fail(KVE_EINVAL, "cc_cache_step: null argument");
+    if (int s = cc_cache_append(c, K_new, V_new, Q_new, H_new, tokens_new, count, stream))
+        return s;
+    if (c->recent < c->h) return KVE_OK;
+    if (int s = cc_cache_refresh(c, W_O, W_U, stream)) return s;
+    if (refreshed) *refreshed = 1;
+    return KVE_OK;
+}
+
+int cc_cache_export(const KveCcCache *c, void *K, void *V, void *Q, void *H, int32_t *tokens,
+                    int32_t *pos, void *stream) {
+    if (int s = injected()) return s;
+    if (!c) return fail(KVE_EINVAL, "cc_cache_export: null cache");
+    const CcDims &D = c->D;
+    const int len = c->mem + c->recent;
+    if (len == 0) return KVE_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const KveCcCache::Buf &b = c->buf[c->cur];
+    const size_t ld = (size_t)D.ld;
+    struct Part {
+        void *dst;
+        const void *src;
+        size_t row;
+        size_t blocks;
+    } parts[6] = {{K, b.K, cc_row_bytes(D, 0), (size_t)D.batch * D.hkv},
+                  {V, b.V, cc_row_bytes(D, 0), (size_t)D.batch * D.hkv},
+                  {Q, b.Q, cc_row_bytes(D, 1), (size_t)D.batch * D.hq},
+                  {H, b.H, cc_row_bytes(D, 2), (size_t)D.batch},
+                  {tokens, b.X, sizeof(int32_t), (size_t)D.batch},
+                  {pos, b.pos, sizeof(int32_t), (size_t)D.batch}};
+    for (const Part &p : parts) {
+        if (!p.dst) continue;
+        cudaError_t e = cudaMemcpy2DAsync(p.dst, len * p.row, p.src, ld * p.row, len * p.row,
+                                          p.blocks, cudaMemcpyDeviceToDevice, st);
+        if (e != cudaSuccess) return cuda_fail(e, "cc_cache_export: copy");
+    }
+    return KVE_OK;
+}
+
+int cc_cache_length(const KveCcCache *c) { return c ? c->mem + c->recent : -KVE_EINVAL; }
+int cc_cache_seen(const KveCcCache *c) { return c ? c->seen : -KVE_EINVAL; }
+
+void cc_cache_destroy(KveCcCache *c) {
+    if (!c) return;
+    for (auto &b : c->buf) {
+        cudaFree(b.K);
+        cudaFree(b.V);
+        cudaFree(b.Q);
+        cudaFree(b.H);
+        cudaFree(b.X);
+        cudaFree(b.pos);
+    }
+    cudaFree(c->ws);
+    cudaFree(c->surprise);
+    cudaFree(c->kept);
+    delete c;
 }
 
 // ---- H2O -------------------------------------------------------------------------------------------

@@ -34,7 +34,7 @@ constexpr float kCaRescaleLog2 = 8.f;  // rescale O only when a row maximum grow
 constexpr float kCaNoMax = -1e30f;     // running maximum before any visible token
 
 struct CcAttnArgs {
-    int n, hq, hkv, g, nblk, units;  // units = batch * hkv
+    int n, ld, hq, hkv, g, nblk, units;  // units = batch * hkv; ld = token row stride
     float k1;                        // log2(e) / sqrt(d)
     float *O;                        // [batch][n][hq * 128] fp32, or
     __nv_bfloat16 *Ob;               // the same in bf16 (the tensor-core projection's operand)
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
             tc::mbar_expect_tx(q_full, 65536);
             for (int t = 0; t < 2; ++t) {
                 const CaTile qt = ca_tile(pair, t, A.g, A.nblk);
-                const int qrow = (b * A.hq + kh * A.g + qt.hh) * A.n + qt.blk * 128;
+                const int qrow = (b * A.hq + kh * A.g + qt.hh) * A.ld + qt.blk * 128;
                 tc::tma_load_2d(sm + CA_Q + t * 32768, &tm_q, 0, qrow, q_full);
                 tc::tma_load_2d(sm + CA_Q + t * 32768 + 16384, &tm_q, 64, qrow, q_full);
             }
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
                 const uint32_t ph = (c / CA_SLOTS) & 1;
                 if (!tc::mbar_wait(&rempty[slot], ph ^ 1, abort_flag, A.err)) break;
                 tc::mbar_expect_tx(&rfull[slot], 32768);
-                const int row = unit * A.n + (kstart + (c >> 1)) * 128;
+                const int row = unit * A.ld + (kstart + (c >> 1)) * 128;
                 const CUtensorMap *map = (c & 1) ? &tm_v : &tm_k;
                 uint8_t *dst = sm + CA_RING + slot * 32768;
                 tc::tma_load_2d(dst, map, 0, row, &rfull[slot]);
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
                        ok && tc::mbar_wait(&o_done[t], (ntl - 1) & 1, abort_flag, A.err))) {
             tc::fence_after_sync();
             const float inv = l > 0.f ? 1.f / l : 0.f;  // the last token sees no key: o = 0
-            const size_t off = ((size_t)(b * A.n + i) * A.hq + kh * A.g + qt.hh) * 128;
+            const size_t off = ((size_t)(b * A.ld + i) * A.hq + kh * A.g + qt.hh) * 128;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 float o[32];
@@ -337,7 +337,7 @@ constexpr uint32_t LG_BAR = LG_STAGES * LG_STAGE;
 constexpr size_t LG_SMEM = LG_BAR + 256 + 1024;
 
 struct CcLogitsArgs {
-    int n, dm, vocab, mtiles, ntiles, ksplit, ksteps, ksteps_per;
+    int n, ld, dm, vocab, mtiles, ntiles, ksplit, ksteps, ksteps_per;
     const __nv_bfloat16 *H, *W_U;
     const int32_t *X;
     float *part;  // [batch][ntiles * ksplit * 2][n]
@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(kLgThreads, 1)
                 tc::mbar_expect_tx(&full[slot], LG_STAGE);
                 uint8_t *dst = sm + slot * LG_STAGE;
                 const int x = (kb + s) * 64;
-                tc::tma_load_2d(dst, &tm_o, x, b * A.n + m0, &full[slot]);
+                tc::tma_load_2d(dst, &tm_o, x, b * A.ld + m0, &full[slot]);
                 tc::tma_load_2d(dst + LG_A, &tm_w, x, n0, &full[slot]);
                 issued = s + 1;
             }
@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(kLgThreads, 1)
         const bool valid = t < A.n;
         int x = 0;
         if (valid) {
-            x = A.X[(size_t)b * A.n + t];
+            x = A.X[(size_t)b * A.ld + t];
             if (x < 0 || x >= A.vocab) {  // reported, and the row read as token 0
                 if (A.err) atomicOr(A.err, KVE_DEVERR_BADINDEX);
                 x = 0;
@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(kLgThreads, 1)
             tc::fence_after_sync();
             const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
             const __nv_bfloat16 *wu = A.W_U + (size_t)x * A.dm;
-            const __nv_bfloat16 *hr = A.H + ((size_t)b * A.n + (valid ? t : 0)) * A.dm;
+            const __nv_bfloat16 *hr = A.H + ((size_t)b * A.ld + (valid ? t : 0)) * A.dm;
             float z = 0.f;
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
@@ -472,7 +472,7 @@ __global__ void __launch_bounds__(kLgThreads, 1)
             }
             if (valid)
                 A.part[((size_t)b * (A.ntiles * A.ksplit * 2) + (nt * A.ksplit + ks) * 2 + half) *
-                           A.n + t] = z;
+                           A.ld + t] = z;
         }
     }
     __syncthreads();
@@ -510,11 +510,12 @@ cudaError_t launch_cc_logits_tc(const CcDims &D, const __nv_bfloat16 *Ob, const 
                                 int ksplit, unsigned *err, cudaStream_t st) {
     const int kdim = D.hq * D.d;
     CUtensorMap to, tw;
-    if (!make_tmap_bf16_2d(&to, Ob, kdim, (uint64_t)D.batch * D.n, 64, 128) ||
+    if (!make_tmap_bf16_2d(&to, Ob, kdim, (uint64_t)D.batch * D.ld, 64, 128) ||
         !make_tmap_bf16_2d(&tw, W_O, kdim, D.dm, 64, 256))
         return cudaErrorInvalidValue;
     CcLogitsArgs A;
     A.n = D.n;
+    A.ld = D.ld;
     A.dm = D.dm;
     A.vocab = D.vocab;
     A.mtiles = (D.n + 127) / 128;
@@ -537,20 +538,21 @@ cudaError_t launch_cc_logits_tc(const CcDims &D, const __nv_bfloat16 *Ob, const 
 }
 
 bool cc_attention_tc_supported(const CcDims &D) {
-    return D.dtype == KVE_BF16 && D.d == 128 && (long)D.batch * D.hkv * D.n >= 128;
+    return D.dtype == KVE_BF16 && D.d == 128 && (long)D.batch * D.hkv * D.ld >= 128;
 }
 
 cudaError_t launch_cc_attention_tc(const CcDims &D, const void *K, const void *V, const void *Q,
                                    float *O, __nv_bfloat16 *Ob, unsigned *err, cudaStream_t st) {
     CUtensorMap tk, tv, tq;
-    const uint64_t kv_rows = (uint64_t)D.batch * D.hkv * D.n;
-    const uint64_t q_rows = (uint64_t)D.batch * D.hq * D.n;
+    const uint64_t kv_rows = (uint64_t)D.batch * D.hkv * D.ld;
+    const uint64_t q_rows = (uint64_t)D.batch * D.hq * D.ld;
     if (!make_tmap_bf16_2d(&tk, K, 128, kv_rows, 64, 128) ||
         !make_tmap_bf16_2d(&tv, V, 128, kv_rows, 64, 128) ||
         !make_tmap_bf16_2d(&tq, Q, 128, q_rows, 64, 128))
         return cudaErrorInvalidValue;
     CcAttnArgs A;
     A.n = D.n;
+    A.ld = D.ld;
     A.hq = D.hq;
     A.hkv = D.hkv;
     A.g = D.hq / D.hkv;

@@ -30,8 +30,8 @@ constexpr int kCcKeys = 32;          // keys per staged tile
 
 template <typename T>
 __global__ void __launch_bounds__(kCcQueriesPerCta * 32) cc_attn_kernel(
-    const T *__restrict__ K, const T *__restrict__ V, const T *__restrict__ Q, int n, int hq,
-    int hkv, int d, float scale, float *__restrict__ O) {
+    const T *__restrict__ K, const T *__restrict__ V, const T *__restrict__ Q, int n, int ld,
+    int hq, int hkv, int d, float scale, float *__restrict__ O) {
     __shared__ float ks[kCcKeys][129];  // padded: lane l reads row l column c conflict-free
     __shared__ float vs[kCcKeys][128];
     __shared__ float qs[kCcQueriesPerCta][128];
@@ -40,9 +40,9 @@ __global__ void __launch_bounds__(kCcQueriesPerCta * 32) cc_attn_kernel(
     const int i0 = blockIdx.x * kCcQueriesPerCta;
     const int i = i0 + warp;
     const int kh = h / (hq / hkv);
-    const T *Kb = K + ((size_t)b * hkv + kh) * n * d;
-    const T *Vb = V + ((size_t)b * hkv + kh) * n * d;
-    const T *Qb = Q + ((size_t)b * hq + h) * n * d;
+    const T *Kb = K + ((size_t)b * hkv + kh) * ld * d;
+    const T *Vb = V + ((size_t)b * hkv + kh) * ld * d;
+    const T *Qb = Q + ((size_t)b * hq + h) * ld * d;
     for (int e = threadIdx.x; e < kCcQueriesPerCta * d; e += blockDim.x) {
         const int r = e / d, c = e % d;
         qs[r][c] = (i0 + r < n) ? to_f(Qb[(size_t)(i0 + r) * d + c]) * scale : 0.f;
@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kCcQueriesPerCta * 32) cc_attn_kernel(
     }
     if (i < n) {
         const float inv = l > 0.f ? 1.f / l : 0.f;  // the last token sees no key: o = 0
-        float *dst = O + ((size_t)b * n + i) * hq * d + (size_t)h * d + lane;
+        float *dst = O + ((size_t)b * ld + i) * hq * d + (size_t)h * d + lane;
 #pragma unroll
         for (int e = 0; e < 4; ++e)
             if (e < per) dst[32 * e] = o[e] * inv;
@@ -96,8 +96,8 @@ constexpr int kPT = 64, kPM = 64, kPK = 32;
 template <typename T>
 __global__ void __launch_bounds__(256) cc_proj_kernel(
     const float *__restrict__ O, const T *__restrict__ Hres, const T *__restrict__ W_O,
-    const T *__restrict__ W_U, const int32_t *__restrict__ X, int n, int kdim, int dm, int vocab,
-    float *__restrict__ part, unsigned *err) {
+    const T *__restrict__ W_U, const int32_t *__restrict__ X, int n, int ld, int kdim, int dm,
+    int vocab, float *__restrict__ part, unsigned *err) {
     __shared__ float as[kPT][kPK + 1];
     __shared__ float bs[kPM][kPK + 1];
     const int b = blockIdx.z;
@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(256) cc_proj_kernel(
     for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
-    const float *Ob = O + (size_t)b * n * kdim;
+    const float *Ob = O + (size_t)b * ld * kdim;
     for (int k0 = 0; k0 < kdim; k0 += kPK) {
         __syncthreads();
         for (int e = threadIdx.x; e < kPT * kPK; e += 256) {
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(256) cc_proj_kernel(
         const int t = t0 + ty * 4 + a;
         float z = 0.f;
         if (t < n) {
-            int x = X[(size_t)b * n + t];
+            int x = X[(size_t)b * ld + t];
             if (x < 0 || x >= vocab) {  // reported, and the row treated as token 0
                 if (err) atomicOr(err, KVE_DEVERR_BADINDEX);
                 x = 0;
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(256) cc_proj_kernel(
             for (int q = 0; q < 4; ++q) {
                 const int mm = m0 + tx * 4 + q;
                 if (mm < dm) {
-                    const float r = acc[a][q] + to_f(Hres[((size_t)b * n + t) * dm + mm]);
+                    const float r = acc[a][q] + to_f(Hres[((size_t)b * ld + t) * dm + mm]);
                     z = fmaf(to_f(W_U[(size_t)x * dm + mm]), r, z);
                 }
             }
@@ -155,18 +155,18 @@ __global__ void __launch_bounds__(256) cc_proj_kernel(
         // sum over the 16 threads (tx) that share these tokens: lanes 0-15 / 16-31 of a warp
 #pragma unroll
         for (int off = 8; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-        if (tx == 0 && t < n) part[((size_t)b * gridDim.y + blockIdx.y) * n + t] = z;
+        if (tx == 0 && t < n) part[((size_t)b * gridDim.y + blockIdx.y) * ld + t] = z;
     }
 }
 
-__global__ void cc_finish_kernel(const float *__restrict__ part, int n, int parts, int sink,
-                                 float *__restrict__ surprise) {
+__global__ void cc_finish_kernel(const float *__restrict__ part, int n, int ld, int parts,
+                                 int sink, float *__restrict__ surprise) {
     const int b = blockIdx.y;
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= n) return;
     float z = 0.f;
-    for (int k = 0; k < parts; ++k) z += part[((size_t)b * parts + k) * n + t];
-    surprise[(size_t)b * n + t] = (t < sink || t == n - 1) ? INFINITY : -z;
+    for (int k = 0; k < parts; ++k) z += part[((size_t)b * parts + k) * ld + t];
+    surprise[(size_t)b * ld + t] = (t < sink || t == n - 1) ? INFINITY : -z;
 }
 
 __device__ __forceinline__ uint32_t cc_key(float f) {  // order-preserving (+inf largest)
@@ -198,16 +198,18 @@ __device__ __forceinline__ int cc_scan(int v, int *warp_tot, int *total) {
     return before + x - v;
 }
 
-__global__ void __launch_bounds__(kSelT) cc_select_kernel(const float *__restrict__ surprise,
-                                                          const int32_t *__restrict__ X, int n,
-                                                          int J, int32_t *__restrict__ kept,
-                                                          int32_t *__restrict__ X_out) {
+// surprise, X, pos: [batch][ld] (first n used); kept [batch][J]; X_out, pos_out: [batch][ldo].
+// pos and pos_out may be null.
+__global__ void __launch_bounds__(kSelT) cc_select_kernel(
+    const float *__restrict__ surprise, const int32_t *__restrict__ X,
+    const int32_t *__restrict__ pos, int n, int ld, int J, int32_t *__restrict__ kept,
+    int32_t *__restrict__ X_out, int32_t *__restrict__ pos_out, int ldo) {
     __shared__ uint32_t hist[256];
     __shared__ int warp_tot[32];
     __shared__ uint32_t s_prefix;
     __shared__ int s_krem;
     const int b = blockIdx.x;
-    const float *S = surprise + (size_t)b * n;
+    const float *S = surprise + (size_t)b * ld;
     int32_t *kb = kept + (size_t)b * J;
     if (threadIdx.x == 0) {
         s_prefix = 0u;
@@ -279,23 +281,30 @@ __global__ void __launch_bounds__(kSelT) cc_select_kernel(const float *__restric
         run += tot;
     }
     __syncthreads();
-    for (int r = threadIdx.x; r < J; r += kSelT) X_out[(size_t)b * J + r] = X[(size_t)b * n + kb[r]];
+    for (int r = threadIdx.x; r < J; r += kSelT) {
+        X_out[(size_t)b * ldo + r] = X[(size_t)b * ld + kb[r]];
+        if (pos_out) pos_out[(size_t)b * ldo + r] = pos[(size_t)b * ld + kb[r]];
+    }
 }
 
-// K', V' rows of every sequence and KV head: 16-byte words, grid-stride over all of them.
-__global__ void cc_gather_kernel(const uint4 *__restrict__ K, const uint4 *__restrict__ V,
-                                 const int32_t *__restrict__ kept, int n, int J, int hkv, int vpr,
-                                 long total, uint4 *__restrict__ K_out, uint4 *__restrict__ V_out) {
-    for (long e = (long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+// Kept rows of up to four row-major tensors [batch][heads][ld][row] (16-byte words): dst row
+// (b, h, r) = src row (b, h, kept[b][r]); one grid-stride loop over all words of all tensors.
+__global__ void cc_gather_kernel(CcGatherSet G, const int32_t *__restrict__ kept, int J,
+                                 int ld_in, int ld_out) {
+    for (long e = (long)blockIdx.x * blockDim.x + threadIdx.x; e < G.start[G.count];
          e += (long)gridDim.x * blockDim.x) {
-        const int c = (int)(e % vpr);
-        const long row = e / vpr;  // (b * hkv + kh) * J + r
+        int k = 0;
+        while (k + 1 < G.count && e >= G.start[k + 1]) ++k;
+        const long local = e - G.start[k];
+        const int vpr = G.vpr[k];
+        const int c = (int)(local % vpr);
+        const long row = local / vpr;  // (b * heads + h) * J + r
         const int r = (int)(row % J);
         const long bh = row / J;
-        const int b = (int)(bh / hkv);
-        const size_t src = ((size_t)bh * n + kept[(size_t)b * J + r]) * vpr + c;
-        K_out[e] = K[src];
-        V_out[e] = V[src];
+        const long b = bh / G.heads[k];
+        const size_t src = ((size_t)bh * ld_in + kept[(size_t)b * J + r]) * vpr + c;
+        const size_t dst = ((size_t)bh * ld_out + r) * vpr + c;
+        G.dst[k][dst] = G.src[k][src];
     }
 }
 
@@ -304,7 +313,7 @@ cudaError_t cc_attention_t(const CcDims &D, const void *K, const void *V, const 
                            cudaStream_t st) {
     cc_attn_kernel<T><<<dim3((D.n + kCcQueriesPerCta - 1) / kCcQueriesPerCta, D.hq, D.batch),
                         kCcQueriesPerCta * 32, 0, st>>>(
-        (const T *)K, (const T *)V, (const T *)Q, D.n, D.hq, D.hkv, D.d,
+        (const T *)K, (const T *)V, (const T *)Q, D.n, D.ld, D.hq, D.hkv, D.d,
         1.f / sqrtf((float)D.d), O);
     return cudaGetLastError();
 }
@@ -315,19 +324,19 @@ cudaError_t cc_logits_t(const CcDims &D, const float *O, const void *H, const vo
                         unsigned *err, cudaStream_t st) {
     const int mtiles = (D.dm + kPM - 1) / kPM;
     cc_proj_kernel<T><<<dim3((D.n + kPT - 1) / kPT, mtiles, D.batch), 256, 0, st>>>(
-        O, (const T *)H, (const T *)W_O, (const T *)W_U, X, D.n, D.hq * D.d, D.dm, D.vocab, part,
-        err);
+        O, (const T *)H, (const T *)W_O, (const T *)W_U, X, D.n, D.ld, D.hq * D.d, D.dm, D.vocab,
+        part, err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    cc_finish_kernel<<<dim3((D.n + 255) / 256, D.batch), 256, 0, st>>>(part, D.n, mtiles, D.sink,
-                                                                      surprise);
+    cc_finish_kernel<<<dim3((D.n + 255) / 256, D.batch), 256, 0, st>>>(part, D.n, D.ld, mtiles,
+                                                                      D.sink, surprise);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t cc_o_bytes(const CcDims &D) {
-    return ((size_t)D.batch * D.n * D.hq * D.d * sizeof(float) + 255) & ~size_t(255);
+    return ((size_t)D.batch * D.ld * D.hq * D.d * sizeof(float) + 255) & ~size_t(255);
 }
 
 size_t cc_workspace_bytes(const CcDims &D) {
@@ -335,7 +344,7 @@ size_t cc_workspace_bytes(const CcDims &D) {
     // tiles x K splits x 2 column halves (tensor cores)
     const size_t parts = std::max<size_t>((D.dm + kPM - 1) / kPM,
                                           (size_t)((D.dm + 255) / 256) * kCcMaxKSplit * 2);
-    return cc_o_bytes(D) + (((size_t)D.batch * parts * D.n * sizeof(float) + 255) & ~size_t(255));
+    return cc_o_bytes(D) + (((size_t)D.batch * parts * D.ld * sizeof(float) + 255) & ~size_t(255));
 }
 
 cudaError_t launch_cc_attention(const CcDims &D, const void *K, const void *V, const void *Q,
@@ -361,8 +370,8 @@ cudaError_t launch_cc_logits(const CcDims &D, const void *H, const void *W_O, co
         if (e != cudaSuccess) return e;
         const int ksteps = D.hq * D.d / 64, per = (ksteps + ksplit - 1) / ksplit;
         const int parts = ((D.dm + 255) / 256) * ((ksteps + per - 1) / per) * 2;
-        cc_finish_kernel<<<dim3((D.n + 255) / 256, D.batch), 256, 0, st>>>(part, D.n, parts,
-                                                                          D.sink, surprise);
+        cc_finish_kernel<<<dim3((D.n + 255) / 256, D.batch), 256, 0, st>>>(part, D.n, D.ld,
+                                                                          parts, D.sink, surprise);
         return cudaGetLastError();
     }
     if (D.dtype == KVE_F32)
@@ -370,21 +379,59 @@ cudaError_t launch_cc_logits(const CcDims &D, const void *H, const void *W_O, co
     return cc_logits_t<__nv_bfloat16>(D, O, H, W_O, W_U, X, part, surprise, err, st);
 }
 
+cudaError_t launch_cc_select_idx(const CcDims &D, const float *surprise, const int32_t *X,
+                                 const int32_t *pos, int32_t *kept, int32_t *X_out,
+                                 int32_t *pos_out, int ldo, cudaStream_t st) {
+    cc_select_kernel<<<D.batch, kSelT, 0, st>>>(surprise, X, pos, D.n, D.ld, D.J, kept, X_out,
+                                                 pos_out, ldo);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_cc_gather(const CcGatherSet &G, const int32_t *kept, int J, int ld_in,
+                             int ld_out, cudaStream_t st) {
+    const long total = G.start[G.count];
+    if (total <= 0) return cudaSuccess;
+    const long blocks = std::min<long>((total + 255) / 256, 152L * 8);
+    cc_gather_kernel<<<(unsigned)blocks, 256, 0, st>>>(G, kept, J, ld_in, ld_out);
+    return cudaGetLastError();
+}
+
+void cc_gather_add(CcGatherSet *G, const void *src, void *dst, int batch, int heads,
+                   size_t row_bytes, int J) {
+    const int k = G->count;
+    G->src[k] = static_cast<const uint4 *>(src);
+    G->dst[k] = static_cast<uint4 *>(dst);
+    G->heads[k] = heads;
+    G->vpr[k] = (int)(row_bytes / 16);
+    G->start[k + 1] = G->start[k] + (long)batch * heads * J * G->vpr[k];
+    G->count = k + 1;
+}
+
+namespace {
+__global__ void cc_fill_pos_kernel(int32_t *__restrict__ pos, int ld, int batch, int count,
+                                   int first) {
+    const int k = blockIdx.x * blockDim.x + threadIdx.x;
+    if (k < batch * count) pos[(size_t)(k / count) * ld + k % count] = first + k % count;
+}
+}  // namespace
+
+cudaError_t launch_cc_fill_pos(int32_t *pos, int ld, int batch, int count, int first,
+                               cudaStream_t st) {
+    cc_fill_pos_kernel<<<(batch * count + 255) / 256, 256, 0, st>>>(pos, ld, batch, count, first);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_cc_select(const CcDims &D, const float *surprise, const void *K, const void *V,
                              const int32_t *X, int32_t *kept, void *K_out, void *V_out,
                              int32_t *X_out, cudaStream_t st) {
     const size_t row = (size_t)D.d * dtype_size(D.dtype);
     if (row % 16 != 0) return cudaErrorInvalidValue;
-    cc_select_kernel<<<D.batch, kSelT, 0, st>>>(surprise, X, D.n, D.J, kept, X_out);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_cc_select_idx(D, surprise, X, nullptr, kept, X_out, nullptr, D.J, st);
     if (e != cudaSuccess) return e;
-    const int vpr = (int)(row / 16);
-    const long total = (long)D.batch * D.hkv * D.J * vpr;
-    const long blocks = std::min<long>((total + 255) / 256, 152L * 8);
-    cc_gather_kernel<<<(unsigned)blocks, 256, 0, st>>>((const uint4 *)K, (const uint4 *)V, kept,
-                                                      D.n, D.J, D.hkv, vpr, total,
-                                                      (uint4 *)K_out, (uint4 *)V_out);
-    return cudaGetLastError();
+    CcGatherSet G{};
+    cc_gather_add(&G, K, K_out, D.batch, D.hkv, row, D.J);
+    cc_gather_add(&G, V, V_out, D.batch, D.hkv, row, D.J);
+    return launch_cc_gather(G, kept, D.J, D.ld, D.J, st);
 }
 
 }  // namespace kve

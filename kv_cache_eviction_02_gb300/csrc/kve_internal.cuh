@@ -131,8 +131,11 @@ cudaError_t launch_h2o_export(const H2OState &s, void *K, void *V, int32_t *pos,
                               int32_t *count, cudaStream_t st);
 
 // Counter-causal surprise refresh, fast single-layer variant (counter_causal.cu)
+// n tokens scored per sequence; ld = row stride of the token dimension (>= n) of K, V, Q, H,
+// the token ids and the surprise (n for the stateless calls, the buffer capacity for the
+// refresh-cycle cache)
 struct CcDims {
-    int batch, hq, hkv, d, dm, n, vocab, dtype, sink, J;
+    int batch, hq, hkv, d, dm, n, vocab, dtype, sink, J, ld;
 };
 size_t cc_o_bytes(const CcDims &D);
 size_t cc_workspace_bytes(const CcDims &D);
@@ -159,5 +162,24 @@ cudaError_t launch_cc_logits(const CcDims &D, const void *H, const void *W_O, co
 cudaError_t launch_cc_select(const CcDims &D, const float *surprise, const void *K, const void *V,
                              const int32_t *X, int32_t *kept, void *K_out, void *V_out,
                              int32_t *X_out, cudaStream_t st);
+// selection only: kept [batch][J]; X_out and pos_out (optional) [batch][ldo]
+cudaError_t launch_cc_select_idx(const CcDims &D, const float *surprise, const int32_t *X,
+                                 const int32_t *pos, int32_t *kept, int32_t *X_out,
+                                 int32_t *pos_out, int ldo, cudaStream_t st);
+// gather of kept rows from up to four tensors [batch][heads][ld][row bytes], one launch
+struct CcGatherSet {
+    const uint4 *src[4];
+    uint4 *dst[4];
+    int heads[4], vpr[4];
+    long start[5];  // word offsets of each tensor in the launch's index space
+    int count;
+};
+void cc_gather_add(CcGatherSet *G, const void *src, void *dst, int batch, int heads,
+                   size_t row_bytes, int J);
+cudaError_t launch_cc_gather(const CcGatherSet &G, const int32_t *kept, int J, int ld_in,
+                             int ld_out, cudaStream_t st);
+// pos[b][k] = first + k for k < count, b < batch (row stride ld)
+cudaError_t launch_cc_fill_pos(int32_t *pos, int ld, int batch, int count, int first,
+                               cudaStream_t st);
 
 }  // namespace kve

@@ -174,3 +174,21 @@ def test_injected_failure_is_reported_then_cleared(api):
         api.lorekv_prepare_wo(pb, None, None, None, 0)
     assert e.value.status == api.KVE_EINVAL
     api.kve_inject_failure(0, 0)
+
+
+def test_cc_cache_create_validates_arguments(api):
+    L = api.lib()
+    h = ctypes.c_void_p()
+    for bad in (dict(keep_J=512, n_tokens=512),       # no room for a chunk
+                dict(keep_J=3, sink=4),                 # sinks plus the last token do not fit
+                dict(d_head=96), dict(dtype=2)):
+        sh = _cc(api, **bad).shape()
+        assert L.cc_cache_create(ctypes.byref(h), ctypes.byref(sh)) in (api.KVE_EINVAL,
+                                                                         api.KVE_EDTYPE)
+        assert not h.value
+    sh = _cc(api).shape()
+    assert L.cc_cache_create(None, ctypes.byref(sh)) == api.KVE_EINVAL
+    fake = ctypes.c_void_p(256)
+    assert L.cc_cache_append(None, fake, fake, fake, fake, fake, 1, None) == api.KVE_EINVAL
+    assert L.cc_cache_refresh(None, fake, fake, None) == api.KVE_EINVAL
+    assert L.cc_cache_length(None) == -api.KVE_EINVAL
