@@ -419,6 +419,7 @@ def run_native(args):
         line["h2o"] = bench_h2o(dev, stream, pg, world, args, pk)
     if not args.no_cc:
         line["cc_refresh"] = bench_cc(dev, stream, pg, args, pk)
+        line["cc_cycle"] = bench_cc_cycle(dev, stream, pg, args)
     if rank == 0 and not args.no_cpu:
         try:
             cb = cpu_baseline(cfg)
@@ -770,14 +771,70 @@ def bench_cc(dev, stream, pg, args, pk):
     return out
 
 
+def bench_cc_cycle(dev, stream, pg, args, J=512, h=128):
+    """Counter-causal refresh cycle (Algorithms 1 and 3 without the model) on the
+    Qwen2.5-7B-shaped last layer: memory J = 512, chunk h = J/4. Tokens of a seeded stream enter
+    in appends of h; each timed iteration is one append of h tokens plus the refresh over the
+    J + h candidates (with evictions), timed alone with CUDA events after a 256 MB L2 flush."""
+    import torch
+    from kv_cache_eviction_02_gb300 import api, synth
+    warm = max(args.warmup, 3)
+    steps = max(1, min(args.steps, 20))
+    T = J + h * (warm + steps)
+    cfg = synth.CC_CONFIGS["qwen7b_512"].replace(name="qwen7b_cycle", n=T, J=J)
+    inp = synth.cc_inputs(cfg, dev)
+    pb = api.CcProblem(cfg.batch, cfg.Hq, cfg.Hkv, cfg.d, cfg.d_model, J + h, cfg.vocab,
+                       api.KVE_BF16, cfg.sink, J)
+    cache = api.CcCache(pb)
+    chunks = [[inp[k][:, :, i:i + h].contiguous() if k in ("K", "V", "Q_fresh")
+               else inp[k][:, i:i + h].contiguous()
+               for k in ("K", "V", "Q_fresh", "H_last", "tokens")] for i in range(0, T, h)]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    it = 0
+    while it < J // h + warm:  # fill the memory (no evictions), then warm-up refreshes
+        assert cache.step(*chunks[it], inp["W_O"], inp["W_U"], stream)
+        it += 1
+    api.kve_check_device()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    barrier(pg)
+    torch.cuda.synchronize(dev)
+    api.kve_profile_enable(True)
+    for e0, e1 in ev:
+        with torch.cuda.stream(stream):
+            flush.zero_()
+        e0.record(stream)
+        cache.step(*chunks[it], inp["W_O"], inp["W_U"], stream)
+        e1.record(stream)
+        it += 1
+    torch.cuda.synchronize(dev)
+    api.kve_profile_enable(False)
+    prof = api.kve_profile_report()
+    api.kve_check_device()
+    ms = max_over_ranks(pg, sum(a.elapsed_time(b) for a, b in ev) / steps, dev)
+    cache.close()
+    del inp, chunks, flush
+    torch.cuda.empty_cache()
+    return {"ms_per_cycle": ms, "steps": steps, "tokens_per_s": h / (ms / 1e3),
+            "stages_ms": {k: v["ms"] / v["groups"] for k, v in prof.items()},
+            "gpu_launches_per_cycle": sum(v["kernels"] for v in prof.values()) // steps,
+            "config": f"qwen7b cycle: batch 1, 28/4 heads, d_head 128, d_model 3584, vocab "
+                      f"152064, memory J {J}, chunk h {h} (J + h = {J + h} candidates), sink 4, "
+                      "bf16; one append of h tokens + one refresh per cycle; L2 flushed before "
+                      "each cycle",
+            "page_ms_rtx4090_fp16": {"refresh n=512": CC_PAGE_MS["qwen7b_512"]}}
+
+
 def run_cc_only(args):
     import torch
     rank, world, local, pg = dist_init(args)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    out = bench_cc(dev, torch.cuda.current_stream(dev), pg, args, peaks())
+    st = torch.cuda.current_stream(dev)
+    out = {"cc_refresh": bench_cc(dev, st, pg, args, peaks()),
+           "cc_cycle": bench_cc_cycle(dev, st, pg, args)}
     if rank == 0:
-        print(json.dumps({"cc_refresh": out}), flush=True)
+        print(json.dumps(out), flush=True)
     barrier(pg)
 
 

@@ -662,27 +662,15 @@ int cc_cache_append(KveCcCache *c, const void *K_new, const void *V_new, const v
     const int at = c->mem + c->recent;
     cudaError_t e;
     {
-        ProfScope ps("cc_append", 6, st);
-        const size_t rk = cc_row_bytes(D, 0), rq = cc_row_bytes(D, 1), rh = cc_row_bytes(D, 2);
-        const size_t ld = (size_t)D.ld;
-        e = cudaMemcpy2DAsync(static_cast<char *>(b.K) + at * rk, ld * rk, K_new, count * rk,
-                              count * rk, (size_t)D.batch * D.hkv, cudaMemcpyDeviceToDevice, st);
-        if (e == cudaSuccess)
-            e = cudaMemcpy2DAsync(static_cast<char *>(b.V) + at * rk, ld * rk, V_new, count * rk,
-                                  count * rk, (size_t)D.batch * D.hkv, cudaMemcpyDeviceToDevice, st);
-        if (e == cudaSuccess)
-            e = cudaMemcpy2DAsync(static_cast<char *>(b.Q) + at * rq, ld * rq, Q_new, count * rq,
-                                  count * rq, (size_t)D.batch * D.hq, cudaMemcpyDeviceToDevice, st);
-        if (e == cudaSuccess)
-            e = cudaMemcpy2DAsync(static_cast<char *>(b.H) + at * rh, ld * rh, H_new, count * rh,
-                                  count * rh, (size_t)D.batch, cudaMemcpyDeviceToDevice, st);
-        if (e == cudaSuccess)
-            e = cudaMemcpy2DAsync(b.X + at, ld * sizeof(int32_t), tokens_new,
-                                  count * sizeof(int32_t), count * sizeof(int32_t), D.batch,
-                                  cudaMemcpyDeviceToDevice, st);
-        if (e == cudaSuccess) e = launch_cc_fill_pos(b.pos + at, D.ld, D.batch, count, c->seen, st);
+        ProfScope ps("cc_append", 1, st);
+        CcGatherSet G{};
+        cc_gather_add(&G, K_new, b.K, D.batch, D.hkv, cc_row_bytes(D, 0), count);
+        cc_gather_add(&G, V_new, b.V, D.batch, D.hkv, cc_row_bytes(D, 0), count);
+        cc_gather_add(&G, Q_new, b.Q, D.batch, D.hq, cc_row_bytes(D, 1), count);
+        cc_gather_add(&G, H_new, b.H, D.batch, 1, cc_row_bytes(D, 2), count);
+        e = launch_cc_append(G, count, at, D.ld, tokens_new, b.X, b.pos, D.batch, c->seen, st);
     }
-    if (e != cudaSuccess) return cuda_fail(e, "cc_cache_append: copy");
+    if (e != cudaSuccess) return cuda_fail(e, "cc_cache_append: launch");
     c->recent += count;
     c->seen += count;
     return KVE_OK;

@@ -408,16 +408,41 @@ void cc_gather_add(CcGatherSet *G, const void *src, void *dst, int batch, int he
 }
 
 namespace {
-__global__ void cc_fill_pos_kernel(int32_t *__restrict__ pos, int ld, int batch, int count,
-                                   int first) {
-    const int k = blockIdx.x * blockDim.x + threadIdx.x;
-    if (k < batch * count) pos[(size_t)(k / count) * ld + k % count] = first + k % count;
+// Appends count rows to tensors [batch][heads][ld][row] at row `at` from [batch][heads][count][row]
+// sources (16-byte words; the same four-tensor table as the gather), plus the ids and positions.
+__global__ void cc_append_kernel(CcGatherSet G, int count, int at, int ld,
+                                 const int32_t *__restrict__ x_new, int32_t *__restrict__ X,
+                                 int32_t *__restrict__ pos, int batch, int first) {
+    const long total = G.start[G.count];
+    for (long e = (long)blockIdx.x * blockDim.x + threadIdx.x; e < total + (long)batch * count;
+         e += (long)gridDim.x * blockDim.x) {
+        if (e >= total) {  // ids and positions
+            const int k = (int)(e - total), b = k / count, r = k % count;
+            X[(size_t)b * ld + at + r] = x_new[k];
+            pos[(size_t)b * ld + at + r] = first + r;
+            continue;
+        }
+        int k = 0;
+        while (k + 1 < G.count && e >= G.start[k + 1]) ++k;
+        const long local = e - G.start[k];
+        const int vpr = G.vpr[k];
+        const int c = (int)(local % vpr);
+        const long row = local / vpr;  // (b * heads + h) * count + r
+        const int r = (int)(row % count);
+        const long bh = row / count;
+        G.dst[k][((size_t)bh * ld + at + r) * vpr + c] = G.src[k][local];
+    }
 }
+
 }  // namespace
 
-cudaError_t launch_cc_fill_pos(int32_t *pos, int ld, int batch, int count, int first,
-                               cudaStream_t st) {
-    cc_fill_pos_kernel<<<(batch * count + 255) / 256, 256, 0, st>>>(pos, ld, batch, count, first);
+cudaError_t launch_cc_append(const CcGatherSet &G, int count, int at, int ld,
+                             const int32_t *x_new, int32_t *X, int32_t *pos, int batch, int first,
+                             cudaStream_t st) {
+    const long total = G.start[G.count] + (long)batch * count;
+    const long blocks = std::min<long>((total + 255) / 256, 152L * 8);
+    cc_append_kernel<<<(unsigned)blocks, 256, 0, st>>>(G, count, at, ld, x_new, X, pos, batch,
+                                                       first);
     return cudaGetLastError();
 }
 

@@ -178,8 +178,11 @@ void cc_gather_add(CcGatherSet *G, const void *src, void *dst, int batch, int he
                    size_t row_bytes, int J);
 cudaError_t launch_cc_gather(const CcGatherSet &G, const int32_t *kept, int J, int ld_in,
                              int ld_out, cudaStream_t st);
-// pos[b][k] = first + k for k < count, b < batch (row stride ld)
-cudaError_t launch_cc_fill_pos(int32_t *pos, int ld, int batch, int count, int first,
-                               cudaStream_t st);
+// append: count new rows of each table tensor (sources [batch][heads][count][row], entered with
+// cc_gather_add(..., J = count)) at row `at` of the [batch][heads][ld][row] destinations, plus
+// ids x_new [batch][count] and positions first + r, in one launch
+cudaError_t launch_cc_append(const CcGatherSet &G, int count, int at, int ld,
+                             const int32_t *x_new, int32_t *X, int32_t *pos, int batch, int first,
+                             cudaStream_t st);
 
 }  // namespace kve
