@@ -271,9 +271,35 @@ def oracle_step(cfg, smp):
     return S
 
 
-def cpu_baseline(cfg, steps=1, warmup=0):
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def cpu_baseline(cfg, steps=1, warmup=0, one_core=True, n_tokens=None):
+    """The oracle on the host cores: as many units as OpenMP threads (all cores busy), and, with
+    one_core, a single unit (the OpenMP loop then keeps one core busy). n_tokens < cfg.n samples
+    units of n_tokens tokens (a unit's pass costs in proportion to its tokens)."""
     import oracle
     threads = oracle.threads()
+    full_n = cfg.n
+    if n_tokens is not None and n_tokens < cfg.n:
+        cfg = cfg.replace(n=n_tokens)
     smp = oracle_sample(cfg, threads)
     for _ in range(warmup):
         oracle_step(cfg, smp)
@@ -282,10 +308,21 @@ def cpu_baseline(cfg, steps=1, warmup=0):
         oracle_step(cfg, smp)
     dt = (time.perf_counter() - t0) / steps
     tokens = smp["units"] * cfg.n
-    return {"value": tokens / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{smp['units']} whole units (layer, KV head) of the {cfg.name} workload, "
-                      f"{cfg.n} tokens each, reliability + scores + top-B + gather, fp64, "
-                      f"OpenMP over units", "seconds_per_step": dt}
+    res = {"value": tokens / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+           "sample": (f"{smp['units']} whole units (layer, KV head) of the {cfg.name} workload, "
+                      f"{cfg.n} tokens each" if cfg.n == full_n else
+                      f"{smp['units']} units (layer, KV head) of the {cfg.name} workload's shape "
+                      f"with {cfg.n} of its {full_n} tokens each (a unit's pass costs in "
+                      "proportion to its tokens)") +
+                     ", reliability + scores + top-B + gather, fp64, OpenMP over units",
+           "seconds_per_step": dt, "cpu_model": cpu_model()}
+    if one_core:
+        del smp
+        smp1 = oracle_sample(cfg, 1)
+        t0 = time.perf_counter()
+        oracle_step(cfg, smp1)
+        res["one_core_value"] = cfg.n / (time.perf_counter() - t0)
+    return res
 
 
 def run_reference(args):
@@ -295,7 +332,13 @@ def run_reference(args):
     if rank != 0:
         barrier(pg)
         return
-    cb = cpu_baseline(cfg, steps=args.steps, warmup=args.warmup)
+    # each step is a bounded sample: the units' token count is sized from a short calibration
+    # step so that warm-up and timed steps together take about 100 s of host time
+    steps_total = max(1, args.steps + args.warmup)
+    cal = cpu_baseline(cfg, steps=1, warmup=0, one_core=False, n_tokens=4096)
+    per_token_s = cal["seconds_per_step"] / 4096
+    n_s = int(min(cfg.n, max(4096, (100.0 / steps_total) / per_token_s)) // 4096 * 4096)
+    cb = cpu_baseline(cfg, steps=args.steps, warmup=args.warmup, one_core=False, n_tokens=n_s)
     line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": cb["seconds_per_step"] * 1e3, "higher_is_better": True,
@@ -303,7 +346,8 @@ def run_reference(args):
             "config": {"workload": f"{cfg.name}: 1 seq x {cfg.L} layers x {cfg.Hq}/{cfg.Hkv} "
                                    f"heads, d_head {cfg.d}, n {cfg.n}, bf16 inputs",
                        "sample": cb["sample"]},
-            "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample",
+                                                "cpu_model")},
             "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -332,6 +376,14 @@ def run_native(args):
     Lf = torch.empty(cfg.L, cfg.Hq, cfg.d, cfg.d, device=dev)
     G = torch.empty_like(Lf)
     api.lorekv_prepare_wo(pb, g["W_O"], Lf, G)
+    # per-model preparation, timed separately (warm: the second call)
+    pw0 = torch.cuda.Event(enable_timing=True)
+    pw1 = torch.cuda.Event(enable_timing=True)
+    pw0.record(stream)
+    api.lorekv_prepare_wo(pb, g["W_O"], Lf, G)
+    pw1.record(stream)
+    torch.cuda.synchronize(dev)
+    prepare_wo_ms = pw0.elapsed_time(pw1)
     run = api.LorekvPass(pb, dev)
     for _ in range(args.warmup):
         run.run(g, Lf, G)
@@ -400,6 +452,8 @@ def run_native(args):
                 "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": traffic,
                 "ms_per_launch": dom_ms}
     hbm_achieved = alg_bytes / (ms / 1e3) / 1e9
+    pass_mma_flops = ((attention_algorithmic_flops_per_token_unit(cfg)
+                       + scores_implemented_flops_per_token_unit(cfg)) * tokens_per_step)
     stages = {k: {"ms_per_step": v["ms"] / args.steps, "kernels": v["kernels"]}
               for k, v in prof.items()}
 
@@ -416,7 +470,13 @@ def run_native(args):
                        "parallelism": f"replicas: {world} x independent sequence"},
             "hbm_roofline": {"algorithmic_bytes": alg_bytes, "achieved_gbs": hbm_achieved,
                              "peak_gbs": pk["hbm_gbs"], "frac": hbm_achieved / pk["hbm_gbs"],
-                             "peak_source": pk["source"]},
+                             "peak_source": pk["source"],
+                             # the pass is a dense contraction: at the bf16 burst its MMA work
+                             # alone takes t_min, which caps the HBM fraction
+                             "ceiling_frac": (alg_bytes / (pass_mma_flops / (pk["bf16_tflops"] * 1e12))
+                                              / 1e9 / pk["hbm_gbs"]) if tensor else None,
+                             "pass_mma_flops": pass_mma_flops if tensor else None},
+            "prepare_wo_ms": prepare_wo_ms,
             "roofline": roof, "stages": stages, "gpu_launches": gpu_launches,
             "clocks": clk.summary()}
 
@@ -437,7 +497,7 @@ def run_native(args):
         try:
             cb = cpu_baseline(cfg)
             line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind",
-                                                       "sample")}
+                                                       "sample", "cpu_model", "one_core_value")}
         except Exception as e:  # the baseline is reported, never required
             line["cpu_baseline"] = {"value": None, "error": repr(e)}
     if rank == 0:
