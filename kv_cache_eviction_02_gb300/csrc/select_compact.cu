@@ -1,12 +1,13 @@
 // Chunked top-B selection and gather-compaction (LORE-KV page, "Evict and decode", Eq. 8;
 // "Hyperparameters": adjacent-token chunks of 4). One CTA per unit:
 //   1. chunk scores C_c = mean of S over [sink + c*chunk, sink + (c+1)*chunk), as order-preserving
-//      32-bit keys;
-//   2. MSB-first radix select (4 passes of 8 bits, shared-memory histograms) finds the key tau of
-//      the (B/chunk)-th largest chunk; every chunk above tau is kept, and among the chunks equal to
-//      tau the lowest indices fill the remainder;
-//   3. a block-wide prefix sum in chunk order writes the kept positions in ascending order
-//      (sink, kept chunks, window);
+//      32-bit keys, computed once into shared memory (recomputed from S when they do not fit);
+//   2. MSB-first radix select (4 passes of 8 bits, shared-memory histograms, one warp finds the
+//      bin) gives the key tau of the (B/chunk)-th largest chunk; every chunk above tau is kept, and
+//      among the chunks equal to tau the lowest indices fill the remainder;
+//   3. each thread owns a contiguous run of chunks: two block-wide prefix sums (chunks equal to tau,
+//      then kept chunks) give every thread its first output slot, and the kept positions are
+//      written in ascending order (sink, kept chunks, window);
 //   4. the CTA gathers the kept K and V rows with 16-byte vector copies.
 #include "kve_internal.cuh"
 
@@ -15,6 +16,7 @@ namespace kve {
 namespace {
 
 constexpr int kSelThreads = 1024;
+constexpr int kSelSmemKeys = 53248;  // chunk keys held in shared memory (208 KB)
 
 __device__ __forceinline__ uint32_t order_key(float f) {
     const uint32_t u = __float_as_uint(f);
@@ -62,6 +64,7 @@ __global__ void __launch_bounds__(kSelThreads) select_compact_kernel(
     LorekvDims D, const float *__restrict__ scores, const VecT *__restrict__ K,
     const VecT *__restrict__ V, int32_t *__restrict__ kept_idx, int32_t *__restrict__ kept_len,
     VecT *__restrict__ K_out, VecT *__restrict__ V_out, int cap, int vec_per_row) {
+    extern __shared__ uint32_t keys_s[];  // [nch] when they fit
     __shared__ uint32_t hist[256];
     __shared__ int warp_tot[32];
     __shared__ uint32_t s_prefix;
@@ -71,9 +74,13 @@ __global__ void __launch_bounds__(kSelThreads) select_compact_kernel(
     int32_t *idx = kept_idx + (size_t)unit * cap;
     const int nch = (D.n - D.sink - D.w) / D.chunk;
     const int keepc = D.B / D.chunk;
+    const bool in_smem = nch <= kSelSmemKeys;
     if (nch <= keepc) {
         for (int i = threadIdx.x; i < D.n; i += blockDim.x) idx[i] = i;
     } else {
+        if (in_smem)
+            for (int c = threadIdx.x; c < nch; c += blockDim.x)
+                keys_s[c] = chunk_key(S, D.sink, D.chunk, c);
         // ---- radix select of the keepc-th largest chunk key ----
         if (threadIdx.x == 0) {
             s_prefix = 0u;
@@ -86,41 +93,70 @@ __global__ void __launch_bounds__(kSelThreads) select_compact_kernel(
             __syncthreads();
             const uint32_t prefix = s_prefix;
             for (int c = threadIdx.x; c < nch; c += blockDim.x) {
-                const uint32_t key = chunk_key(S, D.sink, D.chunk, c);
+                const uint32_t key = in_smem ? keys_s[c] : chunk_key(S, D.sink, D.chunk, c);
                 if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
             }
             __syncthreads();
-            if (threadIdx.x == 0) {
-                int krem = s_krem;
-                int b = 255;
-                for (; b > 0; --b) {
-                    if ((int)hist[b] >= krem) break;
-                    krem -= (int)hist[b];
+            if (threadIdx.x < 32) {  // warp 0 finds the bin of the krem-th largest key
+                const int lane = threadIdx.x;
+                uint32_t cnt[8];
+                int sum = 0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    cnt[k] = hist[255 - 8 * lane - k];
+                    sum += (int)cnt[k];
                 }
-                s_krem = krem;
-                s_prefix = prefix | ((uint32_t)b << shift);
+                int incl = sum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const int krem = s_krem;
+                const unsigned ball = __ballot_sync(0xffffffffu, incl >= krem);
+                if (ball != 0u && lane == __ffs(ball) - 1) {
+                    int kr = krem - (incl - sum);
+                    int bsel = 248 - 8 * lane;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        if ((int)cnt[k] >= kr) {
+                            bsel = 255 - 8 * lane - k;
+                            break;
+                        }
+                        kr -= (int)cnt[k];
+                    }
+                    s_krem = kr;
+                    s_prefix = prefix | ((uint32_t)bsel << shift);
+                }
             }
             __syncthreads();
         }
         const uint32_t tau = s_prefix;
         const int take_eq = s_krem;  // chunks equal to tau to keep, lowest indices first
-        // ---- ordered write-out of the kept chunk positions ----
-        int run_eq = 0, run_sel = 0;
-        for (int base = 0; base < nch; base += blockDim.x) {
-            const int c = base + threadIdx.x;
-            uint32_t key = 0u;
-            if (c < nch) key = chunk_key(S, D.sink, D.chunk, c);
-            const int eq = (c < nch && key == tau) ? 1 : 0;
-            int tot_eq;
-            const int rank_eq = run_eq + block_exclusive_scan(eq, warp_tot, &tot_eq);
-            const int sel = (c < nch && (key > tau || (eq && rank_eq < take_eq))) ? 1 : 0;
-            int tot_sel;
-            const int pos = run_sel + block_exclusive_scan(sel, warp_tot, &tot_sel);
-            if (sel)
+        // ---- ordered write-out: thread t owns chunks [c0, c1) ----
+        // an odd run length puts the 32 threads of a warp on 32 different shared-memory banks
+        const int seg = ((nch + blockDim.x - 1) / blockDim.x) | 1;
+        const int c0 = min(nch, (int)threadIdx.x * seg), c1 = min(nch, c0 + seg);
+        int n_gt = 0, n_eq = 0;
+        for (int c = c0; c < c1; ++c) {
+            const uint32_t key = in_smem ? keys_s[c] : chunk_key(S, D.sink, D.chunk, c);
+            n_gt += key > tau;
+            n_eq += key == tau;
+        }
+        int tot;
+        const int eq_before = block_exclusive_scan(n_eq, warp_tot, &tot);
+        const int take_here = max(0, min(n_eq, take_eq - eq_before));
+        int pos = block_exclusive_scan(n_gt + take_here, warp_tot, &tot);
+        int eq_seen = 0;
+        for (int c = c0; c < c1; ++c) {
+            const uint32_t key = in_smem ? keys_s[c] : chunk_key(S, D.sink, D.chunk, c);
+            bool sel = key > tau;
+            if (key == tau) sel = eq_seen++ < take_here;
+            if (sel) {
                 for (int j = 0; j < D.chunk; ++j)
                     idx[D.sink + pos * D.chunk + j] = D.sink + c * D.chunk + j;
-            run_eq += tot_eq;
-            run_sel += tot_sel;
+                ++pos;
+            }
         }
         for (int i = threadIdx.x; i < D.sink; i += blockDim.x) idx[i] = i;
         for (int i = threadIdx.x; i < D.w; i += blockDim.x)
@@ -150,7 +186,13 @@ cudaError_t launch_select_compact(const LorekvDims &D, const float *scores, cons
     const size_t row_bytes = (size_t)D.d * dtype_size(D.dtype);
     if (row_bytes % 16 != 0) return cudaErrorInvalidValue;
     const int vpr = (int)(row_bytes / 16);
-    select_compact_kernel<uint4><<<D.units, kSelThreads, 0, st>>>(
+    const int nch = (D.n - D.sink - D.w) / D.chunk;
+    const size_t smem = nch <= kSelSmemKeys ? (size_t)nch * sizeof(uint32_t) : 0;
+    cudaError_t e = cudaFuncSetAttribute(select_compact_kernel<uint4>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSelSmemKeys * (int)sizeof(uint32_t));
+    if (e != cudaSuccess) return e;
+    select_compact_kernel<uint4><<<D.units, kSelThreads, smem, st>>>(
         D, scores, (const uint4 *)K, (const uint4 *)V, kept_idx, kept_len, (uint4 *)K_out,
         (uint4 *)V_out, cap, vpr);
     return cudaGetLastError();
