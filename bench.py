@@ -185,11 +185,14 @@ def scores_algorithmic_flops_per_token_unit(cfg) -> int:
 
 
 def scores_implemented_flops_per_token_unit(cfg) -> int:
-    """MMA work the tensor-core scoring kernel executes per (token, unit), two query heads per CTA
-    (64-query rows each): S = K [Q_h0;Q_h1]^T (N = 128) and [X | Y_a] = V [U; L^T(0:64)]^T (N = 256)
-    over K = d plus one constant-adding K step of 16, and Y_b (N = 128) over the second half of d."""
+    """MMA work the tensor-core scoring kernel (d = 128) executes per (token, unit), two query
+    heads per CTA (64-query rows each): S = K [Q_h0;Q_h1]^T (N = 128) over K = 128 plus a
+    constant-adding K step of 16; X = V U^T (128 columns) over K = 128; Y = V L_h of both heads in
+    16-column groups that each run only the K steps at or after their diagonal block (Y_a: 26 and
+    Y_b: 10 group-steps of 32 columns x 16); the constant-adding step over X | Y_a (N = 256)."""
     pairs = (cfg.g + 1) // 2
-    return 2 * pairs * (128 * (cfg.d + 16) + 256 * (cfg.d + 16) + 128 * (cfg.d // 2))
+    per_pair = 128 * (128 + 16) + 128 * 128 + 32 * 16 * 26 + 32 * 16 * 10 + 256 * 16
+    return 2 * pairs * per_pair
 
 
 def attention_algorithmic_flops_per_token_unit(cfg) -> int:

@@ -210,7 +210,8 @@ LorekvWorkspace lorekv_ws_layout(const LorekvDims &D) {
     const bool bf = D.dtype == KVE_BF16;
     W.u16 = take(bf ? 2 * uq * D.d : 0);
     W.q16 = take(bf ? 2 * uq * D.d : 0);
-    W.lt16 = take(bf ? 2 * (size_t)D.L * D.Hq * D.d * D.d : 0);
+    // L^T packed per pair of query heads (256 rows of d each; an odd group size pads one head)
+    W.lt16 = take(bf ? 2 * (size_t)D.L * D.Hkv * ((D.g + 1) / 2) * 256 * D.d : 0);
     W.part_s = take(bf ? sizeof(float) * (size_t)D.units * D.g * D.n : 0);
     W.qconst = take(bf ? sizeof(float4) * uq : 0);
     W.rel_part = take(sizeof(float4) * (size_t)D.S * D.MT * D.rel_splits);

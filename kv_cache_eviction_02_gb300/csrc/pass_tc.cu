@@ -94,13 +94,26 @@ void tc_plan(LorekvDims *D) {
 namespace {
 
 // ---- small packing kernels -------------------------------------------------------------------------
-// lt16[lh][j][k] = bf16(L[lh][k][j]): the B operand (N = j, K = k, K-major) of Y = V L.
+// The B operand (N = j, K = k, K-major) of Y = V L_h for the two query heads of a CTA, d = 128:
+// lt16[l][kv head][pair][r][k] = bf16(L_h[k][j]). Rows 0-127 hold columns j < 64 and rows
+// 128-255 columns j >= 64, both in groups of 16 columns alternating between the pair's heads
+// (r = 32 g + 16 head + t <-> j = 16 g + t, offset by 64 for the second half). Since L_h is
+// lower triangular, column j only gets contributions from k >= j: at the 16-wide K step s only
+// the first groups are non-zero, and the MMA over K step s reads just those leading rows. A
+// missing second head (odd group size) is zero.
 __global__ void pack_lt_kernel(const float *__restrict__ L, __nv_bfloat16 *__restrict__ lt,
-                               int d) {
-    const size_t base = (size_t)blockIdx.x * d * d;
-    for (int e = threadIdx.x; e < d * d; e += blockDim.x) {
-        const int j = e / d, k = e % d;
-        lt[base + e] = __float2bfloat16_rn(L[base + (size_t)k * d + j]);
+                               int Hq, int Hkv, int g, int npairs) {
+    constexpr int d = 128;
+    const int blk = blockIdx.x;  // (l * Hkv + kh) * npairs + pair
+    const int pair = blk % npairs, kh = (blk / npairs) % Hkv, l = blk / (npairs * Hkv);
+    for (int e = threadIdx.x; e < 256 * d; e += blockDim.x) {
+        const int r = e / d, k = e % d;
+        const int rr = r & 127, hd = (rr >> 4) & 1;
+        const int j = (r >= 128 ? 64 : 0) + 16 * (rr >> 5) + (rr & 15);
+        const int hin = 2 * pair + hd;
+        float v = 0.f;
+        if (hin < g) v = L[(((size_t)l * Hq + kh * g + hin) * d + k) * d + j];
+        lt[(size_t)blk * 256 * d + e] = __float2bfloat16_rn(v);
     }
 }
 
@@ -151,9 +164,10 @@ constexpr int kScThreads = 320;  // TMA, MMA issuer, 2 epilogue groups (one per 
 // and the heads' operands are interleaved so that each MMA is wide (N = 128 or 256).
 // Shared memory:
 //   Q    2 K-blocks x 16 KB: rows [Q_h0 (64) | Q_h1 (64)]           -> B of S = K [Q_h0;Q_h1]^T
-//   B2   rows [U_h0 | U_h1 | Lt_h0 0-63 | Lt_h1 0-63 | Lt_h0 64-127 | Lt_h1 64-127] (64 rows
-//        each; Lt_h = L_h^T) -> B of V B2^T. Rows 64..127 of L_h^T are zero for k < 64, so
-//        K-block 0 holds rows 0-255 (32 KB) and K-block 1 rows 0-383 (48 KB).
+//   B2   rows [U_h0 | U_h1 | Lt rows for Y columns 0-63 | Lt rows for Y columns 64-127] -> B of
+//        V B2^T, where the L_h^T rows of the two heads alternate in groups of 16 (the packing
+//        in pack_lt_kernel). Rows of L_h^T for columns >= 64 are zero for k < 64, so K-block 0
+//        holds rows 0-255 (32 KB) and K-block 1 rows 0-383 (48 KB).
 //   ring 3 x 32 KB TMA boxes (V_i, K_i, V_i+1, ...).
 //   one extra K step (32-byte swizzle, 16 bf16 per row) that adds per-query constants inside the
 //   MMAs: A_aug (128 token rows [1, 1, 1, 0, ...]), B_aug_S (the 128 query rows of S: -lse2/k1
@@ -161,9 +175,10 @@ constexpr int kScThreads = 320;  // TMA, MMA issuer, 2 epilogue groups (one per 
 //   terms, then 128 zero rows under Y). With U staged as -2u, the MMAs give S' = s - lse2/k1 and
 //   X' = c - 2 v.u directly.
 //   per-query weights (general query layout) | per-set weights | barriers.
-// TMEM (512 columns, one buffer): S_h0 | S_h1 | X_h0 | X_h1 | Ya_h0 | Ya_h1 | Yb_h0 | Yb_h1,
-// 64 columns each (X = V U^T; Ya/Yb = columns 0-63 / 64-127 of Y = V L_h); Yb only takes the
-// second K-block of V.
+// TMEM (512 columns, one buffer): S_h0 | S_h1 | X_h0 | X_h1 (64 columns each) | Ya | Yb (128
+// each: columns 0-63 / 64-127 of Y = V L_h of both heads, in alternating groups of 16). Yb only
+// takes the second K-block of V, and each 16-column group only the K steps at or after its
+// diagonal block.
 constexpr int SC_HPC = 2;                                  // query heads per CTA
 constexpr uint32_t SC_Q = 0, SC_B2 = 32768;
 constexpr uint32_t SC_B2_K0 = 0, SC_B2_K1 = 32768;         // K-block offsets inside B2
@@ -282,19 +297,27 @@ __global__ void __launch_bounds__(kScThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {  // ---- TMA producer ----
-            tc::mbar_expect_tx(ops_full, 57344u * nh);
+            tc::mbar_expect_tx(ops_full, 32768u * nh + 49152u);
             for (int hh = 0; hh < nh; ++hh) {
                 const int qrow = unit * A.Qu + (j0 + hh) * A.nq;
-                const int lrow = (l * A.Hq + kh * A.g + j0 + hh) * 128;
                 for (int kb = 0; kb < 2; ++kb) {
                     uint8_t *b2 = sm + SC_B2 + (kb ? SC_B2_K1 : SC_B2_K0) + hh * 8192;
                     tc::tma_load_2d(sm + SC_Q + kb * 16384 + hh * 8192, &tm_q, 64 * kb, qrow,
                                     ops_full);
                     tc::tma_load_2d(b2, &tm_u, 64 * kb, qrow, ops_full);
-                    tc::tma_load_2d(b2 + 16384, &tm_lt, 64 * kb, lrow, ops_full);
-                    if (kb) tc::tma_load_2d(b2 + 32768, &tm_lt, 64 * kb, lrow + 64, ops_full);
                 }
             }
+            // the pair's packed L^T rows: 0-127 (Y columns 0-63) into both K-blocks, 128-255
+            // (Y columns 64-127) into the second
+            const int lrow = ((l * A.Hkv + kh) * npairs + hp) * 256;
+            for (int kb = 0; kb < 2; ++kb) {
+                uint8_t *b2 = sm + SC_B2 + (kb ? SC_B2_K1 : SC_B2_K0);
+                tc::tma_load_2d(b2 + 16384, &tm_lt, 64 * kb, lrow, ops_full);
+                tc::tma_load_2d(b2 + 16384 + 8192, &tm_lt, 64 * kb, lrow + 64, ops_full);
+            }
+            tc::tma_load_2d(sm + SC_B2 + SC_B2_K1 + 32768, &tm_lt, 64, lrow + 128, ops_full);
+            tc::tma_load_2d(sm + SC_B2 + SC_B2_K1 + 32768 + 8192, &tm_lt, 64, lrow + 192,
+                            ops_full);
             int issued = 0;
             for (int c = 0; c < 2 * ntl; ++c) {
                 const int slot = c % SC_SLOTS;
@@ -332,20 +355,26 @@ __global__ void __launch_bounds__(kScThreads, 1)
                 if (!tc::mbar_wait(tfree1, (i & 1) ^ 1, abort_flag, A.err)) break;
                 tc::fence_after_sync();
                 const uint32_t v_addr = ring + sv * 32768;
+                // K steps from the last down: the first product covers every column; at K step
+                // s the Y_a columns of groups above s are zero (L lower triangular) and are left
+                // out by narrowing N to the leading B rows
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
+                for (int k = 7; k >= 0; --k) {
                     const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;
                     const uint32_t bo = ((k >> 2) ? SC_B2_K1 : SC_B2_K0) + (k & 3) * 32;
+                    const int nn = 128 + 32 * (k < 3 ? k + 1 : 4);
                     tc::mma_bf16(tmem + 128, tc::sdesc_sw128(v_addr + ao, 16, 1024),
-                                 tc::sdesc_sw128(b2_addr + bo, 16, 1024), id256, k > 0);
+                                 tc::sdesc_sw128(b2_addr + bo, 16, 1024),
+                                 tc::idesc_bf16(128, nn, 0), k < 7);
                 }
                 tc::mma_bf16(tmem + 128, tc::sdesc_sw32(aug_a), tc::sdesc_sw32(aug_v), id256, 1);
 #pragma unroll
-                for (int k = 4; k < 8; ++k) {
+                for (int k = 7; k >= 4; --k) {  // Y_b: groups g need K steps >= 4 + g
                     const uint32_t ao = 16384 + (k & 3) * 32;
                     const uint32_t bo = SC_B2_K1 + 32768 + (k & 3) * 32;
                     tc::mma_bf16(tmem + 384, tc::sdesc_sw128(v_addr + ao, 16, 1024),
-                                 tc::sdesc_sw128(b2_addr + bo, 16, 1024), id128, k > 4);
+                                 tc::sdesc_sw128(b2_addr + bo, 16, 1024),
+                                 tc::idesc_bf16(128, 32 * (k - 3), 0), k < 7);
                 }
                 tc::mma_commit(&rempty[sv]);
                 tc::mma_commit(tfull1);
@@ -391,29 +420,32 @@ __global__ void __launch_bounds__(kScThreads, 1)
             float x0[32], x1[32];
             uint64_t np2[4] = {0, 0, 0, 0};  // bit pattern 0 = (0.f, 0.f)
             {
-                float y0[32], y1[32];
-                tc::tmem_ld32(tb + 256 + 64 * hh, y0);
-                tc::tmem_ld32(tb + 288 + 64 * hh, y1);
+                // this head's 64 Y_a and 64 Y_b columns: groups of 16 at 32 g + 16 hh
+                float y[4][16];
+#pragma unroll
+                for (int gi = 0; gi < 4; ++gi) tc::tmem_ld16(tb + 256 + 32 * gi + 16 * hh, y[gi]);
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    const uint64_t a = tc::pk2(y0[c], y0[c + 1]), b = tc::pk2(y1[c], y1[c + 1]);
-                    np2[(c >> 1) & 3] = tc::fma2(a, a, np2[(c >> 1) & 3]);
-                    np2[(c >> 1) & 3] = tc::fma2(b, b, np2[(c >> 1) & 3]);
-                }
-                tc::tmem_ld32(tb + 384 + 64 * hh, y0);
-                tc::tmem_ld32(tb + 416 + 64 * hh, y1);
+                for (int gi = 0; gi < 4; ++gi)
+#pragma unroll
+                    for (int c = 0; c < 16; c += 2) {
+                        const uint64_t a = tc::pk2(y[gi][c], y[gi][c + 1]);
+                        np2[(c >> 1) & 3] = tc::fma2(a, a, np2[(c >> 1) & 3]);
+                    }
+#pragma unroll
+                for (int gi = 0; gi < 4; ++gi) tc::tmem_ld16(tb + 384 + 32 * gi + 16 * hh, y[gi]);
                 tc::tmem_ld32(tb + 128 + 64 * hh, x0);
                 tc::tmem_ld32(tb + 160 + 64 * hh, x1);
                 tc::tmem_wait_ld();
                 tc::fence_before_sync();
                 tc::mbar_arrive(tfree1);
 #pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    const uint64_t a = tc::pk2(y0[c], y0[c + 1]), b = tc::pk2(y1[c], y1[c + 1]);
-                    np2[(c >> 1) & 3] = tc::fma2(a, a, np2[(c >> 1) & 3]);
-                    np2[(c >> 1) & 3] = tc::fma2(b, b, np2[(c >> 1) & 3]);
-                }
+                for (int gi = 0; gi < 4; ++gi)
+#pragma unroll
+                    for (int c = 0; c < 16; c += 2) {
+                        const uint64_t a = tc::pk2(y[gi][c], y[gi][c + 1]);
+                        np2[(c >> 1) & 3] = tc::fma2(a, a, np2[(c >> 1) & 3]);
+                    }
             }
             float nv;
             {
@@ -841,7 +873,8 @@ cudaError_t launch_scores_tc(const LorekvDims &D, const void *K, const void *V, 
                              cudaStream_t st) {
     char *b = static_cast<char *>(ws);
     __nv_bfloat16 *lt16 = reinterpret_cast<__nv_bfloat16 *>(b + W.lt16);
-    pack_lt_kernel<<<D.L * D.Hq, 256, 0, st>>>(Lf, lt16, D.d);
+    const int npairs = (D.g + SC_HPC - 1) / SC_HPC;
+    pack_lt_kernel<<<D.L * D.Hkv * npairs, 256, 0, st>>>(Lf, lt16, D.Hq, D.Hkv, D.g, npairs);
     const long rows_q = (long)D.units * D.Qu;
     pack_qconst_kernel<<<(unsigned)((rows_q + 255) / 256), 256, 0, st>>>(
         reinterpret_cast<const float *>(b + W.lse2), reinterpret_cast<const float *>(b + W.cq),
@@ -853,7 +886,7 @@ cudaError_t launch_scores_tc(const LorekvDims &D, const void *K, const void *V, 
         !make_tmap_bf16_2d(&tv, V, 128, rows, 64, 128) ||
         !make_tmap_bf16_2d(&tq, b + W.q16, 128, (uint64_t)rows_q, 64, 64) ||
         !make_tmap_bf16_2d(&tu, b + W.u16, 128, (uint64_t)rows_q, 64, 64) ||
-        !make_tmap_bf16_2d(&tl, lt16, 128, (uint64_t)D.L * D.Hq * 128, 64, 64))
+        !make_tmap_bf16_2d(&tl, lt16, 128, (uint64_t)D.L * D.Hkv * npairs * 256, 64, 64))
         return cudaErrorInvalidValue;
     ScoresArgs A;
     A.n = D.n;
@@ -866,7 +899,6 @@ cudaError_t launch_scores_tc(const LorekvDims &D, const void *K, const void *V, 
     A.sink = D.sink;
     A.w = D.w;
     A.ntiles = (D.n + 127) / 128;
-    const int npairs = (D.g + SC_HPC - 1) / SC_HPC;
     A.nranges = balance_parts((long)D.units * npairs, A.ntiles, 64);
     A.tpr = (A.ntiles + A.nranges - 1) / A.nranges;
     A.nranges = (A.ntiles + A.tpr - 1) / A.tpr;
