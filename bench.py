@@ -534,6 +534,53 @@ def gpu_local_cpus(dev):
     return cpus or None
 
 
+def _cpulist(text: str) -> set:
+    cpus = set()
+    for part in text.strip().split(","):
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        elif part:
+            cpus.add(int(part))
+    return cpus
+
+
+def numa_report(dev) -> dict:
+    """Where host memory and CPUs sit relative to the GPU: the GPU's NUMA node (sysfs of its PCI
+    function) and, per node, the CPUs this process may use and the node's memory."""
+    import torch
+    out = {"gpu_node": None, "nodes": {}}
+    p = torch.cuda.get_device_properties(dev)
+    bus = getattr(p, "pci_bus_id", None)
+    if bus is not None:
+        path = (f"/sys/bus/pci/devices/{getattr(p, 'pci_domain_id', 0):04x}:{bus:02x}:"
+                f"{getattr(p, 'pci_device_id', 0):02x}.0/numa_node")
+        try:
+            with open(path) as f:
+                out["gpu_node"] = int(f.read().strip())
+        except (OSError, ValueError):
+            pass
+    allowed = os.sched_getaffinity(0)
+    base = "/sys/devices/system/node"
+    try:
+        names = sorted(x for x in os.listdir(base) if x.startswith("node") and x[4:].isdigit())
+    except OSError:
+        names = []
+    for name in names:
+        info = {}
+        try:
+            with open(os.path.join(base, name, "cpulist")) as f:
+                info["cpus"] = len(_cpulist(f.read()) & allowed)
+            with open(os.path.join(base, name, "meminfo")) as f:
+                for ln in f:
+                    if "MemTotal" in ln:
+                        info["mem_gb"] = round(int(ln.split()[-2]) / 2**20, 1)
+        except (OSError, ValueError):
+            pass
+        out["nodes"][name[4:]] = info
+    return out
+
+
 def e2e_lorekv(cfg, g, run, Lf, G, dev, stream, pg, world, args):
     """Host buffers in, host buffers out: per step the inputs are copied from pinned host memory,
     the pass runs, and the compressed cache is read back.
@@ -619,6 +666,19 @@ def e2e_lorekv(cfg, g, run, Lf, G, dev, stream, pg, world, args):
 
     one()
     torch.cuda.synchronize(dev)
+    # the link's own rate on this machine: pinned host -> device copies of one layer's K
+    probe_src = host["K"][:, 0]
+    probe_dst = torch.empty(probe_src.shape, dtype=probe_src.dtype, device=dev)
+    p0 = torch.cuda.Event(enable_timing=True)
+    p1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        p0.record(stream)
+        for _ in range(4):
+            probe_dst.copy_(probe_src, non_blocking=True)
+        p1.record(stream)
+    torch.cuda.synchronize(dev)
+    link_gbs = 4 * probe_src.numel() * probe_src.element_size() / (p0.elapsed_time(p1) / 1e3) / 1e9
+    del probe_dst
     barrier(pg)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -632,7 +692,9 @@ def e2e_lorekv(cfg, g, run, Lf, G, dev, stream, pg, world, args):
     os.sched_setaffinity(0, old_aff)
     res = {"value": cfg.units * cfg.n * world / (ms / 1e3), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-           "steps": steps}
+           "steps": steps, "h2d_gbs_effective": h2d / (ms / 1e3) / 1e9,
+           "link_probe_gbs": link_gbs,
+           "numa": numa_report(dev)}
     if chunked:
         res["issue"] = (f"{cfg.L // cl} chunks of {cl} layers: the next chunk's host-to-device "
                         "copy overlaps the current chunk's pass (copy stream + compute stream)")
