@@ -803,9 +803,20 @@ def bench_h2o(dev, stream, pg, world, args, pk):
     st.close()
     del hin
     torch.cuda.empty_cache()
+    # prefill: two passes of 128 x 128 x 128 products (row normalisers, then column sums) over
+    # every (query tile, key tile <= it) pair of the causal prompt; algorithmically one q.k over
+    # the causal triangle
+    nt = (cfg.prompt + 127) // 128
+    pf_impl = cfg.units * 2 * (nt * (nt + 1) // 2) * 2 * 128 ** 3
+    pf_alg = cfg.units * (cfg.prompt * (cfg.prompt + 1) // 2) * 2 * cfg.d
+    pf_roof = {"kernel": "h2o_colsum_tc + h2o_compress", "bound": "tensor",
+               "achieved": pf_alg / (prefill_ms / 1e3) / 1e12, "peak": pk["bf16_tflops"],
+               "unit": "TFLOP/s", "frac": pf_alg / (prefill_ms / 1e3) / 1e12 / pk["bf16_tflops"],
+               "flops": "algorithmic", "implemented_flops": pf_impl,
+               "implemented_frac": pf_impl / (prefill_ms / 1e3) / 1e12 / pk["bf16_tflops"]}
     return {"metric": "KV tokens attended+scored/sec (H2O decode step)",
             "value": tokens * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
-            "steps": steps, "warmup": w, "prefill_ms": prefill_ms,
+            "steps": steps, "warmup": w, "prefill_ms": prefill_ms, "prefill_roofline": pf_roof,
             "config": f"{cfg.name}: batch {cfg.batch}, {cfg.L} layers, {cfg.H} heads, d_head {cfg.d}, "
                       f"prompt {cfg.prompt}, {cfg.steps} decode steps, budget 20%, fp16",
             "roofline": {"kernel": "h2o_step", "bound": "hbm", "achieved": ach,
