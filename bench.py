@@ -399,12 +399,19 @@ def run_native(args):
     ev1 = torch.cuda.Event(enable_timing=True)
     barrier(pg)
     torch.cuda.synchronize(dev)
+    # an event between consecutive steps as well, for the per-step spread (the steps still run
+    # back to back; the first and last events bracket the timed region)
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(max(0, args.steps - 1))]
     with ClockSampler(local) as clk:
         ev0.record(stream)
-        for _ in range(args.steps):
+        for k in range(args.steps):
             run.run(g, Lf, G)
+            if k + 1 < args.steps:
+                step_ev[k].record(stream)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
+    marks = [ev0] + step_ev + [ev1]
+    step_ms = [a.elapsed_time(b) for a, b in zip(marks[:-1], marks[1:])]
     barrier(pg)
     api.kve_profile_enable(False)
     prof = api.kve_profile_report()
@@ -480,6 +487,8 @@ def run_native(args):
                                               / 1e9 / pk["hbm_gbs"]) if tensor else None,
                              "pass_mma_flops": pass_mma_flops if tensor else None},
             "prepare_wo_ms": prepare_wo_ms,
+            "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms),
+                        "max": max(step_ms)},
             "roofline": roof, "stages": stages, "gpu_launches": gpu_launches,
             "clocks": clk.summary()}
 
