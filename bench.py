@@ -42,7 +42,7 @@ WORKLOAD = "llama"        # the 128K-context configuration the metric is quoted 
 # scores_tc_kernel: 2.208 GB read + 0.068 GB written per launch on the Mistral-7B-shaped workload
 # (n = 16384, ncu --set full), scaled by the 8x token count of the 128K workload (every term of the
 # traffic is proportional to the tokens scored).
-NCU_TRAFFIC = {"scores": (8 * (2.207931e9 + 0.068153e9), "dd5753f54b8e670b")}
+NCU_TRAFFIC = {"scores": (8 * (2.207931e9 + 0.068153e9), "60571dc18ccf0bef")}
 # cc_attn_tc_kernel on the n = 4096 counter-causal workload (ncu --set full, one launch):
 # 37.807 MB read + 0.233 MB written
 NCU_TRAFFIC_CC = {("cc_attention", "qwen7b_4096"): (37.80736e6 + 0.23296e6, "741c9d25cbda615d")}
