@@ -113,8 +113,10 @@ int lorekv_score(const KveShape *shape, const KveLorekvParams *params, const voi
  *     lorekv_workspace_size() exceeds 64 MiB are rejected with KVE_EWORKSPACE (nothing launched);
  *     use lorekv_score with a workspace for them.
  *   - The call allocates nothing (no cudaMalloc/cudaFree, no library allocator).
- *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
- *     that device current; make that first call before any stream capture.
+ *   - The first call in each CUDA context (a device's primary context, a context made current
+ *     through the driver API, a context created again after cudaDeviceReset) looks up the
+ *     array's device address in that context (cudaGetSymbolAddress) and caches it by the
+ *     driver's context id; make that first call before any stream capture.
  *   - The array is shared by every call on the device and keeps the last call's contents; nothing
  *     in it needs to start at zero (each call writes every scratch region before reading it).
  *     Calls that overlap on the GPU (different streams, or threads without ordering) race on it:
@@ -174,7 +176,9 @@ typedef struct KveH2O KveH2O;
 
 /* Allocates the state for batch x n_layers x n_heads units of head size d_head, for sequences of
  * up to max_len tokens (prompt + decode steps), budget_frac in (0, 1]. Slot capacity per unit is
- * floor(budget_frac*max_len) + 1. dtype KVE_F16 or KVE_BF16. *out receives the handle. */
+ * floor(budget_frac*max_len) + 1. dtype KVE_F16 or KVE_BF16. *out receives the handle. The state
+ * also holds the prefill's scratch (two fp32 partial column sums per unit and prompt token, sized
+ * for a prompt of max_len), so h2o_prefill and h2o_decode_step allocate nothing. */
 int h2o_state_create(KveH2O **out, int batch, int n_layers, int n_heads, int d_head, int max_len,
                      float budget_frac, int dtype);
 

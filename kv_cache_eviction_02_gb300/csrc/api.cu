@@ -102,21 +102,57 @@ int report_error(int code, const char *fmt, ...) {
     return code;
 }
 
+// ---- device addresses of the library's __device__ variables ------------------------------------
+namespace {
+using PFN_ctxGetCurrent = int (*)(void **);
+using PFN_ctxGetId = int (*)(void *, unsigned long long *);
+
+// The driver's unique id of the calling thread's current context (ids are never reused, so a
+// context created after cudaDeviceReset, or a non-primary context, has an id of its own).
+bool current_context_id(unsigned long long *id) {
+    static PFN_ctxGetCurrent get_cur = nullptr;
+    static PFN_ctxGetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_cur = reinterpret_cast<PFN_ctxGetCurrent>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_ctxGetId>(p);
+    });
+    if (!get_cur || !get_id) return false;
+    void *ctx = nullptr;
+    if (get_cur(&ctx) != 0 || !ctx) return false;
+    return get_id(ctx, id) == 0;
+}
+}  // namespace
+
+void *context_symbol_address(const void *symbol, SymbolCache &cache) {
+    unsigned long long id = 0;
+    std::lock_guard<std::mutex> lk(cache.mu);
+    const bool have_id = current_context_id(&id);
+    if (have_id)
+        for (auto &e : cache.entries)
+            if (e.first == id) return e.second;
+    void *p = nullptr;  // also makes the runtime's context current if none was yet
+    if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess || !p) return nullptr;
+    if (have_id || current_context_id(&id)) cache.entries.emplace_back(id, p);
+    return p;
+}
+
 // ---- device error word ---------------------------------------------------------------------------
 __device__ unsigned g_kve_error_word;
 
 unsigned *device_error_word() {
-    static std::mutex mu;
-    static unsigned *addr[64] = {nullptr};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lk(mu);
-    if (!addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_kve_error_word) != cudaSuccess) return nullptr;
-        addr[dev] = static_cast<unsigned *>(p);
-    }
-    return addr[dev];
+    static SymbolCache cache;
+    return static_cast<unsigned *>(
+        context_symbol_address(reinterpret_cast<const void *>(&g_kve_error_word), cache));
 }
 
 // ---- LORE-KV shape rules -------------------------------------------------------------------------
@@ -216,6 +252,11 @@ LorekvWorkspace lorekv_ws_layout(const LorekvDims &D) {
     W.qconst = take(bf ? sizeof(float4) * uq : 0);
     W.rel_part = take(sizeof(float4) * (size_t)D.S * D.MT * D.rel_splits);
     W.cosm = take(sizeof(float) * (size_t)D.S * D.L * D.Hq * D.M * D.M);
+    W.part_mx = take(sizeof(float) * uq * D.nsplit);
+    W.amax = take(sizeof(float) * uq);
+    W.pk_cnt = take(sizeof(int) * uq);
+    W.pk_tok = take(sizeof(int) * uq * kPeakSlots);
+    W.pk_e = take(sizeof(float) * uq * kPeakSlots);
     W.total = off;
     return W;
 }
@@ -564,6 +605,10 @@ int lorekv_score(const KveShape *shape, const KveLorekvParams *params, const voi
         else
             e = launch_scores_simt(D, K, V, Q_W, Q_look, L, workspace, W, scores_out, st);
     }
+    if (e == cudaSuccess) {  // pairs with a > 1/4, left out above, evaluated exactly
+        ProfScope ps("peak_fix", 2, st);
+        e = launch_peak_fix(D, K, V, Q_W, Q_look, L, workspace, W, scores_out, st);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "lorekv_score: launch");
     return KVE_OK;
 }
@@ -818,6 +863,9 @@ int h2o_state_create(KveH2O **out, int batch, int n_layers, int n_heads, int d_h
     if (e == cudaSuccess) e = cudaMalloc(&s.pos, rows * sizeof(int32_t));
     if (e == cudaSuccess) e = cudaMalloc(&s.nslots, s.units * sizeof(int32_t));
     if (e == cudaSuccess) e = cudaMalloc(&s.hole, s.units * sizeof(int32_t));
+    // scratch of the prefill's partial column sums, sized for a prompt of max_len tokens
+    if (e == cudaSuccess)
+        e = cudaMalloc(&s.prefill_part, sizeof(float) * (size_t)s.units * kColsumTcParts * max_len);
     if (e == cudaSuccess) e = cudaMemset(s.K, 0, rows * d_head * 2);
     if (e == cudaSuccess) e = cudaMemset(s.V, 0, rows * d_head * 2);
     if (e == cudaSuccess) e = cudaMemset(s.acc, 0, rows * sizeof(float));
@@ -891,6 +939,7 @@ void h2o_state_destroy(KveH2O *h) {
     cudaFree(s.pos);
     cudaFree(s.nslots);
     cudaFree(s.hole);
+    cudaFree(s.prefill_part);
     delete h;
 }
 

@@ -535,17 +535,10 @@ cudaError_t launch_h2o_prefill(H2OState &s, const void *K, const void *V, const 
                                cudaStream_t st) {
     int keep_k = (int)floor((double)s.frac * (double)P);
     if (keep_k > P) keep_k = P;
-    // partial prefill scores [units][parts][P], stream-ordered scratch freed after the compression
-    float *acc_tmp = nullptr;
-    cudaError_t e =
-        cudaMallocAsync(&acc_tmp, sizeof(float) * (size_t)s.units * kColsumTcParts * P, st);
-    if (e != cudaSuccess) return e;
-    if (s.dtype == KVE_F16)
-        e = prefill_t<__half>(s, K, V, Q, P, keep_k, acc_tmp, st);
-    else
-        e = prefill_t<__nv_bfloat16>(s, K, V, Q, P, keep_k, acc_tmp, st);
-    const cudaError_t ef = cudaFreeAsync(acc_tmp, st);
-    return e != cudaSuccess ? e : ef;
+    // partial prefill scores [units][parts][P] go to the state's preallocated scratch (sized for
+    // P = max_len when the state was created): the prefill allocates nothing
+    if (s.dtype == KVE_F16) return prefill_t<__half>(s, K, V, Q, P, keep_k, s.prefill_part, st);
+    return prefill_t<__nv_bfloat16>(s, K, V, Q, P, keep_k, s.prefill_part, st);
 }
 
 cudaError_t launch_h2o_step(H2OState &s, const void *q, const void *k, const void *v, void *out,

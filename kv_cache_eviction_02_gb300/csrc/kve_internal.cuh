@@ -6,6 +6,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <utility>
+#include <vector>
+
 #include "../../include/kvevict.h"
 
 namespace kve {
@@ -28,7 +32,16 @@ inline size_t dtype_size(int dt) { return dt == KVE_F32 ? 4 : 2; }
 // Bit 0: a bounded wait on an mbarrier gave up. The host reads and clears it in kve_check_device.
 // Bit 1: a token id outside [0, vocab) reached the counter-causal logit kernel.
 enum : unsigned { KVE_DEVERR_TIMEOUT = 1u, KVE_DEVERR_BADINDEX = 2u };
-unsigned *device_error_word();  // device address of the word (per device, set up lazily)
+unsigned *device_error_word();  // device address of the word in the current context
+
+// Device address of a __device__ variable (its host-side stand-in `symbol`) in the calling
+// thread's current context, looked up with cudaGetSymbolAddress once per context and cached by
+// the driver's context id. nullptr if the lookup fails.
+struct SymbolCache {
+    std::mutex mu;
+    std::vector<std::pair<unsigned long long, void *>> entries;
+};
+void *context_symbol_address(const void *symbol, SymbolCache &cache);
 
 // Records a message for kve_last_error() on the calling thread and returns `code`.
 int report_error(int code, const char *fmt, ...);
@@ -72,8 +85,25 @@ struct LorekvWorkspace {
     size_t qconst;             // per-query {-lse2, c, weight, 0} [units][Qu] float4
     size_t rel_part;           // reliability partials [S][MT][rel_splits] float4
     size_t cosm;               // cosine sums [S][L*Hq][M][M] f32
+    // peaked pairs (a > kPeakTau): per-split maximum logit over non-protected tokens [units]
+    // [nsplit][Qu] (log2 domain), the largest non-protected probability a_max [units][Qu], and
+    // per query the count, tokens and weighted exact scores of the pairs the scoring kernels
+    // left out [units][Qu] / [units][Qu][kPeakSlots]
+    size_t part_mx, amax, pk_cnt, pk_tok, pk_e;
     size_t total;
 };
+
+// Peaked pairs. Where a_{q,i} is close to 1, o_q is close to v_i and the expanded quadratic form
+// ||L^T v||^2 - 2 v.(G o) + o^T G o cancels, 1 - a cancels, and the bf16 rounding of the
+// attention weights in o no longer averages out against the small ||L^T (v_i - o_q)||. Pairs
+// with a > kPeakTau are therefore left out by the scoring kernels, recorded (at most
+// kPeakSlots per query: more than three tokens cannot exceed 1/4) and evaluated exactly by
+// peak_fix_kernel in difference form. The tensor-core scoring kernel only checks pairs in CTAs
+// whose queries have a_max > kPeakFlag (a margin below kPeakTau), so unpeaked workloads pay
+// nothing for it.
+constexpr float kPeakTau = 0.25f;
+constexpr float kPeakFlag = 0.125f;
+constexpr int kPeakSlots = 4;
 
 bool lorekv_dims(const KveShape *sh, const KveLorekvParams *p, LorekvDims *D, const char **why);
 bool tc_supported(const LorekvDims &D);  // tensor-core kernels cover this shape
@@ -96,6 +126,10 @@ cudaError_t launch_prep_u(const LorekvDims &D, const float *G, const float *omeg
 cudaError_t launch_scores_simt(const LorekvDims &D, const void *K, const void *V,
                                const void *QW, const void *QL, const float *Lf, void *ws,
                                const LorekvWorkspace &W, float *scores, cudaStream_t st);
+// exact scores of the recorded peaked pairs, then added into scores [units][n] in a fixed order
+cudaError_t launch_peak_fix(const LorekvDims &D, const void *K, const void *V, const void *QW,
+                            const void *QL, const float *Lf, void *ws, const LorekvWorkspace &W,
+                            float *scores, cudaStream_t st);
 cudaError_t launch_select_compact(const LorekvDims &D, const float *scores, const void *K,
                                   const void *V, int32_t *kept_idx, int32_t *kept_len,
                                   void *K_out, void *V_out, int cap, cudaStream_t st);
@@ -112,6 +146,7 @@ struct H2OState {
     int32_t *pos;      // [units][cap], -1 = empty
     int32_t *nslots;   // [units] slots in use (including a hole)
     int32_t *hole;     // [units] free slot left by the last eviction, -1 if none
+    float *prefill_part;  // [units][kColsumTcParts][max_len] partial prefill scores (scratch)
 };
 cudaError_t launch_h2o_prefill(H2OState &s, const void *K, const void *V, const void *Q, int P,
                                cudaStream_t st);

@@ -5,10 +5,11 @@
 // process whose allocator is not available at the call site.
 //
 // The array lives in this file's device image. In host code `g_noalloc_scratch` names a host-side
-// stand-in, not a device address, so its device address is looked up once per device with
-// cudaGetSymbolAddress while that device is current, and that address is what the kernels get.
-#include <mutex>
-
+// stand-in, not a device address, so its device address is looked up with cudaGetSymbolAddress,
+// once per CUDA context (on the first call made while that context is current; cached by the
+// driver's context id, so the primary context of each device, a context made current with the
+// driver API and a context re-created after cudaDeviceReset each get their own), and that
+// address is what the kernels get.
 #include "kve_internal.cuh"
 
 namespace {
@@ -17,8 +18,7 @@ constexpr size_t kNoallocScratchBytes = size_t(64) << 20;  // 64 MiB on every de
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[64] = {nullptr};  // device address of the array, per device ordinal
+kve::SymbolCache g_noalloc_cache;  // device address of the array, per context
 
 }  // namespace
 
@@ -36,25 +36,11 @@ extern "C" int lorekv_score_noalloc(const KveShape *shape, const KveLorekvParams
                                  "lorekv_score_noalloc: this shape needs %zu bytes of scratch; "
                                  "the fixed array holds %zu (use lorekv_score with a workspace)",
                                  need, kNoallocScratchBytes);
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 64)
-        return kve::report_error(KVE_ECUDA, "lorekv_score_noalloc: no current device (%s)",
-                                 cudaGetErrorString(e));
-    void *scratch = nullptr;
-    {
-        std::lock_guard<std::mutex> lk(g_noalloc_mu);
-        if (!g_noalloc_ptr[dev]) {
-            void *p = nullptr;
-            e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-            if (e != cudaSuccess || !p)
-                return kve::report_error(KVE_ECUDA,
-                                         "lorekv_score_noalloc: scratch address lookup failed (%s)",
-                                         cudaGetErrorString(e));
-            g_noalloc_ptr[dev] = p;
-        }
-        scratch = g_noalloc_ptr[dev];
-    }
+    void *scratch = kve::context_symbol_address(
+        reinterpret_cast<const void *>(&g_noalloc_scratch), g_noalloc_cache);
+    if (!scratch)
+        return kve::report_error(KVE_ECUDA, "lorekv_score_noalloc: scratch address lookup failed (%s)",
+                                 cudaGetErrorString(cudaGetLastError()));
     return lorekv_score(shape, params, K, V, Q_W, Q_look, L, G, logits, sampled, scores_out,
                         omega_out, scratch, kNoallocScratchBytes, stream);
 }

@@ -43,7 +43,8 @@ __global__ void __launch_bounds__(256) attn_partial_kernel(const T *__restrict__
                                                            const T *__restrict__ QW,
                                                            const T *__restrict__ QL, LorekvDims D,
                                                            float2 *__restrict__ part_ml,
-                                                           float *__restrict__ part_o) {
+                                                           float *__restrict__ part_o,
+                                                           float *__restrict__ part_mx) {
     constexpr int d = DPL * 32;
     extern __shared__ float sm[];
     float *qs = sm;                       // [kQB][d]
@@ -60,11 +61,12 @@ __global__ void __launch_bounds__(256) attn_partial_kernel(const T *__restrict__
     const int t0 = sp * D.split_len, t1 = min(D.n, t0 + D.split_len);
     const T *Ku = K + (size_t)unit * D.n * d;
     const T *Vu = V + (size_t)unit * D.n * d;
-    float m[4], l[4], o[4][DPL];
+    float m[4], l[4], o[4][DPL], mnp[4];  // mnp: largest visible non-protected logit
     int nvis[4];
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
         m[a] = -INFINITY;
+        mnp[a] = -INFINITY;
         l[a] = 0.f;
         const int qi = qb * kQB + warp * 4 + a;
         nvis[a] = (qi < D.Qu) ? visible_tokens(D, qi) : 0;
@@ -81,6 +83,9 @@ __global__ void __launch_bounds__(256) attn_partial_kernel(const T *__restrict__
         }
         __syncthreads();
         const int tok = base + lane;
+        const bool np_tok = tok >= D.sink && tok < D.n - D.w;
+        // the tile holds sink or window tokens (block-uniform)
+        const bool has_prot = base < D.sink || base + kTT > D.n - D.w;
         float s[4] = {0.f, 0.f, 0.f, 0.f};
         const float *kr = ks + lane * (d + 1);
         const float *qr = qs + (warp * 4) * d;
@@ -94,6 +99,7 @@ __global__ void __launch_bounds__(256) attn_partial_kernel(const T *__restrict__
             const bool valid = tok < t1 && tok < nvis[a];
             const float sv = valid ? s[a] : -INFINITY;
             const float mt = warp_max(sv);
+            mnp[a] = fmaxf(mnp[a], has_prot ? warp_max(np_tok ? sv : -INFINITY) : mt);
             const float mn = fmaxf(m[a], mt);
             if (mn == -INFINITY) continue;  // nothing visible yet
             const float corr = (m[a] == -INFINITY) ? 0.f : exp2f(m[a] - mn);
@@ -115,7 +121,10 @@ __global__ void __launch_bounds__(256) attn_partial_kernel(const T *__restrict__
         const int qi = qb * kQB + warp * 4 + a;
         if (qi >= D.Qu) continue;
         const size_t row = ((size_t)unit * D.nsplit + sp) * D.Qu + qi;
-        if (lane == 0) part_ml[row] = make_float2(m[a], l[a]);
+        if (lane == 0) {
+            part_ml[row] = make_float2(m[a], l[a]);
+            part_mx[row] = mnp[a];
+        }
 #pragma unroll
         for (int c = 0; c < DPL; ++c) part_o[row * d + lane + 32 * c] = o[a][c];
     }
@@ -125,8 +134,11 @@ __global__ void __launch_bounds__(256) attn_partial_kernel(const T *__restrict__
 // fewer. Merges the token splits of the query.
 __global__ void __launch_bounds__(256) combine_kernel(LorekvDims D, const float2 *__restrict__ part_ml,
                                                       const float *__restrict__ part_o,
+                                                      const float *__restrict__ part_mx,
                                                       float *__restrict__ lse2,
                                                       float *__restrict__ o,
+                                                      float *__restrict__ amax,
+                                                      int *__restrict__ pk_cnt,
                                                       float *__restrict__ lse_out,
                                                       float *__restrict__ o_out) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -164,6 +176,11 @@ __global__ void __launch_bounds__(256) combine_kernel(LorekvDims D, const float2
         const float v = mx + log2f(l);
         lse2[row] = v;
         if (lse_out) lse_out[row] = v * kLn2;
+        // a_max over non-protected tokens: flags the queries whose pairs may be peaked
+        float mnp = -INFINITY;
+        for (int sp = 0; sp < D.nsplit; ++sp) mnp = fmaxf(mnp, part_mx[base + (size_t)sp * D.Qu]);
+        amax[row] = mnp > -1e30f ? exp2f(mnp - v) : 0.f;
+        pk_cnt[row] = 0;
     }
 }
 
@@ -266,7 +283,8 @@ __global__ void __launch_bounds__(256) scores_simt_kernel(
     const T *__restrict__ K, const T *__restrict__ V, const T *__restrict__ QW,
     const T *__restrict__ QL, const float *__restrict__ Lf, LorekvDims D,
     const float *__restrict__ lse2, const float *__restrict__ u32, const float *__restrict__ cq,
-    const float *__restrict__ wq, float *__restrict__ scores) {
+    const float *__restrict__ wq, float *__restrict__ scores, int *__restrict__ pk_cnt,
+    int *__restrict__ pk_tok) {
     constexpr int d = DPL * 32;
     extern __shared__ float sm[];
     float *ks = sm;                        // [kTT][d+1]
@@ -337,7 +355,15 @@ __global__ void __launch_bounds__(256) scores_simt_kernel(
                 s = fmaf(qr[k], kr[k], s);
                 vu = fmaf(ur[k], vr[k], vu);
             }
-            const float a = exp2f(s - qc[r]);
+            float a = exp2f(s - qc[r]);
+            if (scored && a > kPeakTau) {  // peaked pair: left out here, evaluated exactly later
+                const size_t row = (size_t)unit * D.Qu + j * D.nq + r;
+                const int slot = atomicAdd(pk_cnt + row, 1);
+                if (slot < kPeakSlots) {
+                    pk_tok[row * kPeakSlots + slot] = tok;
+                    a = 0.f;
+                }
+            }
             const float x = fmaxf(fmaf(-2.f, vu, nv + qc[D.nq + r]), 0.f);
             const float e = a / (1.f - a + D.eps) * sqrtf(x);
             Sacc = fmaf(qc[2 * D.nq + r], e, Sacc);
@@ -356,7 +382,7 @@ __global__ void __launch_bounds__(256) scores_simt_kernel(
 
 template <typename T>
 cudaError_t attn_dispatch(const LorekvDims &D, const void *K, const void *V, const void *QW,
-                          const void *QL, float2 *ml, float *po, cudaStream_t st) {
+                          const void *QL, float2 *ml, float *po, float *mx, cudaStream_t st) {
     const dim3 grid((D.Qu + kQB - 1) / kQB, D.nsplit, D.units);
     const size_t smem = sizeof(float) * (kQB * D.d + 2 * kTT * (D.d + 1));
 #define KVE_ATTN_CASE(DPL)                                                                     \
@@ -364,7 +390,7 @@ cudaError_t attn_dispatch(const LorekvDims &D, const void *K, const void *V, con
         auto kern = attn_partial_kernel<T, DPL>;                                               \
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);    \
         kern<<<grid, 256, smem, st>>>((const T *)K, (const T *)V, (const T *)QW, (const T *)QL, \
-                                      D, ml, po);                                              \
+                                      D, ml, po, mx);                                          \
         break;                                                                                 \
     }
     switch (D.d / 32) {
@@ -380,7 +406,8 @@ cudaError_t attn_dispatch(const LorekvDims &D, const void *K, const void *V, con
 template <typename T>
 cudaError_t scores_dispatch(const LorekvDims &D, const void *K, const void *V, const void *QW,
                             const void *QL, const float *Lf, const float *lse2, const float *u32,
-                            const float *cq, const float *wq, float *scores, cudaStream_t st) {
+                            const float *cq, const float *wq, float *scores, int *pk_cnt,
+                            int *pk_tok, cudaStream_t st) {
     const dim3 grid((D.n + kTT - 1) / kTT, D.units);
     const size_t smem = sizeof(float) * (2 * kTT * (D.d + 1) + 2 * D.nq * D.d + D.d * D.d +
                                          3 * D.nq + 8 * 32);
@@ -389,7 +416,7 @@ cudaError_t scores_dispatch(const LorekvDims &D, const void *K, const void *V, c
         auto kern = scores_simt_kernel<T, DPL>;                                                 \
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);     \
         kern<<<grid, 256, smem, st>>>((const T *)K, (const T *)V, (const T *)QW, (const T *)QL, \
-                                      Lf, D, lse2, u32, cq, wq, scores);                        \
+                                      Lf, D, lse2, u32, cq, wq, scores, pk_cnt, pk_tok);        \
         break;                                                                                  \
     }
     switch (D.d / 32) {
@@ -410,8 +437,9 @@ cudaError_t launch_attention_simt(const LorekvDims &D, const void *K, const void
     char *b = static_cast<char *>(ws);
     float2 *ml = reinterpret_cast<float2 *>(b + W.part_ml);
     float *po = reinterpret_cast<float *>(b + W.part_o);
-    if (D.dtype == KVE_F32) return attn_dispatch<float>(D, K, V, QW, QL, ml, po, st);
-    return attn_dispatch<__nv_bfloat16>(D, K, V, QW, QL, ml, po, st);
+    float *mx = reinterpret_cast<float *>(b + W.part_mx);
+    if (D.dtype == KVE_F32) return attn_dispatch<float>(D, K, V, QW, QL, ml, po, mx, st);
+    return attn_dispatch<__nv_bfloat16>(D, K, V, QW, QL, ml, po, mx, st);
 }
 
 cudaError_t launch_combine(const LorekvDims &D, void *ws, const LorekvWorkspace &W,
@@ -419,8 +447,10 @@ cudaError_t launch_combine(const LorekvDims &D, void *ws, const LorekvWorkspace 
     char *b = static_cast<char *>(ws);
     combine_kernel<<<dim3((D.Qu + 7) / 8, D.units), 256, 0, st>>>(
         D, reinterpret_cast<const float2 *>(b + W.part_ml),
-        reinterpret_cast<const float *>(b + W.part_o), reinterpret_cast<float *>(b + W.lse2),
-        reinterpret_cast<float *>(b + W.o), lse_out, o_out);
+        reinterpret_cast<const float *>(b + W.part_o),
+        reinterpret_cast<const float *>(b + W.part_mx), reinterpret_cast<float *>(b + W.lse2),
+        reinterpret_cast<float *>(b + W.o), reinterpret_cast<float *>(b + W.amax),
+        reinterpret_cast<int *>(b + W.pk_cnt), lse_out, o_out);
     return cudaGetLastError();
 }
 
@@ -467,9 +497,13 @@ cudaError_t launch_scores_simt(const LorekvDims &D, const void *K, const void *V
     const float *u32 = reinterpret_cast<const float *>(b + W.u32);
     const float *cq = reinterpret_cast<const float *>(b + W.cq);
     const float *wq = reinterpret_cast<const float *>(b + W.wq);
+    int *pk_cnt = reinterpret_cast<int *>(b + W.pk_cnt);
+    int *pk_tok = reinterpret_cast<int *>(b + W.pk_tok);
     if (D.dtype == KVE_F32)
-        return scores_dispatch<float>(D, K, V, QW, QL, Lf, lse2, u32, cq, wq, scores, st);
-    return scores_dispatch<__nv_bfloat16>(D, K, V, QW, QL, Lf, lse2, u32, cq, wq, scores, st);
+        return scores_dispatch<float>(D, K, V, QW, QL, Lf, lse2, u32, cq, wq, scores, pk_cnt,
+                                      pk_tok, st);
+    return scores_dispatch<__nv_bfloat16>(D, K, V, QW, QL, Lf, lse2, u32, cq, wq, scores, pk_cnt,
+                                          pk_tok, st);
 }
 
 }  // namespace kve

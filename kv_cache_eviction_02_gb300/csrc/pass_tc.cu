@@ -138,12 +138,12 @@ __global__ void pack_queries_kernel(const __nv_bfloat16 *__restrict__ QW,
     for (int k = threadIdx.x; k < D.d; k += blockDim.x) dst[k] = src[k];
 }
 
-// Per-query constants of the scoring epilogue: {-lse2, c, w, 0}.
+// Per-query constants of the scoring epilogue: {-lse2, c, w, a_max}.
 __global__ void pack_qconst_kernel(const float *__restrict__ lse2, const float *__restrict__ cq,
-                                   const float *__restrict__ wq, long rows,
-                                   float4 *__restrict__ qconst) {
+                                   const float *__restrict__ wq, const float *__restrict__ amax,
+                                   long rows, float4 *__restrict__ qconst) {
     const long r = (long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (r < rows) qconst[r] = make_float4(-lse2[r], cq[r], wq[r], 0.f);
+    if (r < rows) qconst[r] = make_float4(-lse2[r], cq[r], wq[r], amax[r]);
 }
 
 // S_i = sum over query heads of the partial scores (fixed order); 0 for protected tokens.
@@ -164,6 +164,7 @@ struct ScoresArgs {
     float eps, k1;
     const float4 *qconst;
     float *part_s;
+    int *pk_cnt, *pk_tok;  // pairs left out for the exact peaked-pair evaluation
     unsigned *err;
 };
 
@@ -219,6 +220,63 @@ __device__ __forceinline__ void split3_bf16(float v, __nv_bfloat16 *dst0, __nv_b
     *dst0 = a;
     *dst1 = b;
     *dst2 = __float2bfloat16_rn(r);
+}
+
+// The pair terms of one token row against the 64 queries of one head (two per packed FP32
+// instruction): unweighted per-set sums (kFixedSets) or weighted sums into acc2. With kPeak,
+// a pair whose a exceeds tau is left out (a := 0) and recorded for the exact evaluation of
+// peaked pairs; a query takes at most kPeakSlots such tokens (a record that finds the slots
+// full keeps its pair in the sum instead).
+template <bool kFixedSets, bool kPeak>
+__device__ __forceinline__ void score_pairs(const float (&s0)[32], const float (&s1)[32],
+                                            const float (&x0)[32], const float (&x1)[32],
+                                            float nv, uint64_t (&acc2)[8],
+                                            const float2 *qwh, uint64_t k1_2, uint64_t one_2,
+                                            uint64_t neg1_2, float tau, int tok, int *pk_cnt,
+                                            int *pk_tok) {
+    const uint64_t nv_2 = tc::pk2(nv, nv);
+#pragma unroll
+    for (int p = 0; p < 32; ++p) {
+        const float sa = (p < 16) ? s0[2 * p] : s1[2 * p - 32];
+        const float sb = (p < 16) ? s0[2 * p + 1] : s1[2 * p - 31];
+        const float xa = (p < 16) ? x0[2 * p] : x1[2 * p - 32];
+        const float xb = (p < 16) ? x0[2 * p + 1] : x1[2 * p - 31];
+        float ea, eb;
+        tc::upk2(tc::mul2(tc::pk2(sa, sb), k1_2), ea, eb);
+        float aa = tc::ex2_approx(ea), ab = tc::ex2_approx(eb);
+        if (kPeak && (aa > tau || ab > tau)) {
+            if (aa > tau) {
+                const int slot = atomicAdd(pk_cnt + 2 * p, 1);
+                if (slot < kPeakSlots) {
+                    pk_tok[(2 * p) * kPeakSlots + slot] = tok;
+                    aa = 0.f;
+                }
+            }
+            if (ab > tau) {
+                const int slot = atomicAdd(pk_cnt + 2 * p + 1, 1);
+                if (slot < kPeakSlots) {
+                    pk_tok[(2 * p + 1) * kPeakSlots + slot] = tok;
+                    ab = 0.f;
+                }
+            }
+        }
+        const uint64_t a2 = tc::pk2(aa, ab);
+        float ya, yb;
+        tc::upk2(tc::add2(tc::pk2(xa, xb), nv_2), ya, yb);
+        const uint64_t x2 = tc::pk2(fmaxf(ya, 1e-30f), fmaxf(yb, 1e-30f));
+        const uint64_t dd2 = tc::fma2(a2, neg1_2, one_2);
+        float za, zb;
+        tc::upk2(tc::mul2(tc::mul2(x2, dd2), dd2), za, zb);
+        const uint64_t r2 = tc::pk2(tc::rsqrt_approx(za), tc::rsqrt_approx(zb));
+        if (kFixedSets) {  // unweighted; the set's weight is applied once at the end
+            const int slot = p < 16 ? (p & 3) : 4 + ((p - 16) >> 2);
+            acc2[slot] = tc::fma2(tc::mul2(a2, x2), r2, acc2[slot]);
+        } else {
+            const float2 cw = qwh[p];
+            acc2[p & 3] = tc::fma2(tc::mul2(tc::mul2(a2, tc::pk2(cw.x, cw.y)), x2), r2,
+                                   acc2[p & 3]);
+        }
+    }
 }
 
 template <bool kFixedSets>
@@ -279,11 +337,13 @@ __global__ void __launch_bounds__(kScThreads, 1)
         const __nv_bfloat16 one = __float2bfloat16_rn(1.f);
         for (int k = 0; k < 3; ++k) aa[tc::sw32_offset(threadIdx.x, k) / 2] = one;
     }
+    int peaked = 0;  // a query of this CTA has a non-protected pair with a > kPeakFlag
     if (threadIdx.x >= 128 && threadIdx.x < 128 + 64 * SC_HPC) {  // one query each
         const int q = threadIdx.x - 128;                           // B row: head q / 64
         const int hh = q >> 6, r = q & 63;
         float4 c = make_float4(-INFINITY, 0.f, 0.f, 0.f);
         if (hh < nh && r < A.nq) c = A.qconst[(size_t)unit * A.Qu + (size_t)(j0 + hh) * A.nq + r];
+        peaked = c.w > kPeakFlag;
         __nv_bfloat16 *bs = reinterpret_cast<__nv_bfloat16 *>(sm + SC_AUG_S);
         __nv_bfloat16 *bv = reinterpret_cast<__nv_bfloat16 *>(sm + SC_AUG_V);
         const uint32_t o0 = tc::sw32_offset(q, 0) / 2, o1 = tc::sw32_offset(q, 1) / 2,
@@ -299,7 +359,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
         }
     }
     tc::fence_proxy_async_smem();  // generic-proxy writes -> MMA operand reads
-    __syncthreads();
+    const int peak_cta = __syncthreads_or(peaked);
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
@@ -413,6 +473,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
         const int row = lg * 32 + lane;
         const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
         float *out = A.part_s + ((size_t)unit * A.g + j0 + hh) * A.n;
+        const size_t qrow0 = (size_t)unit * A.Qu + (size_t)(j0 + hh) * A.nq;
+        int *pk_cnt = A.pk_cnt + qrow0, *pk_tok = A.pk_tok + qrow0 * kPeakSlots;
         const float one_eps = 1.f + A.eps;
         const float2 *qwh = qw + hh * 32;
         const uint64_t k1_2 = tc::pk2(A.k1, A.k1);
@@ -473,32 +535,16 @@ __global__ void __launch_bounds__(kScThreads, 1)
             // e = a sqrt(x) / (1 - a + eps) for two queries per packed FP32 instruction, with
             // a = exp2(S' k1) (S' = s - lse2/k1), x = ||L^T v||^2 + X' (X' = c - 2 v.u) and
             // sqrt(x) / dd = x rsqrt(x dd^2)
-            const uint64_t nv_2 = tc::pk2(nv, nv);
+            const int tok = (t_begin + i) * 128 + row;
             uint64_t acc2[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-#pragma unroll
-            for (int p = 0; p < 32; ++p) {
-                const float sa = (p < 16) ? s0[2 * p] : s1[2 * p - 32];
-                const float sb = (p < 16) ? s0[2 * p + 1] : s1[2 * p - 31];
-                const float xa = (p < 16) ? x0[2 * p] : x1[2 * p - 32];
-                const float xb = (p < 16) ? x0[2 * p + 1] : x1[2 * p - 31];
-                float ea, eb;
-                tc::upk2(tc::mul2(tc::pk2(sa, sb), k1_2), ea, eb);
-                const uint64_t a2 = tc::pk2(tc::ex2_approx(ea), tc::ex2_approx(eb));
-                float ya, yb;
-                tc::upk2(tc::add2(tc::pk2(xa, xb), nv_2), ya, yb);
-                const uint64_t x2 = tc::pk2(fmaxf(ya, 1e-30f), fmaxf(yb, 1e-30f));
-                const uint64_t dd2 = tc::fma2(a2, neg1_2, one_2);
-                float za, zb;
-                tc::upk2(tc::mul2(tc::mul2(x2, dd2), dd2), za, zb);
-                const uint64_t r2 = tc::pk2(tc::rsqrt_approx(za), tc::rsqrt_approx(zb));
-                if (kFixedSets) {  // unweighted; the set's weight is applied once at the end
-                    const int slot = p < 16 ? (p & 3) : 4 + ((p - 16) >> 2);
-                    acc2[slot] = tc::fma2(tc::mul2(a2, x2), r2, acc2[slot]);
-                } else {
-                    const float2 cw = qwh[p];
-                    acc2[p & 3] = tc::fma2(tc::mul2(tc::mul2(a2, tc::pk2(cw.x, cw.y)), x2), r2,
-                                           acc2[p & 3]);
-                }
+            if (peak_cta) {
+                // pairs of non-protected tokens with a > kPeakTau are left out and recorded
+                const float tau = (tok >= A.sink && tok < A.n - A.w) ? kPeakTau : INFINITY;
+                score_pairs<kFixedSets, true>(s0, s1, x0, x1, nv, acc2, qwh, k1_2, one_2, neg1_2,
+                                              tau, tok, pk_cnt, pk_tok);
+            } else {
+                score_pairs<kFixedSets, false>(s0, s1, x0, x1, nv, acc2, qwh, k1_2, one_2, neg1_2,
+                                               INFINITY, tok, pk_cnt, pk_tok);
             }
             float acc = 0.f;
             if (kFixedSets) {
@@ -524,7 +570,6 @@ __global__ void __launch_bounds__(kScThreads, 1)
                     acc += u + v;
                 }
             }
-            const int tok = (t_begin + i) * 128 + row;
             if (tok < A.n) out[tok] = (tok >= A.sink && tok < A.n - A.w) ? acc : 0.f;
         }
     }
@@ -537,10 +582,11 @@ __global__ void __launch_bounds__(kScThreads, 1)
 
 // ---- attention-statistics kernel ------------------------------------------------------------------
 struct AttnArgs {
-    int n, Qu, nq, w, window_causal, nsplit, split_len, nqp;
+    int n, Qu, nq, w, sink, window_causal, nsplit, split_len, nqp;
     float k1;
     float2 *part_ml;
     float *part_o;
+    float *part_mx;  // largest visible non-protected logit of the split (log2 domain)
     unsigned *err;
 };
 
@@ -706,6 +752,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         const uint32_t s_col = tmem + lane_off + t * 128;
         const uint32_t o_col = tmem + lane_off + 256 + t * 128;
         float m_used = kNoMax, l = 0.f;  // finite sentinel: exp2(x - kNoMax) = 0
+        float m_np = kNoMax;             // true maximum over visible non-protected tokens
         bool ok = true;
         for (int i = 0; i < ntl; ++i) {
             if (!tc::mbar_wait_warp(&s_full[t], i & 1, abort_flag, A.err)) {
@@ -733,6 +780,24 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) m4[c] = tc::max3(m4[c], s[c][e], s[c][e + 1]);
                 mt = tc::max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
+            }
+            {
+                // the largest a over non-protected tokens flags queries with peaked pairs; only
+                // the tiles holding sink or window tokens (CTA-uniform) need a masked maximum
+                const int tbase = t0 + i * 128;
+                float mnp = mt;
+                if (tbase < A.sink || tbase + 128 > A.n - A.w) {
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int tok = tbase + c * 32 + e;
+                            if (tok >= A.sink && tok < A.n - A.w) m4[c] = fmaxf(m4[c], s[c][e]);
+                        }
+                    mnp = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                }
+                m_np = fmaxf(m_np, mnp * A.k1);
             }
             const float m_new = fmaxf(m_used, mt * A.k1);
             // O is rescaled only when the row maximum grew by more than 2^8 (and O holds data)
@@ -808,7 +873,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                         dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
                 }
             }
-            if (valid_row) A.part_ml[rowi] = make_float2(m_used, l);
+            if (valid_row) {
+                A.part_ml[rowi] = make_float2(m_used, l);
+                A.part_mx[rowi] = m_np;
+            }
         }
     }
     __syncthreads();
@@ -861,6 +929,7 @@ cudaError_t launch_attention_tc(const LorekvDims &D, const void *K, const void *
     A.Qu = D.Qu;
     A.nq = D.nq;
     A.w = D.w;
+    A.sink = D.sink;
     A.window_causal = D.window_causal;
     A.nsplit = D.nsplit;
     A.split_len = D.split_len;
@@ -868,6 +937,7 @@ cudaError_t launch_attention_tc(const LorekvDims &D, const void *K, const void *
     A.k1 = kLog2e / sqrtf((float)D.d);
     A.part_ml = reinterpret_cast<float2 *>(b + W.part_ml);
     A.part_o = reinterpret_cast<float *>(b + W.part_o);
+    A.part_mx = reinterpret_cast<float *>(b + W.part_mx);
     A.err = err;
     cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AT_SMEM);
@@ -891,8 +961,8 @@ cudaError_t launch_scores_tc(const LorekvDims &D, const void *K, const void *V, 
     const long rows_q = (long)D.units * D.Qu;
     pack_qconst_kernel<<<(unsigned)((rows_q + 255) / 256), 256, 0, st>>>(
         reinterpret_cast<const float *>(b + W.lse2), reinterpret_cast<const float *>(b + W.cq),
-        reinterpret_cast<const float *>(b + W.wq), rows_q,
-        reinterpret_cast<float4 *>(b + W.qconst));
+        reinterpret_cast<const float *>(b + W.wq), reinterpret_cast<const float *>(b + W.amax),
+        rows_q, reinterpret_cast<float4 *>(b + W.qconst));
     CUtensorMap tk, tv, tq, tu, tl;
     const uint64_t rows = (uint64_t)D.units * D.n;
     if (!make_tmap_bf16_2d(&tk, K, 128, rows, 64, 128) ||
@@ -919,6 +989,8 @@ cudaError_t launch_scores_tc(const LorekvDims &D, const void *K, const void *V, 
     A.k1 = kLog2e / sqrtf((float)D.d);
     A.qconst = reinterpret_cast<const float4 *>(b + W.qconst);
     A.part_s = reinterpret_cast<float *>(b + W.part_s);
+    A.pk_cnt = reinterpret_cast<int *>(b + W.pk_cnt);
+    A.pk_tok = reinterpret_cast<int *>(b + W.pk_tok);
     A.err = err;
     // the window / trajectory layout of the configured workloads gets compile-time query sets
     const bool fixed_sets = D.w == kSetW && D.M == kSetM && D.T == kSetT;

@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(256) rel_rows_kernel(const float *__restrict__
     RowAcc acc{-INFINITY, 0.f, 0.f};
     for (long v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
         float x = __ldg(z + v);
+        // a -inf logit (a masked token) has p = 0 and adds nothing to the sums (0 log 0 = 0)
+        if (x == -INFINITY) continue;
         if (x > acc.m) {
             float sc = (acc.m == -INFINITY) ? 0.f : expf(acc.m - x);
             acc.a = acc.a * sc + 1.f;

@@ -65,7 +65,7 @@ void kvo_row_stats(long V, const double *z, long y, double *lse, double *H, doub
     for (long v = 0; v < V; ++v) {
         double logp = z[v] - l;
         double p = exp(logp);
-        h -= p * logp;
+        if (p > 0.0) h -= p * logp; /* 0 log 0 = 0: a -inf logit (masked token) adds nothing */
     }
     *lse = l;
     *H = h;

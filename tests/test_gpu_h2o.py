@@ -243,3 +243,26 @@ def test_h2o_prefill_shapes(P, dtype, shape):
             assert torch.equal(Kx[u, slot], hin["K"][bb, l, h, p].cpu()), (u, p)
             assert torch.equal(Vx[u, slot], hin["V"][bb, l, h, p].cpu()), (u, p)
     st.close()
+
+
+def test_h2o_prefill_allocates_nothing():
+    """The state created by h2o_state_create holds the prefill's scratch: a prefill (and a decode
+    step) leaves the device's free memory unchanged. A first state runs once beforehand so that
+    loading the kernels is not counted."""
+    cfg = synth.H2OConfig("prefill_noalloc", "f16", batch=2, L=2, H=8, d=128, prompt=384, steps=2)
+    hin = {k: v.to(_dev()) for k, v in synth.h2o_inputs(cfg, "cpu", steps=2).items()}
+    out = torch.empty(cfg.batch, cfg.L, cfg.H, cfg.d, dtype=torch.float16, device=_dev())
+    states = []
+    for _ in range(2):
+        st = api.h2o_state_create(cfg.batch, cfg.L, cfg.H, cfg.d, cfg.prompt + 2, cfg.budget_frac,
+                                  torch.float16)
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
+        st.prefill(hin["K"], hin["V"], hin["Q"])
+        st.decode_step(hin["q"][0], hin["k"][0], hin["v"][0], out)
+        torch.cuda.synchronize()
+        free1 = torch.cuda.mem_get_info()[0]
+        states.append(st)
+    assert free1 == free0, f"prefill + decode step changed free device memory by {free0 - free1}"
+    for st in states:
+        st.close()

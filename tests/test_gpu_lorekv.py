@@ -311,6 +311,28 @@ def test_output_fidelity_matches_oracle():
     assert float(mean.item()) == pytest.approx(float(cos_g.mean()), rel=1e-5)
 
 
+def test_masked_logits_match_oracle():
+    """Logits of -inf (masked vocabulary entries, common in real decoders) contribute nothing to
+    lse, H and log q: omega and the scores match the oracle, which treats 0 log 0 as 0."""
+    cfg = SMALL["bf16_gqa4_D"]
+    inp = synth.lorekv_inputs(cfg, "cpu")
+    gen = torch.Generator().manual_seed(5)
+    mask = torch.rand(inp["logits"].shape, generator=gen) < 0.3
+    rows = torch.arange(inp["sampled"].numel())
+    mask.view(-1, cfg.vocab)[rows, inp["sampled"].view(-1).long()] = False  # y stays finite
+    mask[..., :3] = True                                                     # a masked prefix
+    inp["logits"] = inp["logits"].masked_fill(mask, float("-inf"))
+    g = {k: v.to(_dev()) for k, v in inp.items()}
+    run = _run_pass(cfg, g)
+    om = run.omega.double().cpu().numpy()
+    assert np.all(np.isfinite(om))
+    S = run.scores.double().cpu().numpy()
+    units = [(0, 0, 0), (1, 1, 1)]
+    for (s, l, kh), r in oracle.lorekv_config_units(cfg, inp, units).items():
+        assert np.allclose(om[s], r["omega"], rtol=OMEGA_RTOL, atol=0), s
+        assert_scores_close(S[_unit_index(cfg, s, l, kh)], r["S"], cfg.dtype, "masked logits")
+
+
 def test_scores_are_deterministic():
     cfg = SMALL["bf16_gqa4_D"]
     g = {k: v.to(_dev()) for k, v in synth.lorekv_inputs(cfg, "cpu").items()}

@@ -49,6 +49,23 @@ def test_centered_score_has_zero_conditional_mean():
         assert abs(H - scipy.stats.entropy(scipy.special.softmax(z))) < 1e-12
 
 
+def test_row_stats_with_masked_logits_equal_the_restricted_vocabulary():
+    """Logits of -inf (masked tokens) have probability 0 and contribute 0 log 0 = 0 to H: the
+    row's lse, H and log q(y) equal those of the row with the masked entries removed."""
+    rng = np.random.default_rng(4)
+    z = 2.0 * rng.standard_normal(300)
+    mask = rng.random(300) < 0.3
+    y = int(np.flatnonzero(~mask)[7])
+    zm = z.copy()
+    zm[mask] = -np.inf
+    got = oracle.row_stats(zm, y)
+    keep = np.flatnonzero(~mask)
+    want = oracle.row_stats(z[keep], int(np.searchsorted(keep, y)))
+    assert np.all(np.isfinite(got))
+    assert np.allclose(got, want, rtol=1e-13, atol=1e-13)
+    assert abs(got[0] - scipy.special.logsumexp(z[keep])) < 1e-12
+
+
 def test_row_stats_invariant_to_logit_shift():
     rng = np.random.default_rng(2)
     z = rng.standard_normal(300)
@@ -225,6 +242,34 @@ def test_projected_deletion_matches_brute_force_deletion(causal):
                             eps=1e-6, window_causal=causal, want=("E",))
     corr = np.where(A > 0, (1 - A) / (1 - A + 1e-6), 0.0)
     assert np.allclose(r2["E"], E_bf * corr, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("target", [0.999, 1 - 1e-7])
+def test_projected_deletion_matches_brute_force_when_one_token_dominates(target):
+    """The peaked regime: one non-protected token takes a of about 0.999 (and 1 - 1e-7) of a
+    query's attention. The oracle's difference form still reproduces brute-force deletion there,
+    where 1 - a and v_i - o_q are small differences of large numbers."""
+    rng = np.random.default_rng(17)
+    M, T = 2, 2
+    K, V, QW, QL, W, Lf = _tiny_unit(rng, M=M, T=T)
+    n, d = K.shape
+    h, qi, p = 1, 5, 9                       # lookahead query 1 of head 1, token 9
+    q = QL[h, qi - QW.shape[1]]
+    s = K @ q / math.sqrt(d)
+    rest = np.delete(np.arange(n), p)
+    R = np.exp(s[rest] - s[rest].max()).sum() * math.exp(s[rest].max())
+    # k_p <- k_p + beta q/|q| so that a_{q,p} = target
+    want = math.log(target / (1 - target) * R)
+    K[p] += (want - s[p]) * math.sqrt(d) / (q @ q) * q
+    E_bf, A = _brute_force_e(K, V, QW, QL, W, 0, M, T)
+    assert abs(A[h, qi, p] - target) < 1e-9
+    r = oracle.lorekv_unit(K, V, QW, QL, Lf, [0.5, 0.5], M=M, T=T, sink=2, lambda_L=1.0,
+                           eps=0.0, window_causal=0, want=("E",))
+    # both sides subtract nearly equal fp64 vectors: brute force o - o_without_i loses digits as
+    # 1/a for tiny a, the difference form v_i - o_q as 1/(1 - a) near a = 1
+    rtol = 1e-10 + 1e-14 / np.maximum(np.minimum(A, 1 - A), 1e-300)
+    assert np.all(np.abs(r["E"] - E_bf) <= rtol * np.abs(E_bf) + 1e-15)
+    assert abs(r["E"][h, qi, p] / E_bf[h, qi, p] - 1) < 1e-14 / (1 - target)
 
 
 def test_aggregation_weights_window_and_trajectories():
