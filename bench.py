@@ -58,6 +58,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-fidelity", action="store_true")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip the other configured workloads (Mistral-16K, Qwen 4x32K, tiny)")
     p.add_argument("--no-cc", action="store_true", help="skip the counter-causal refresh")
     p.add_argument("--only-cc", action="store_true",
                    help="run only the counter-causal refresh and print its JSON (profiling)")
@@ -360,21 +362,14 @@ def run_reference(args):
 # ---------------------------------------------------------------------------------------------
 # native arm
 # ---------------------------------------------------------------------------------------------
-def run_native(args):
+def measure_pass(cfg, g, dev, stream, pg, world, steps, warmup, pk, sample_clocks=None):
+    """Times `steps` eviction passes (lorekv_score + lorekv_select_compact) on inputs `g` already
+    resident in HBM, after `warmup` untimed passes; returns the bench fields of that workload
+    (value, ms per step, HBM roofline, dominant-kernel roofline, stage times) plus the objects
+    the later measurements reuse."""
     import torch
-    from kv_cache_eviction_02_gb300 import api, synth
+    from kv_cache_eviction_02_gb300 import api
 
-    rank, world, local, pg = dist_init(args)
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    cfg = synth.LOREKV_CONFIGS[args.workload]
-    if world > 1:
-        cfg = cfg.replace(seed=cfg.seed + rank)   # each rank scores its own sequence
-    pk = peaks()
-    stream = torch.cuda.current_stream(dev)
-
-    # ---- inputs resident in HBM, per-model preparation (not timed) ----
-    g = synth.lorekv_inputs(cfg, dev)
     pb = api.LorekvProblem.from_config(cfg)
     Lf = torch.empty(cfg.L, cfg.Hq, cfg.d, cfg.d, device=dev)
     G = torch.empty_like(Lf)
@@ -388,12 +383,12 @@ def run_native(args):
     torch.cuda.synchronize(dev)
     prepare_wo_ms = pw0.elapsed_time(pw1)
     run = api.LorekvPass(pb, dev)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         run.run(g, Lf, G)
     api.kve_check_device()
     torch.cuda.synchronize(dev)
 
-    # ---- timed region: K passes, inputs (17 GB) larger than L2 ----
+    # ---- timed region ----
     api.kve_profile_enable(True)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
@@ -401,12 +396,13 @@ def run_native(args):
     torch.cuda.synchronize(dev)
     # an event between consecutive steps as well, for the per-step spread (the steps still run
     # back to back; the first and last events bracket the timed region)
-    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(max(0, args.steps - 1))]
-    with ClockSampler(local) as clk:
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(max(0, steps - 1))]
+    clk = sample_clocks if sample_clocks is not None else _NoClock()
+    with clk:
         ev0.record(stream)
-        for k in range(args.steps):
+        for k in range(steps):
             run.run(g, Lf, G)
-            if k + 1 < args.steps:
+            if k + 1 < steps:
                 step_ev[k].record(stream)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
@@ -416,7 +412,7 @@ def run_native(args):
     api.kve_profile_enable(False)
     prof = api.kve_profile_report()
     api.kve_check_device()
-    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = ev0.elapsed_time(ev1) / steps
     ms = max_over_ranks(pg, ms, dev)
     tokens_per_step = cfg.units * cfg.n
     value = whole_job_value(tokens_per_step, world, ms)
@@ -436,10 +432,10 @@ def run_native(args):
     src = ("kv_cache_eviction_02_gb300/csrc/pass_tc.cu" if tensor
            else "kv_cache_eviction_02_gb300/csrc/pass_simt.cu")
     traffic = None
-    if dom in NCU_TRAFFIC and NCU_TRAFFIC[dom][1] == src_hash(src):
+    if cfg.name == WORKLOAD and dom in NCU_TRAFFIC and NCU_TRAFFIC[dom][1] == src_hash(src):
         traffic = NCU_TRAFFIC[dom][0]
     if flops is not None and tensor:
-        # a ~20 ms step timed for well under a second: the burst bf16 figure applies
+        # a step timed for well under a second: the burst bf16 figure applies
         ach = flops / (dom_ms / 1e3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "traffic": traffic,
@@ -464,33 +460,72 @@ def run_native(args):
     hbm_achieved = alg_bytes / (ms / 1e3) / 1e9
     pass_mma_flops = ((attention_algorithmic_flops_per_token_unit(cfg)
                        + scores_implemented_flops_per_token_unit(cfg)) * tokens_per_step)
-    stages = {k: {"ms_per_step": v["ms"] / args.steps, "kernels": v["kernels"]}
+    stages = {k: {"ms_per_step": v["ms"] / steps, "kernels": v["kernels"]}
               for k, v in prof.items()}
+    out = {"value": value, "unit": UNIT, "ms_per_step": ms, "steps": steps, "warmup": warmup,
+           "dtype": cfg.dtype,
+           "workload": f"{cfg.name}: {cfg.S} seq x {cfg.L} layers x {cfg.Hq}/{cfg.Hkv} "
+                       f"heads, d_head {cfg.d}, d_model {cfg.d_model}, n {cfg.n}, "
+                       f"vocab {cfg.vocab}, w {cfg.w}, M {cfg.M}, T {cfg.T}, "
+                       f"B {cfg.B}, chunk {cfg.chunk}, sink {cfg.sink}",
+           "units": cfg.units, "kv_tokens_per_step": tokens_per_step,
+           "hbm_roofline": {"algorithmic_bytes": alg_bytes, "achieved_gbs": hbm_achieved,
+                            "peak_gbs": pk["hbm_gbs"], "frac": hbm_achieved / pk["hbm_gbs"],
+                            "peak_source": pk["source"],
+                            # the pass is a dense contraction: at the bf16 burst its MMA work
+                            # alone takes t_min, which caps the HBM fraction
+                            "ceiling_frac": (alg_bytes / (pass_mma_flops / (pk["bf16_tflops"] * 1e12))
+                                             / 1e9 / pk["hbm_gbs"]) if tensor else None,
+                            "pass_mma_flops": pass_mma_flops if tensor else None},
+           "prepare_wo_ms": prepare_wo_ms,
+           "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms),
+                       "max": max(step_ms)},
+           "roofline": roof, "stages": stages, "gpu_launches": gpu_launches}
+    return out, run, Lf, G
 
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+
+class _NoClock:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+
+# the other configured workloads, reported beside the headline (name: timed steps)
+OTHER_WORKLOADS = {"mistral": 20, "qwen": 6, "tiny": 50}
+
+
+def run_native(args):
+    import torch
+    from kv_cache_eviction_02_gb300 import api, synth
+
+    rank, world, local, pg = dist_init(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = synth.LOREKV_CONFIGS[args.workload]
+    if world > 1:
+        cfg = cfg.replace(seed=cfg.seed + rank)   # each rank scores its own sequence
+    pk = peaks()
+    stream = torch.cuda.current_stream(dev)
+
+    # ---- inputs resident in HBM (17 GB per pass for the 128K workload: larger than L2) ----
+    g = synth.lorekv_inputs(cfg, dev)
+    clk = ClockSampler(local)   # nvidia-smi sampling during the timed passes only
+    m, run, Lf, G = measure_pass(cfg, g, dev, stream, pg, world, args.steps, args.warmup, pk,
+                                 sample_clocks=clk)
+    alg_bytes = m["hbm_roofline"]["algorithmic_bytes"]
+    line = {"metric": METRIC, "value": m["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": cfg.dtype, "data": "synthetic",
-            "config": {"workload": f"{cfg.name}: {cfg.S} seq x {cfg.L} layers x {cfg.Hq}/{cfg.Hkv} "
-                                   f"heads, d_head {cfg.d}, d_model {cfg.d_model}, n {cfg.n}, "
-                                   f"vocab {cfg.vocab}, w {cfg.w}, M {cfg.M}, T {cfg.T}, "
-                                   f"B {cfg.B}, chunk {cfg.chunk}, sink {cfg.sink}",
-                       "units_per_gpu": cfg.units, "kv_tokens_per_step_per_gpu": tokens_per_step,
+            "config": {"workload": m["workload"],
+                       "units_per_gpu": cfg.units, "kv_tokens_per_step_per_gpu": m["kv_tokens_per_step"],
                        "l2": f"inputs larger than L2 ({alg_bytes / 1e9:.1f} GB per pass)",
                        "parallelism": f"replicas: {world} x independent sequence"},
-            "hbm_roofline": {"algorithmic_bytes": alg_bytes, "achieved_gbs": hbm_achieved,
-                             "peak_gbs": pk["hbm_gbs"], "frac": hbm_achieved / pk["hbm_gbs"],
-                             "peak_source": pk["source"],
-                             # the pass is a dense contraction: at the bf16 burst its MMA work
-                             # alone takes t_min, which caps the HBM fraction
-                             "ceiling_frac": (alg_bytes / (pass_mma_flops / (pk["bf16_tflops"] * 1e12))
-                                              / 1e9 / pk["hbm_gbs"]) if tensor else None,
-                             "pass_mma_flops": pass_mma_flops if tensor else None},
-            "prepare_wo_ms": prepare_wo_ms,
-            "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms),
-                        "max": max(step_ms)},
-            "roofline": roof, "stages": stages, "gpu_launches": gpu_launches,
-            "clocks": clk.summary()}
+            "hbm_roofline": m["hbm_roofline"], "prepare_wo_ms": m["prepare_wo_ms"],
+            "step_ms": m["step_ms"], "roofline": m["roofline"], "stages": m["stages"],
+            "gpu_launches": m["gpu_launches"], "clocks": clk.summary()}
 
     # ---- end to end through the public API with host buffers ----
     if not args.no_e2e:
@@ -500,6 +535,20 @@ def run_native(args):
     del g
     torch.cuda.empty_cache()
 
+    if not args.no_workloads:
+        line["workloads"] = {}
+        for name, steps in OTHER_WORKLOADS.items():
+            if name == cfg.name:
+                continue
+            wc = synth.LOREKV_CONFIGS[name]
+            if world > 1:
+                wc = wc.replace(seed=wc.seed + rank)
+            wg = synth.lorekv_inputs(wc, dev)
+            wm, wrun, _, _ = measure_pass(wc, wg, dev, stream, pg, world, steps,
+                                          max(3, args.warmup), pk)
+            line["workloads"][name] = wm
+            del wg, wrun
+            torch.cuda.empty_cache()
     if not args.no_h2o:
         line["h2o"] = bench_h2o(dev, stream, pg, world, args, pk)
     if not args.no_cc:

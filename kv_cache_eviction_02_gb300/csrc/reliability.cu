@@ -95,12 +95,14 @@ __global__ void __launch_bounds__(128) rel_cos_kernel(const T *__restrict__ QL, 
     }
 }
 
-// grid S, block 64 (one thread per logits row; MT <= 64). Fixed-order merges, double precision.
+// grid S, block 64 (one thread per logits row; MT <= 64). Fixed-order merges, double precision;
+// the disagreement sums over the L*Hq query heads are split over the 64 threads (head lh goes to
+// thread lh % 64) and the 64 partial sums added in thread order.
 __global__ void rel_final_kernel(const float *__restrict__ logits, const int32_t *__restrict__ y,
                                  const float4 *__restrict__ part, const float *__restrict__ cosm,
                                  int M, int Tn, long vocab, int splits, int LH, float beta,
                                  float gamma, float lambda_D, float *__restrict__ omega) {
-    __shared__ double c_s[64], h_s[64], R_s[32];
+    __shared__ double c_s[64], h_s[64], R_s[32], red[64], dsum[32];
     const int s = blockIdx.x, u = threadIdx.x, MT = M * Tn;
     if (u < MT) {
         const float4 *p = part + ((size_t)s * MT + u) * splits;
@@ -124,17 +126,30 @@ __global__ void rel_final_kernel(const float *__restrict__ logits, const int32_t
         h_s[u] = H;
     }
     __syncthreads();
+    const bool disagree = lambda_D != 0.f && M > 1;
+    if (disagree) {
+        for (int mm = 0; mm < M; ++mm) {
+            double acc = 0.0;
+            for (int lh = u; lh < LH; lh += blockDim.x)
+                for (int m2 = 0; m2 < M; ++m2)
+                    if (m2 != mm) acc += cosm[(((size_t)s * LH + lh) * M + mm) * M + m2];
+            red[u] = acc;
+            __syncthreads();
+            if (u == 0) {
+                double t = 0.0;
+                for (int k = 0; k < (int)blockDim.x; ++k) t += red[k];
+                dsum[mm] = t;
+            }
+            __syncthreads();
+        }
+    }
     if (u == 0) {
         double D[32], Dh[32];
         for (int mm = 0; mm < M; ++mm) Dh[mm] = 0.0;
-        if (lambda_D != 0.f && M > 1) {
+        if (disagree) {
             double mean = 0.0;
             for (int mm = 0; mm < M; ++mm) {
-                double acc = 0.0;
-                for (int lh = 0; lh < LH; ++lh)
-                    for (int m2 = 0; m2 < M; ++m2)
-                        if (m2 != mm) acc += cosm[(((size_t)s * LH + lh) * M + mm) * M + m2];
-                D[mm] = 1.0 - acc / ((double)(M - 1) * LH);
+                D[mm] = 1.0 - dsum[mm] / ((double)(M - 1) * LH);
                 mean += D[mm];
             }
             mean /= M;

@@ -110,7 +110,15 @@ def test_attention_statistics_match_oracle(name):
         o_ref = r["o"].reshape(-1, cfg.d)
         assert np.allclose(lse[ui], lse_ref, rtol=0, atol=tol * np.maximum(1, np.abs(lse_ref)).max())
         err = np.linalg.norm(o[ui] - o_ref, axis=1)
-        assert np.all(err <= tol * np.linalg.norm(o_ref, axis=1) + 1e-6), (name, err.max())
+        if cfg.dtype == "f32":
+            assert np.all(err <= tol * np.linalg.norm(o_ref, axis=1) + 1e-6), (name, err.max())
+        else:
+            # bf16: every a_j reaches the tensor cores rounded to bf16 (relative error uniform in
+            # [-2^-9, 2^-9]), so |o_gpu - o| has an RMS of 2^-9/sqrt(3) sqrt(sum_j a_j^2 |v_j|^2);
+            # allow 4 sigma plus fp32 accumulation
+            sigma = 2.0 ** -9 / np.sqrt(3.0) * _attention_weighted_vnorm(cfg, u, lse_ref)
+            bound = 4.0 * sigma + 1e-5 * np.linalg.norm(o_ref, axis=1) + 1e-6
+            assert np.all(err <= bound), (name, float((err / bound).max()))
 
 
 def _run_pass(cfg, g):
