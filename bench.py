@@ -42,7 +42,13 @@ WORKLOAD = "llama"        # the 128K-context configuration the metric is quoted 
 # scores_tc_kernel: 2.208 GB read + 0.068 GB written per launch on the Mistral-7B-shaped workload
 # (n = 16384, ncu --set full), scaled by the 8x token count of the 128K workload (every term of the
 # traffic is proportional to the tokens scored).
-NCU_TRAFFIC = {"scores": (8 * (2.207931e9 + 0.068153e9), "60571dc18ccf0bef")}
+NCU_TRAFFIC = {"scores": (8 * (2.207626e9 + 0.067719e9), "0dedb9c82af682a6")}
+# h2o_step_kernel on the OPT-30B shape at batch 8 (ncu, decode steps 21-23 after the 512-token
+# prompt): 1.2094 GB read + 0.0268 GB written per launch against 1.2189 GB of algorithmic bytes
+# (retained K/V rows, accumulated scores and positions, q/k/v/out): DRAM traffic is 1.014 x the
+# algorithmic bytes, a ratio that holds at any batch and length (every term grows with the units
+# and the retained rows), applied to the batch-64 launches.
+NCU_TRAFFIC_H2O = (1.0146, "93a5caf6cc381a20")
 # cc_attn_tc_kernel on the n = 4096 counter-causal workload (ncu --set full, one launch):
 # 37.807 MB read + 0.233 MB written
 NCU_TRAFFIC_CC = {("cc_attention", "qwen7b_4096"): (37.80736e6 + 0.23296e6, "741c9d25cbda615d")}
@@ -682,10 +688,17 @@ def e2e_lorekv(cfg, g, run, Lf, G, dev, stream, pg, world, args):
         nch = cfg.L // cl
         scores = run.scores  # every chunk writes its slice of the full-size outputs
 
-        def one():
+        # per-chunk timing of one instrumented step: copy start/end on the copy stream, pass
+        # start/end on the compute stream (timing events; recorded only when `marks` is given)
+        def one(marks=None):
             start_ev.record(stream)
+            if marks is not None:
+                marks["t0"].record(stream)
             cs.wait_event(start_ev)
-            with torch.cuda.stream(stream):
+            # the logits and ids go first on the copy stream: the pass of chunk 0 waits on the
+            # copy stream's event, which covers them (a copy queued on the compute stream behind
+            # the copy engine's chunk copies would hold chunk 0's pass until the next chunk's copy)
+            with torch.cuda.stream(cs):
                 for k in ("logits", "sampled"):
                     small[k].copy_(host[k], non_blocking=True)
             for c in range(nch):
@@ -693,10 +706,16 @@ def e2e_lorekv(cfg, g, run, Lf, G, dev, stream, pg, world, args):
                 if c >= 2:
                     cs.wait_event(done[b])  # chunk c - 2 has finished with buffer b
                 with torch.cuda.stream(cs):
+                    if marks is not None:
+                        marks["copy"][c][0].record(cs)
                     for k in layered:
                         dev_in[b][k].copy_(host[k][:, c * cl:(c + 1) * cl], non_blocking=True)
                     copied[b].record(cs)
+                    if marks is not None:
+                        marks["copy"][c][1].record(cs)
                 stream.wait_event(copied[b])
+                if marks is not None:
+                    marks["pass"][c][0].record(stream)
                 x = dev_in[b]
                 u0, u1 = c * upc, (c + 1) * upc
                 sl = slice(c * cl, (c + 1) * cl)
@@ -707,6 +726,8 @@ def e2e_lorekv(cfg, g, run, Lf, G, dev, stream, pg, world, args):
                                           run.kept_len[u0:u1], run.K_out[u0:u1],
                                           run.V_out[u0:u1], None, stream.cuda_stream)
                 done[b].record(stream)
+                if marks is not None:
+                    marks["pass"][c][1].record(stream)
             with torch.cuda.stream(stream):  # the step's results, read back once
                 for t, h in zip(outs, host_out):
                     h.copy_(t, non_blocking=True)
@@ -746,6 +767,25 @@ def e2e_lorekv(cfg, g, run, Lf, G, dev, stream, pg, world, args):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     ms = max_over_ranks(pg, e0.elapsed_time(e1) / steps, dev)
+    timeline = None
+    if chunked:  # one more step, instrumented: where the step's time goes, chunk by chunk
+        ev = lambda: torch.cuda.Event(enable_timing=True)
+        marks = {"t0": ev(), "copy": [(ev(), ev()) for _ in range(nch)],
+                 "pass": [(ev(), ev()) for _ in range(nch)]}
+        one(marks)
+        torch.cuda.synchronize(dev)
+        t0 = marks["t0"]
+        per = [float(marks["copy"][c][0].elapsed_time(marks["copy"][c][1])) for c in range(nch)]
+        chunk_bytes = sum(host[k][:, :cl].numel() * host[k].element_size() for k in layered)
+        timeline = {
+            "chunk_bytes": chunk_bytes,
+            "copy_ms": [[round(t0.elapsed_time(a), 3), round(t0.elapsed_time(b), 3)]
+                        for a, b in marks["copy"]],
+            "pass_ms": [[round(t0.elapsed_time(a), 3), round(t0.elapsed_time(b), 3)]
+                        for a, b in marks["pass"]],
+            "copy_gbs": [round(chunk_bytes / (x / 1e3) / 1e9, 1) for x in per],
+            "note": "ms from the step's start; copy: copy stream, pass: compute stream",
+        }
     del host, dev_in
     os.sched_setaffinity(0, old_aff)
     res = {"value": cfg.units * cfg.n * world / (ms / 1e3), "unit": UNIT,
@@ -756,6 +796,7 @@ def e2e_lorekv(cfg, g, run, Lf, G, dev, stream, pg, world, args):
     if chunked:
         res["issue"] = (f"{cfg.L // cl} chunks of {cl} layers: the next chunk's host-to-device "
                         "copy overlaps the current chunk's pass (copy stream + compute stream)")
+        res["timeline"] = timeline
     res["host_buffers"] = (f"pinned, allocated from the GPU's local CPUs ({len(local)} CPUs)"
                            if local else "pinned (GPU-local CPUs unknown)")
     return res
@@ -881,7 +922,10 @@ def bench_h2o(dev, stream, pg, world, args, pk):
                       f"prompt {cfg.prompt}, {cfg.steps} decode steps, budget 20%, fp16",
             "roofline": {"kernel": "h2o_step", "bound": "hbm", "achieved": ach,
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
-                         "traffic": None, "bytes_per_launch": per_step_bytes}}
+                         "traffic": (NCU_TRAFFIC_H2O[0] * per_step_bytes
+                                     if NCU_TRAFFIC_H2O[1] == src_hash("kv_cache_eviction_02_gb300/csrc/h2o.cu")
+                                     else None),
+                         "bytes_per_launch": per_step_bytes}}
 
 
 # Counter-causal refresh latency of the fast single-layer variant on the page's own setup (Qwen2.5-

@@ -70,8 +70,11 @@ def _check_prefill(ex, units, orc, cfg, hin):
 
 
 def _advance(o, q, k, v, kept_gpu, tn, frac, what):
-    """One oracle step teacher-forced to the GPU's retained set; returns the oracle output."""
+    """One oracle step teacher-forced to the GPU's retained set; returns the oracle output and
+    the magnitude sum_j p_j |v_j| of its terms."""
     o_ref, _, pre = o.step(q, k, v, evict=False)
+    p, _ = oracle.h2o_attend(o.K, o.V, q)
+    mag = p @ np.abs(o.V)
     k_t, r_t = oracle.h2o_budget(tn, frac)
     pre_pos = pre["pos"].tolist()
     gone = [p for p in pre_pos if p not in kept_gpu]
@@ -85,13 +88,19 @@ def _advance(o, q, k, v, kept_gpu, tn, frac, what):
         assert gone[0] < tn - r_t, f"{what}: evicted a protected recent token"
         assert g_acc <= accs.min() * (1 + 1e-3) + 1e-6 * pre["acc"].max(), what
     o.adopt(sorted(kept_gpu))
-    return o_ref
+    return o_ref, mag
 
 
-def _check_out(o_gpu, o_ref, what):
+def _check_out(o_gpu, o_ref, mag, what, half_ulp=2.0 ** -11):
+    """attn_out is written in the state's 16-bit type (fp16 here): each component carries that
+    rounding (half an ulp, 2^-11 relative, plus the fp16 subnormal spacing); the fp32
+    accumulation and exponentials add at most 1e-5 of the terms' magnitude
+    mag_k = sum_j p_j |v_jk|. Both stay inside the rel 2e-3 budget wherever |o_k| is not a
+    small difference of large terms."""
     err = np.abs(o_gpu - o_ref)
-    lim = OUT_RTOL * np.maximum(np.abs(o_ref), 0.05 * np.abs(o_ref).max())
-    assert np.all(err <= lim), (what, float(err.max()))
+    lim = half_ulp * np.abs(o_ref) + 1e-5 * mag + 2.0 ** -24
+    assert np.all(err <= lim), (what, float((err / lim).max()))
+    assert np.all(err <= OUT_RTOL * np.abs(o_ref) + 1e-5 * mag + 2.0 ** -24), what
 
 
 def _teacher_forced_run(cfg, hin, units, steps, check_kv=True):
@@ -119,9 +128,9 @@ def _teacher_forced_run(cfg, hin, units, steps, check_kv=True):
         for u in units:
             b, l, h = _unit_coords(cfg, u)
             kept_gpu = set(pos[u][pos[u] >= 0].tolist())
-            o_ref = _advance(orc[u], q[b, l, h], k[b, l, h], v[b, l, h], kept_gpu, tn,
-                             cfg.budget_frac, (t, u))
-            _check_out(o_gpu[u], o_ref, (t, u))
+            o_ref, mag = _advance(orc[u], q[b, l, h], k[b, l, h], v[b, l, h], kept_gpu, tn,
+                                  cfg.budget_frac, (t, u))
+            _check_out(o_gpu[u], o_ref, mag, (t, u))
         _check_state(ex, units, orc, f"step {t}")
         if check_kv:
             Kx, Vx = ex["K"].cpu(), ex["V"].cpu()
@@ -193,9 +202,9 @@ def test_h2o_full_size_sampled_units():
         for i, u in enumerate(units):
             b, l, h = _unit_coords(cfg, u)
             kept_gpu = set(pos_c[u][pos_c[u] >= 0].tolist())
-            o_ref = _advance(orc[u], q[b, l, h], k[b, l, h], v[b, l, h], kept_gpu, tn,
-                             cfg.budget_frac, (t, u))
-            _check_out(o_gpu[i], o_ref, (t, u))
+            o_ref, mag = _advance(orc[u], q[b, l, h], k[b, l, h], v[b, l, h], kept_gpu, tn,
+                                  cfg.budget_frac, (t, u))
+            _check_out(o_gpu[i], o_ref, mag, (t, u))
     st.close()
     del hin
     torch.cuda.empty_cache()
