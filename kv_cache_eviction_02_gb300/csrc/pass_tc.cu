@@ -601,7 +601,7 @@ constexpr float kNoMax = -1e30f;     // running maximum before any visible token
 // S_t = Q_t K_i^T for query tile t (K_i = ring item 2i) into TMEM columns [128 t, 128 t + 128).
 // Issued after P_t(i-1) V_(i-1) by the same thread: MMAs execute in issue order, so the product
 // has read P_t (which lives in these columns) before S_t(i) overwrites it.
-__device__ __forceinline__ bool attn_issue_s(uint32_t base, uint32_t tmem, int t, int i,
+__device__ __forceinline__ bool attn_issue_s(uint32_t base, uint32_t tmem, int t, int i, int nqt,
                                              uint64_t *rfull, uint64_t *rempty, uint64_t *s_full,
                                              volatile int *abort_flag, unsigned *err) {
     constexpr uint32_t id_s = tc::idesc_bf16(128, 128, 0);
@@ -618,13 +618,13 @@ __device__ __forceinline__ bool attn_issue_s(uint32_t base, uint32_t tmem, int t
                      tc::sdesc_sw128(k_addr + o, 16, 1024), id_s, k > 0);
     }
     tc::mma_commit(&s_full[t]);
-    if (t == 1) tc::mma_commit(&rempty[slot]);  // K_i is done once both tiles used it
+    if (t == nqt - 1) tc::mma_commit(&rempty[slot]);  // K_i is done once every tile used it
     return true;
 }
 
 // O_t += P_t V_i for query tile t: P_t is read from TMEM (bf16 pairs in the first 64 columns of
 // S_t, 8 columns per 16 tokens), V_i (ring item 2i+1) is the MN-major B operand.
-__device__ __forceinline__ bool attn_issue_pv(uint32_t base, uint32_t tmem, int t, int i,
+__device__ __forceinline__ bool attn_issue_pv(uint32_t base, uint32_t tmem, int t, int i, int nqt,
                                               uint64_t *rfull, uint64_t *rempty, uint64_t *p_full,
                                               uint64_t *o_done, volatile int *abort_flag,
                                               unsigned *err) {
@@ -641,7 +641,7 @@ __device__ __forceinline__ bool attn_issue_pv(uint32_t base, uint32_t tmem, int 
                         tc::sdesc_sw128(v_addr + k * 2048, 16384, 1024), id_pv,
                         (i > 0 || k > 0) ? 1u : 0u);
     tc::mma_commit(&o_done[t]);
-    if (t == 1) tc::mma_commit(&rempty[slot]);  // V_i is done once both tiles used it
+    if (t == nqt - 1) tc::mma_commit(&rempty[slot]);  // V_i is done once every tile used it
     return true;
 }
 
@@ -661,6 +661,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     const int ntl = (t1 - t0 + 127) / 128;
     if (ntl <= 0) return;
     const int qbase = qp * 256;
+    // query tiles with a valid row: the last CTA of a unit may hold only one (e.g. 320 queries
+    // per KV head at GQA 5: rows 256-319); an empty second tile is neither computed nor waited on
+    const int nqt = qbase + 128 < A.Qu ? 2 : 1;
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + AT_BAR);
     uint64_t *q_full = bars + 0, *rfull = bars + 1, *rempty = bars + 1 + AT_SLOTS,
@@ -695,8 +698,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     if (warp == 0) {
         if (lane == 0) {  // ---- TMA producer: Q once, then K_i, V_i through the ring ----
             const int qrow = unit * A.Qu + qbase;
-            tc::mbar_expect_tx(q_full, 65536);
-            for (int t = 0; t < 2; ++t) {
+            tc::mbar_expect_tx(q_full, 32768u * nqt);
+            for (int t = 0; t < nqt; ++t) {
                 tc::tma_load_2d(sm + AT_Q + t * 32768, &tm_q, 0, qrow + 128 * t, q_full);
                 tc::tma_load_2d(sm + AT_Q + t * 32768 + 16384, &tm_q, 64, qrow + 128 * t, q_full);
             }
@@ -724,15 +727,16 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         // cycle apart (one group's exponentials run while the other's products do).
         if (lane == 0 && tc::mbar_wait(q_full, 0, abort_flag, A.err)) {
             const uint32_t base = tc::smem_u32(sm);
-            bool ok = attn_issue_s(base, tmem, 0, 0, rfull, rempty, s_full, abort_flag, A.err) &&
-                      attn_issue_s(base, tmem, 1, 0, rfull, rempty, s_full, abort_flag, A.err);
+            bool ok = true;
+            for (int t = 0; ok && t < nqt; ++t)
+                ok = attn_issue_s(base, tmem, t, 0, nqt, rfull, rempty, s_full, abort_flag, A.err);
             for (int i = 0; ok && i < ntl; ++i) {
-                for (int t = 0; ok && t < 2; ++t) {
-                    ok = attn_issue_pv(base, tmem, t, i, rfull, rempty, p_full, o_done,
+                for (int t = 0; ok && t < nqt; ++t) {
+                    ok = attn_issue_pv(base, tmem, t, i, nqt, rfull, rempty, p_full, o_done,
                                        abort_flag, A.err);
                     if (ok && i + 1 < ntl)
-                        ok = attn_issue_s(base, tmem, t, i + 1, rfull, rempty, s_full, abort_flag,
-                                          A.err);
+                        ok = attn_issue_s(base, tmem, t, i + 1, nqt, rfull, rempty, s_full,
+                                          abort_flag, A.err);
                 }
             }
         }
@@ -740,7 +744,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             tc::mma_commit(drain);
             tc::mbar_drain(drain, 0);
         }
-    } else if (warp >= 4) {  // ---- softmax groups: warps 4-7 own query tile 0, 8-11 tile 1 ----
+    } else if (warp >= 4 && ((warp - 4) >> 2) < nqt) {
+        // ---- softmax groups: warps 4-7 own query tile 0, 8-11 tile 1 ----
         const int t = (warp - 4) >> 2, lg = warp & 3;
         const int r = lg * 32 + lane;
         const int qi = qbase + 128 * t + r;
