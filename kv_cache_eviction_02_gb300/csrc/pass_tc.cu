@@ -24,6 +24,7 @@
 namespace kve {
 
 constexpr int kSms = 152;  // GB300
+constexpr long kScSetupTiles = 4;  // a scoring CTA's set-up, in 128-token tiles of its loop
 
 bool tc_supported(const LorekvDims &D) {
     return D.dtype == KVE_BF16 && D.d == 128 && D.nq >= 1 && D.nq <= 64;
@@ -54,14 +55,16 @@ bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint6
 }
 
 // Token splits (attention) or ranges (scores) that spread `items * parts` CTAs evenly over the
-// SMs: minimise ceil(items*parts / SMs) * ceil(tiles / parts).
-static int balance_parts(long items, long tiles, int max_parts) {
+// SMs: minimise ceil(items*parts / SMs) * (ceil(tiles / parts) + setup), where `setup` is a CTA's
+// fixed cost in tiles (the scoring CTA stages 112 KB of Q, U and L^T and sets up its TMEM and
+// constant tiles before its first token tile).
+static int balance_parts(long items, long tiles, int max_parts, long setup = 0) {
     int best = 1;
     long best_cost = -1;
     for (int p = 1; p <= max_parts && p <= tiles; ++p) {
         const long waves = (items * p + kSms - 1) / kSms;
         const long per = (tiles + p - 1) / p;
-        const long cost = waves * per;
+        const long cost = waves * (per + setup);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
             best = p;
@@ -987,7 +990,7 @@ cudaError_t launch_scores_tc(const LorekvDims &D, const void *K, const void *V, 
     A.sink = D.sink;
     A.w = D.w;
     A.ntiles = (D.n + 127) / 128;
-    A.nranges = balance_parts((long)D.units * npairs, A.ntiles, 64);
+    A.nranges = balance_parts((long)D.units * npairs, A.ntiles, 64, kScSetupTiles);
     A.tpr = (A.ntiles + A.nranges - 1) / A.nranges;
     A.nranges = (A.ntiles + A.tpr - 1) / A.tpr;
     A.eps = D.eps;
