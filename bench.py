@@ -39,10 +39,9 @@ WORKLOAD = "llama"        # the 128K-context configuration the metric is quoted 
 
 # DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by the sha256 of the
 # kernel's source file at capture time; a changed source reports null until re-captured.
-# scores_tc_kernel: 2.208 GB read + 0.068 GB written per launch on the Mistral-7B-shaped workload
-# (n = 16384, ncu --set full), scaled by the 8x token count of the 128K workload (every term of the
-# traffic is proportional to the tokens scored).
-NCU_TRAFFIC = {"scores": (8 * (2.207626e9 + 0.067719e9), "0dedb9c82af682a6")}
+# scores_tc_kernel: 17.245 GB read + 0.535 GB written in one launch at the 128K workload (ncu
+# --metrics dram__bytes_read.sum,dram__bytes_write.sum, one pass); K and V are 17.18 GB.
+NCU_TRAFFIC = {"scores": (17245312000 + 535038976, "5efc21013b7bb758")}
 # h2o_step_kernel on the OPT-30B shape at batch 8 (ncu, decode steps 21-23 after the 512-token
 # prompt): 1.2094 GB read + 0.0268 GB written per launch against 1.2189 GB of algorithmic bytes
 # (retained K/V rows, accumulated scores and positions, q/k/v/out): DRAM traffic is 1.014 x the
@@ -688,8 +687,8 @@ def e2e_lorekv(cfg, g, run, Lf, G, dev, stream, pg, world, args):
         nch = cfg.L // cl
         scores = run.scores  # every chunk writes its slice of the full-size outputs
 
-        # per-chunk timing of one instrumented step: copy start/end on the copy stream, pass
-        # start/end on the compute stream (timing events; recorded only when `marks` is given)
+        # per-chunk timing: copy start/end on the copy stream, pass start/end on the compute
+        # stream (timing events; recorded only when `marks` is given)
         def one(marks=None):
             start_ev.record(stream)
             if marks is not None:
@@ -759,38 +758,50 @@ def e2e_lorekv(cfg, g, run, Lf, G, dev, stream, pg, world, args):
     link_gbs = 4 * probe_src.numel() * probe_src.element_size() / (p0.elapsed_time(p1) / 1e3) / 1e9
     del probe_dst
     barrier(pg)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        one()
-    e1.record(stream)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    se = [ev() for _ in range(steps + 1)]
+    # every timed step carries its per-chunk marks (copy start/end on the copy stream, pass
+    # start/end on the compute stream): a slow step shows which copies were slow
+    marks = [{"t0": ev(), "copy": [(ev(), ev()) for _ in range(nch)],
+              "pass": [(ev(), ev()) for _ in range(nch)]} if chunked else None
+             for _ in range(steps)]
+    se[0].record(stream)
+    for i in range(steps):
+        if chunked:
+            one(marks[i])
+        else:
+            one()
+        se[i + 1].record(stream)
     torch.cuda.synchronize(dev)
-    ms = max_over_ranks(pg, e0.elapsed_time(e1) / steps, dev)
+    ms = max_over_ranks(pg, se[0].elapsed_time(se[steps]) / steps, dev)
+    step_ms = [round(se[i].elapsed_time(se[i + 1]), 3) for i in range(steps)]
     timeline = None
-    if chunked:  # one more step, instrumented: where the step's time goes, chunk by chunk
-        ev = lambda: torch.cuda.Event(enable_timing=True)
-        marks = {"t0": ev(), "copy": [(ev(), ev()) for _ in range(nch)],
-                 "pass": [(ev(), ev()) for _ in range(nch)]}
-        one(marks)
-        torch.cuda.synchronize(dev)
-        t0 = marks["t0"]
-        per = [float(marks["copy"][c][0].elapsed_time(marks["copy"][c][1])) for c in range(nch)]
+    if chunked:
         chunk_bytes = sum(host[k][:, :cl].numel() * host[k].element_size() for k in layered)
+
+        def rates(mk):
+            return [round(chunk_bytes / (a.elapsed_time(b) / 1e3) / 1e9, 1) for a, b in mk["copy"]]
+
+        slow = max(range(steps), key=lambda i: step_ms[i])
+        mk = marks[slow]
+        t0 = mk["t0"]
         timeline = {
             "chunk_bytes": chunk_bytes,
+            "copy_gbs_by_step": [rates(m) for m in marks],
+            "slowest_step": slow,
             "copy_ms": [[round(t0.elapsed_time(a), 3), round(t0.elapsed_time(b), 3)]
-                        for a, b in marks["copy"]],
+                        for a, b in mk["copy"]],
             "pass_ms": [[round(t0.elapsed_time(a), 3), round(t0.elapsed_time(b), 3)]
-                        for a, b in marks["pass"]],
-            "copy_gbs": [round(chunk_bytes / (x / 1e3) / 1e9, 1) for x in per],
-            "note": "ms from the step's start; copy: copy stream, pass: compute stream",
+                        for a, b in mk["pass"]],
+            "note": "copy_ms / pass_ms: the slowest timed step, ms from its start (copy: copy "
+                    "stream, pass: compute stream); copy_gbs_by_step: each chunk's copy rate in "
+                    "every timed step",
         }
     del host, dev_in
     os.sched_setaffinity(0, old_aff)
     res = {"value": cfg.units * cfg.n * world / (ms / 1e3), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-           "steps": steps, "h2d_gbs_effective": h2d / (ms / 1e3) / 1e9,
+           "steps": steps, "step_ms": step_ms, "h2d_gbs_effective": h2d / (ms / 1e3) / 1e9,
            "link_probe_gbs": link_gbs,
            "numa": numa_report(dev)}
     if chunked:
