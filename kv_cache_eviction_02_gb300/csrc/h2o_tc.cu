@@ -81,10 +81,10 @@ __global__ void __launch_bounds__(kHpThreads, 1)
         }
         for (int i = 0; i < HP_TSLOTS; ++i) {
             tc::mbar_init(&tfull[i], 1);
-            tc::mbar_init(&tempty[i], 256);
+            tc::mbar_init(&tempty[i], 8);  // one arrival per lane-owner warp
         }
-        tc::mbar_init(lsef, 256);
-        tc::mbar_init(lsef2, 256);
+        tc::mbar_init(lsef, 8);
+        tc::mbar_init(lsef2, 8);
         tc::mbar_init(drain, 1);
         *abort_flag = 0;
         tc::mbar_fence_init();
@@ -230,18 +230,27 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                     float v[64];
                     load_half(tmem + tcol + ts * 128, v);
                     tc::fence_before_sync();
-                    tc::mbar_arrive(&tempty[ts]);
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&tempty[ts]);
                     ++tcn;
                     const bool full = b < r && 128 * (b + 1) <= A.P;  // warp-uniform
                     // key column c of this half valid iff c <= lim
                     const int lim = min(q - 128 * b, A.P - 1 - 128 * b) - 64 * hf;
-                    float mx = kNoMax;
-                    if (full) {
+                    float mx;
+                    {
+                        float m4[4] = {kNoMax, kNoMax, kNoMax, kNoMax};
+                        if (full) {
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) mx = fmaxf(mx, v[c]);
-                    } else {
+                            for (int c = 0; c < 64; c += 2)
+                                m4[(c >> 1) & 3] = tc::max3(m4[(c >> 1) & 3], v[c], v[c + 1]);
+                        } else {
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) mx = fmaxf(mx, c <= lim ? v[c] : kNoMax);
+                            for (int c = 0; c < 64; c += 2)
+                                m4[(c >> 1) & 3] =
+                                    tc::max3(m4[(c >> 1) & 3], c <= lim ? v[c] : kNoMax,
+                                             c + 1 <= lim ? v[c + 1] : kNoMax);
+                        }
+                        mx = tc::max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
                     }
                     const float mn = fmaxf(m, mx);
                     const float nmk = -mn * k1;
@@ -280,7 +289,8 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                 if (!ok) break;
                 // merge the halves: half 1 hands (m, l) over, half 0 writes lse2 of the row
                 if (hf == 1) ml_s[row] = make_float2(m, l);
-                tc::mbar_arrive(lsef);
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(lsef);
                 if (!tc::mbar_wait_warp(lsef, lcn & 1, abort_flag, A.err)) {
                     ok = false;
                     break;
@@ -292,7 +302,8 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                                      o.y * tc::ex2_approx((o.x - mm) * k1);
                     lse_s[row] = -(mm * k1 + __log2f(ll));  // -lse2 of query row q
                 }
-                tc::mbar_arrive(lsef2);
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(lsef2);
                 if (!tc::mbar_wait_warp(lsef2, lcn & 1, abort_flag, A.err)) {
                     ok = false;
                     break;
@@ -314,7 +325,8 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                     float v[64];
                     load_half(tmem + tcol + ts * 128, v);
                     tc::fence_before_sync();
-                    tc::mbar_arrive(&tempty[ts]);
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&tempty[ts]);
                     ++tcn;
                     const int j = 128 * b + row;
                     const bool full = b < r && qmax >= 63;  // warp-uniform
