@@ -219,11 +219,13 @@ __device__ __forceinline__ void tmem_wait_st() {
 
 // ---- descriptors -----------------------------------------------------------------------------------
 // Instruction descriptor of kind::f16: A and B both bf16 (ab_bf16 = 1) or both f16 (0), fp32 D,
-// M x N, A K-major, B K-major (b_mn_major = 0) or MN-major (1).
-__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, int b_mn_major, int ab_bf16) {
+// M x N, A K-major (a_mn_major = 0) or MN-major (1), B K-major (b_mn_major = 0) or MN-major (1).
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, int b_mn_major, int ab_bf16,
+                                                     int a_mn_major = 0) {
     return (1u << 4)                       // D format: f32
            | (uint32_t(ab_bf16) << 7)      // A format: f16 (0) / bf16 (1)
            | (uint32_t(ab_bf16) << 10)     // B format: same as A
+           | (uint32_t(a_mn_major) << 15)  // A major-ness
            | (uint32_t(b_mn_major) << 16)  // B major-ness
            | (uint32_t(N >> 3) << 17)      // N / 8
            | (uint32_t(M >> 4) << 24);     // M / 16
