@@ -186,7 +186,9 @@ __global__ void __launch_bounds__(256) combine_kernel(LorekvDims D, const float2
 
 // grid (g, units), block 256. u_q = G_h o_q, c_q = o_q^T G_h o_q and the query's weight, for the
 // nq queries of one query head; bf16 copy of u for the tensor-core path. G_h and the head's o rows
-// are staged in shared memory; a thread computes a 4-query x 8-dimension block of U.
+// (transposed: [dimension][query]) are staged in shared memory; a thread computes a 4-query x
+// 8-dimension block of U, reading its 4 queries' o values for a dimension as one 16-byte word
+// (consecutive threads hold consecutive query groups: no bank conflict).
 template <typename T>
 __global__ void __launch_bounds__(256) prep_u_kernel(LorekvDims D, const float *__restrict__ G,
                                                      const float *__restrict__ omega,
@@ -201,7 +203,7 @@ __global__ void __launch_bounds__(256) prep_u_kernel(LorekvDims D, const float *
     extern __shared__ float sm[];
     const int d = D.d;
     float *Gs = sm;                 // [d][d]
-    float *Os = sm + d * d;         // [nq_pad][d]
+    float *OsT = sm + d * d;        // [d][nq_pad]: o transposed
     const int j = blockIdx.x, unit = blockIdx.y;
     const int kh = unit % D.Hkv, l = (unit / D.Hkv) % D.L, s = unit / (D.Hkv * D.L);
     const int h = kh * D.g + j;
@@ -213,11 +215,16 @@ __global__ void __launch_bounds__(256) prep_u_kernel(LorekvDims D, const float *
         float4 *s4 = reinterpret_cast<float4 *>(Gs);
 #pragma unroll 4
         for (int idx = threadIdx.x; idx < d * d / 4; idx += blockDim.x) s4[idx] = g4[idx];
+        // query fastest, so that the transposed stores of a warp hit consecutive words
         const float4 *o4 = reinterpret_cast<const float4 *>(o + row0 * d);
-        float4 *os4 = reinterpret_cast<float4 *>(Os);
-#pragma unroll 4
-        for (int idx = threadIdx.x; idx < nq_pad * d / 4; idx += blockDim.x)
-            os4[idx] = (idx * 4 / d < D.nq) ? o4[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int idx = threadIdx.x; idx < nq_pad * d / 4; idx += blockDim.x) {
+            const int q = idx % nq_pad, k4 = idx / nq_pad;
+            const float4 v = q < D.nq ? o4[(size_t)q * (d / 4) + k4] : make_float4(0.f, 0.f, 0.f, 0.f);
+            OsT[(4 * k4 + 0) * nq_pad + q] = v.x;
+            OsT[(4 * k4 + 1) * nq_pad + q] = v.y;
+            OsT[(4 * k4 + 2) * nq_pad + q] = v.z;
+            OsT[(4 * k4 + 3) * nq_pad + q] = v.w;
+        }
     }
     __syncthreads();
     const int gsz = d / 8;                       // threads sharing 4 queries (one per 8 dims)
@@ -235,19 +242,24 @@ __global__ void __launch_bounds__(256) prep_u_kernel(LorekvDims D, const float *
             const float4 g0 = *reinterpret_cast<const float4 *>(Gs + k * d + jb * 8);
             const float4 g1 = *reinterpret_cast<const float4 *>(Gs + k * d + jb * 8 + 4);
             const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            const float4 o4k = *reinterpret_cast<const float4 *>(OsT + k * nq_pad + q0);
+            const float ov[4] = {o4k.x, o4k.y, o4k.z, o4k.w};
 #pragma unroll
-            for (int a = 0; a < 4; ++a) {
-                const float ov = Os[(q0 + a) * d + k];
+            for (int a = 0; a < 4; ++a)
 #pragma unroll
-                for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(gv[b], ov, acc[a][b]);  // G symmetric
-            }
+                for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(gv[b], ov[a], acc[a][b]);  // G symmetric
         }
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
             const int r = q0 + a;
             float cpart = 0.f;
+            if (r < D.nq) {  // o_q . u_q over this thread's 8 dimensions (o from global: L2)
+                const float4 *op = reinterpret_cast<const float4 *>(o + (row0 + r) * d + jb * 8);
+                const float4 x0 = op[0], x1 = op[1];
+                const float ox[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-            for (int b = 0; b < 8; ++b) cpart = fmaf(Os[r * d + jb * 8 + b], acc[a][b], cpart);
+                for (int b = 0; b < 8; ++b) cpart = fmaf(ox[b], acc[a][b], cpart);
+            }
             for (int off = gsz / 2; off > 0; off >>= 1)
                 cpart += __shfl_xor_sync(0xffffffffu, cpart, off);
             if (active && r < D.nq) {

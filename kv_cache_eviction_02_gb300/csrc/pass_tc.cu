@@ -129,16 +129,21 @@ __global__ void pack_lt_kernel(const float *__restrict__ L, __nv_bfloat16 *__res
 }
 
 // q16[unit][qi][:] = the query of row qi (head-major, window rows then lookahead rows).
+// grid (ceil(Qu * d / 8 / 256), units), block 256: one 16-byte word (8 values) per thread.
 __global__ void pack_queries_kernel(const __nv_bfloat16 *__restrict__ QW,
                                     const __nv_bfloat16 *__restrict__ QL, LorekvDims D,
                                     __nv_bfloat16 *__restrict__ q16) {
-    const int qi = blockIdx.x, unit = blockIdx.y;
+    const int unit = blockIdx.y;
+    const int per_row = D.d / 8;
+    const long e = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= (long)D.Qu * per_row) return;
+    const int qi = (int)(e / per_row), k8 = (int)(e % per_row);
     const int kh = unit % D.Hkv, sl = unit / D.Hkv;
     const int j = qi / D.nq, r = qi % D.nq, h = kh * D.g + j;
     const __nv_bfloat16 *src = (r < D.w) ? QW + (((size_t)sl * D.Hq + h) * D.w + r) * D.d
                                          : QL + (((size_t)sl * D.Hq + h) * D.MT + (r - D.w)) * D.d;
     __nv_bfloat16 *dst = q16 + ((size_t)unit * D.Qu + qi) * D.d;
-    for (int k = threadIdx.x; k < D.d; k += blockDim.x) dst[k] = src[k];
+    reinterpret_cast<uint4 *>(dst)[k8] = __ldg(reinterpret_cast<const uint4 *>(src) + k8);
 }
 
 // Per-query constants of the scoring epilogue: {-lse2, c, w, a_max}.
@@ -918,7 +923,8 @@ cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, unsigned *err, cudaS
 cudaError_t launch_pack_queries(const LorekvDims &D, const void *QW, const void *QL, void *ws,
                                 const LorekvWorkspace &W, cudaStream_t st) {
     __nv_bfloat16 *q16 = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) + W.q16);
-    pack_queries_kernel<<<dim3(D.Qu, D.units), 128, 0, st>>>(
+    const long words = (long)D.Qu * (D.d / 8);
+    pack_queries_kernel<<<dim3((unsigned)((words + 255) / 256), D.units), 256, 0, st>>>(
         static_cast<const __nv_bfloat16 *>(QW), static_cast<const __nv_bfloat16 *>(QL), D, q16);
     return cudaGetLastError();
 }
