@@ -75,6 +75,31 @@ def test_prepare_wo_matches_oracle(name):
             assert np.allclose(Lc[l, h], Lr, rtol=1e-6, atol=1e-7 * np.abs(Lr).max())
 
 
+# (d_model, d_head): tensor-core Gram (bf16, d_head 128, d_model a multiple of 128) and each of
+# its fall-backs to the double-precision kernel
+_GRAM_SHAPES = [(384, 128), (1280, 128), (200, 128), (256, 64)]
+
+
+@pytest.mark.parametrize("d_model,d", _GRAM_SHAPES, ids=[f"dm{a}-d{b}" for a, b in _GRAM_SHAPES])
+def test_prepare_wo_gram_paths_match_oracle(d_model, d):
+    """G and L of bf16 weights, on the tensor-core path and its fall-backs, against the oracle's
+    double-precision Gram and Cholesky (LORE-KV page, Method, Eqs. 5-7)."""
+    L, Hq = 2, 3
+    gen = torch.Generator().manual_seed(d_model * 131 + d)
+    W = (torch.randn(L, d_model, Hq * d, generator=gen) / d_model ** 0.5).to(torch.bfloat16)
+    pb = api.LorekvProblem(1, L, Hq, 1, d, d_model, 256, 10, api.KVE_BF16)
+    Lf = torch.empty(L, Hq, d, d, device=_dev())
+    G = torch.empty_like(Lf)
+    api.lorekv_prepare_wo(pb, W.to(_dev()), Lf, G)
+    Lc, Gc = Lf.double().cpu().numpy(), G.double().cpu().numpy()
+    for l in range(L):
+        for h in range(Hq):
+            Gr, Lr, st = oracle.gram_cholesky(W[l], d, h)
+            assert st == oracle.OK
+            assert np.allclose(Gc[l, h], Gr, rtol=1e-6, atol=1e-7 * np.abs(Gr).max()), (l, h)
+            assert np.allclose(Lc[l, h], Lr, rtol=1e-6, atol=1e-7 * np.abs(Lr).max()), (l, h)
+
+
 def test_prepare_wo_reports_not_positive_definite():
     # d_model < d_head: every Gram matrix is rank deficient
     pb = api.LorekvProblem(1, 1, 2, 1, 64, 16, 100, 10, api.KVE_F32)
