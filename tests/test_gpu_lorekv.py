@@ -156,7 +156,33 @@ def _run_pass(cfg, g):
 
 @pytest.mark.parametrize("name", list(SMALL))
 def test_eviction_pass_matches_oracle(name):
-    cfg = SMALL[name]
+    _check_full_pass(SMALL[name], name)
+
+
+# Degenerate settings of the method: nothing to evict (n = sink + w), one trajectory of one
+# lookahead query (M = T = 1), a single window query (w = 1), window-only aggregation
+# (lambda_L = 0); tensor-core path (bf16, d_head 128) and CUDA-core path (fp32).
+DEGENERATE = {
+    "bf16_no_candidates": CFG("bf16_no_cand", "bf16", S=1, L=1, Hq=4, Hkv=1, d=128, d_model=256,
+                              n=36, vocab=300),
+    "bf16_M1_T1": CFG("bf16_m1t1", "bf16", S=1, L=2, Hq=4, Hkv=2, d=128, d_model=256, n=552,
+                      vocab=300, M=1, T=1, B=64),
+    "bf16_w1": CFG("bf16_w1", "bf16", S=1, L=1, Hq=8, Hkv=2, d=128, d_model=256, n=517,
+                   vocab=300, w=1, B=64),
+    "bf16_window_only": CFG("bf16_winonly", "bf16", S=1, L=1, Hq=4, Hkv=1, d=128, d_model=256,
+                            n=548, vocab=300, lambda_L=0.0),
+    "f32_window_only_M1": CFG("f32_winonly", "f32", S=1, L=1, Hq=4, Hkv=2, d=32, d_model=64,
+                              n=300, vocab=300, lambda_L=0.0, M=1, T=2, w=8, B=64),
+}
+
+
+@pytest.mark.parametrize("name", list(DEGENERATE))
+def test_degenerate_settings_match_oracle(name):
+    _check_full_pass(DEGENERATE[name], name)
+
+
+def _check_full_pass(cfg, name):
+    """The whole pass (omega, scores, kept sets, compaction) against the oracle on every unit."""
     inp = synth.lorekv_inputs(cfg, "cpu")
     g = {k: v.to(_dev()) for k, v in inp.items()}
     run = _run_pass(cfg, g)
