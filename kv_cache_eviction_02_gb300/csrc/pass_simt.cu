@@ -227,8 +227,12 @@ __global__ void __launch_bounds__(256) prep_u_kernel(LorekvDims D, const float *
         }
     }
     __syncthreads();
-    const int gsz = d / 8;                       // threads sharing 4 queries (one per 8 dims)
+    // gsz threads share 4 queries; thread jb takes dimensions 4 jb .. 4 jb + 3 and d/2 + 4 jb ..
+    // d/2 + 4 jb + 3, so that each 16-byte G load of the group covers consecutive words (no bank
+    // conflict)
+    const int gsz = d / 8;
     const int jb = threadIdx.x % gsz, qg = threadIdx.x / gsz;
+    const int c0 = 4 * jb, c1 = d / 2 + 4 * jb;
     const int qstep = blockDim.x / gsz;
     for (int base = 0; base < nq_pad; base += qstep * 4) {  // uniform trip count: shuffles below
         const bool active = base + qg * 4 < nq_pad;
@@ -239,8 +243,8 @@ __global__ void __launch_bounds__(256) prep_u_kernel(LorekvDims D, const float *
 #pragma unroll
             for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
         for (int k = 0; k < d; ++k) {
-            const float4 g0 = *reinterpret_cast<const float4 *>(Gs + k * d + jb * 8);
-            const float4 g1 = *reinterpret_cast<const float4 *>(Gs + k * d + jb * 8 + 4);
+            const float4 g0 = *reinterpret_cast<const float4 *>(Gs + k * d + c0);
+            const float4 g1 = *reinterpret_cast<const float4 *>(Gs + k * d + c1);
             const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
             const float4 o4k = *reinterpret_cast<const float4 *>(OsT + k * nq_pad + q0);
             const float ov[4] = {o4k.x, o4k.y, o4k.z, o4k.w};
@@ -254,8 +258,9 @@ __global__ void __launch_bounds__(256) prep_u_kernel(LorekvDims D, const float *
             const int r = q0 + a;
             float cpart = 0.f;
             if (r < D.nq) {  // o_q . u_q over this thread's 8 dimensions (o from global: L2)
-                const float4 *op = reinterpret_cast<const float4 *>(o + (row0 + r) * d + jb * 8);
-                const float4 x0 = op[0], x1 = op[1];
+                const float *orow = o + (row0 + r) * d;
+                const float4 x0 = *reinterpret_cast<const float4 *>(orow + c0);
+                const float4 x1 = *reinterpret_cast<const float4 *>(orow + c1);
                 const float ox[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
                 for (int b = 0; b < 8; ++b) cpart = fmaf(ox[b], acc[a][b], cpart);
@@ -265,11 +270,12 @@ __global__ void __launch_bounds__(256) prep_u_kernel(LorekvDims D, const float *
             if (active && r < D.nq) {
                 const size_t row = row0 + r;
 #pragma unroll
-                for (int b = 0; b < 8; ++b) u32[row * d + jb * 8 + b] = acc[a][b];
+                for (int b = 0; b < 8; ++b) u32[row * d + (b < 4 ? c0 + b : c1 + b - 4)] = acc[a][b];
                 if (u16)  // -2 u_q (exact scaling of the rounded u_q): B operand of X = -2 V U^T
 #pragma unroll
                     for (int b = 0; b < 8; ++b)
-                        u16[row * d + jb * 8 + b] = __float2bfloat16_rn(-2.f * acc[a][b]);
+                        u16[row * d + (b < 4 ? c0 + b : c1 + b - 4)] =
+                            __float2bfloat16_rn(-2.f * acc[a][b]);
                 if (jb == 0) cq[row] = cpart;
             }
         }
