@@ -104,27 +104,32 @@ namespace {
 // lower triangular, column j only gets contributions from k >= j: at the 16-wide K step s only
 // the first groups are non-zero, and the MMA over K step s reads just those leading rows. A
 // missing second head (odd group size) is zero.
-// The pair's two L_h are staged in shared memory (rows padded to 129 floats) so that both the
-// reads of L (along j) and the writes of the packed rows (along k) are coalesced.
-constexpr size_t kPackLtSmem = 2 * 128 * 129 * sizeof(float);
-__global__ void pack_lt_kernel(const float *__restrict__ L, __nv_bfloat16 *__restrict__ lt,
-                               int Hq, int Hkv, int g, int npairs) {
+// grid (L * Hkv * npairs, 8), block 256: CTA (blk, rb) writes the 32 packed rows 32 rb .. 32 rb +
+// 31, i.e. one 16-column group of both heads: it stages those 16 columns of the two L_h (all 128
+// k, rows padded to 17 floats) in shared memory, so that the reads of L (64 bytes along j) and the
+// writes of the packed rows (along k, two values a thread) are coalesced and many CTAs share an
+// SM.
+__global__ void __launch_bounds__(256) pack_lt_kernel(const float *__restrict__ L,
+                                                      __nv_bfloat16 *__restrict__ lt, int Hq,
+                                                      int Hkv, int g, int npairs) {
     constexpr int d = 128;
-    extern __shared__ float lsm[];  // [2][d][d + 1]: L_h[k][j] of the pair's heads
-    const int blk = blockIdx.x;  // (l * Hkv + kh) * npairs + pair
+    __shared__ float lsm[2][d][17];  // L_h[k][j0 + t] of the pair's two heads
+    const int blk = blockIdx.x;     // (l * Hkv + kh) * npairs + pair
+    const int rb = blockIdx.y;      // packed rows 32 rb .. 32 rb + 31
     const int pair = blk % npairs, kh = (blk / npairs) % Hkv, l = blk / (npairs * Hkv);
-    for (int e = threadIdx.x; e < 2 * d * d; e += blockDim.x) {
-        const int hd = e / (d * d), k = (e / d) % d, j = e % d;
+    const int j0 = 64 * (rb >> 2) + 16 * (rb & 3);
+    for (int e = threadIdx.x; e < 2 * d * 16; e += blockDim.x) {
+        const int hd = e / (d * 16), k = (e / 16) % d, t = e % 16;
         const int hin = 2 * pair + hd;
-        lsm[(hd * d + k) * (d + 1) + j] =
-            hin < g ? L[(((size_t)l * Hq + kh * g + hin) * d + k) * d + j] : 0.f;
+        lsm[hd][k][t] = hin < g ? L[(((size_t)l * Hq + kh * g + hin) * d + k) * d + j0 + t] : 0.f;
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < 256 * d; e += blockDim.x) {
-        const int r = e / d, k = e % d;
-        const int rr = r & 127, hd = (rr >> 4) & 1;
-        const int j = (r >= 128 ? 64 : 0) + 16 * (rr >> 5) + (rr & 15);
-        lt[(size_t)blk * 256 * d + e] = __float2bfloat16_rn(lsm[(hd * d + k) * (d + 1) + j]);
+    __nv_bfloat162 *dst =
+        reinterpret_cast<__nv_bfloat162 *>(lt + ((size_t)blk * 256 + 32 * rb) * d);
+    for (int e = threadIdx.x; e < 32 * d / 2; e += blockDim.x) {
+        const int r = e / (d / 2), k = 2 * (e % (d / 2));
+        const int hd = r >> 4, t = r & 15;  // row r of the group: head hd, column j0 + t
+        dst[e] = __floats2bfloat162_rn(lsm[hd][k][t], lsm[hd][k + 1][t]);
     }
 }
 
@@ -966,12 +971,8 @@ cudaError_t launch_scores_tc(const LorekvDims &D, const void *K, const void *V, 
     char *b = static_cast<char *>(ws);
     __nv_bfloat16 *lt16 = reinterpret_cast<__nv_bfloat16 *>(b + W.lt16);
     const int npairs = (D.g + SC_HPC - 1) / SC_HPC;
-    cudaError_t pe = cudaFuncSetAttribute(pack_lt_kernel,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)kPackLtSmem);
-    if (pe != cudaSuccess) return pe;
-    pack_lt_kernel<<<D.L * D.Hkv * npairs, 256, kPackLtSmem, st>>>(Lf, lt16, D.Hq, D.Hkv, D.g,
-                                                                   npairs);
+    pack_lt_kernel<<<dim3(D.L * D.Hkv * npairs, 8), 256, 0, st>>>(Lf, lt16, D.Hq, D.Hkv, D.g,
+                                                                  npairs);
     const long rows_q = (long)D.units * D.Qu;
     pack_qconst_kernel<<<(unsigned)((rows_q + 255) / 256), 256, 0, st>>>(
         reinterpret_cast<const float *>(b + W.lse2), reinterpret_cast<const float *>(b + W.cq),

@@ -95,14 +95,16 @@ __global__ void __launch_bounds__(128) rel_cos_kernel(const T *__restrict__ QL, 
     }
 }
 
-// grid S, block 64 (one thread per logits row; MT <= 64). Fixed-order merges, double precision;
-// the disagreement sums over the L*Hq query heads are split over the 64 threads (head lh goes to
-// thread lh % 64) and the 64 partial sums added in thread order.
+// grid S, block kRelFinalThreads (one thread per logits row; MT <= 64). Fixed-order merges,
+// double precision; the disagreement sums over the L*Hq query heads are split over the threads
+// (head lh goes to thread lh % kRelFinalThreads) and the partial sums added by a pairwise tree of
+// fixed shape.
+constexpr int kRelFinalThreads = 256;
 __global__ void rel_final_kernel(const float *__restrict__ logits, const int32_t *__restrict__ y,
                                  const float4 *__restrict__ part, const float *__restrict__ cosm,
                                  int M, int Tn, long vocab, int splits, int LH, float beta,
                                  float gamma, float lambda_D, float *__restrict__ omega) {
-    __shared__ double c_s[64], h_s[64], R_s[32], red[64], dsum[32];
+    __shared__ double c_s[64], h_s[64], R_s[32], red[kRelFinalThreads], dsum[32];
     const int s = blockIdx.x, u = threadIdx.x, MT = M * Tn;
     if (u < MT) {
         const float4 *p = part + ((size_t)s * MT + u) * splits;
@@ -135,11 +137,11 @@ __global__ void rel_final_kernel(const float *__restrict__ logits, const int32_t
                     if (m2 != mm) acc += cosm[(((size_t)s * LH + lh) * M + mm) * M + m2];
             red[u] = acc;
             __syncthreads();
-            if (u == 0) {
-                double t = 0.0;
-                for (int k = 0; k < (int)blockDim.x; ++k) t += red[k];
-                dsum[mm] = t;
+            for (int stride = kRelFinalThreads / 2; stride > 0; stride >>= 1) {
+                if (u < stride) red[u] += red[u + stride];
+                __syncthreads();
             }
+            if (u == 0) dsum[mm] = red[0];
             __syncthreads();
         }
     }
@@ -196,7 +198,7 @@ cudaError_t launch_reliability(const LorekvDims &D, const void *Q_look, const fl
             rel_cos_kernel<__nv_bfloat16><<<dim3(LH, D.S), 128, smem, st>>>(
                 static_cast<const __nv_bfloat16 *>(Q_look), LH, D.M, D.T, D.d, cosm);
     }
-    rel_final_kernel<<<D.S, 64, 0, st>>>(logits, sampled, part, cosm, D.M, D.T, D.vocab,
+    rel_final_kernel<<<D.S, kRelFinalThreads, 0, st>>>(logits, sampled, part, cosm, D.M, D.T, D.vocab,
                                          D.rel_splits, LH, D.beta, D.gamma, D.lambda_D, omega_out);
     return cudaGetLastError();
 }
