@@ -658,6 +658,206 @@ __device__ __forceinline__ bool attn_issue_pv(uint32_t base, uint32_t tmem, int 
     return true;
 }
 
+// One query tile (the CTA's second 128 queries hold no valid row): S is double-buffered in the
+// columns the two tiles use otherwise, so S(i + 1) is computed while the softmax of S(i) runs.
+// S(i) goes to buffer i % 2 (TMEM columns 128 (i % 2)); it is issued right after P(i - 2) V,
+// which read its P from the same columns (MMAs execute in issue order).
+__device__ __forceinline__ bool attn_db_issue_s(uint32_t base, uint32_t tmem, int i,
+                                                uint64_t *rfull, uint64_t *rempty,
+                                                uint64_t *s_full, volatile int *abort_flag,
+                                                unsigned *err) {
+    constexpr uint32_t id_s = tc::idesc_bf16(128, 128, 0);
+    const int c = 2 * i, slot = c % AT_SLOTS, b = i & 1;
+    if (!tc::mbar_wait(&rfull[slot], (c / AT_SLOTS) & 1, abort_flag, err)) return false;
+    tc::fence_after_sync();
+    const uint32_t q_addr = base + AT_Q;
+    const uint32_t k_addr = base + AT_RING + slot * 32768;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
+        tc::mma_bf16(tmem + b * 128, tc::sdesc_sw128(q_addr + o, 16, 1024),
+                     tc::sdesc_sw128(k_addr + o, 16, 1024), id_s, k > 0);
+    }
+    tc::mma_commit(&s_full[b]);
+    tc::mma_commit(&rempty[slot]);
+    return true;
+}
+// O += P(i) V_i with P(i) in buffer i % 2; the last product also completes the single-use
+// o_final barrier (o_done alone can be two phases behind the softmax here: S(i + 1) is issued
+// before P(i) V).
+__device__ __forceinline__ bool attn_db_issue_pv(uint32_t base, uint32_t tmem, int i, int ntl,
+                                                 uint64_t *rfull, uint64_t *rempty,
+                                                 uint64_t *p_full, uint64_t *o_done,
+                                                 uint64_t *o_final, volatile int *abort_flag,
+                                                 unsigned *err) {
+    constexpr uint32_t id_pv = tc::idesc_bf16(128, 128, 1);
+    const int c = 2 * i + 1, slot = c % AT_SLOTS, b = i & 1;
+    if (!tc::mbar_wait(&rfull[slot], (c / AT_SLOTS) & 1, abort_flag, err)) return false;
+    if (!tc::mbar_wait(&p_full[b], (i >> 1) & 1, abort_flag, err)) return false;
+    tc::fence_after_sync();
+    const uint32_t v_addr = base + AT_RING + slot * 32768;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        tc::mma_bf16_ts(tmem + 256, tmem + b * 128 + 8 * k,
+                        tc::sdesc_sw128(v_addr + k * 2048, 16384, 1024), id_pv,
+                        (i > 0 || k > 0) ? 1u : 0u);
+    tc::mma_commit(&o_done[0]);
+    if (i == ntl - 1) tc::mma_commit(o_final);
+    tc::mma_commit(&rempty[slot]);
+    return true;
+}
+
+// ---- softmax groups: warps 4-7 own query tile 0, 8-11 tile 1. DB: one query tile, S(i) in
+// buffer i % 2 (TMEM columns 128 (i % 2)), each buffer's barriers completing every second tile.
+// The two layouts are separate instantiations so each keeps its own register allocation.
+template <bool DB>
+__device__ __forceinline__ void attn_softmax(const AttnArgs &A, uint32_t tmem, int warp, int lane,
+                                             int qbase, int t0, int t1, int ntl, int unit, int sp,
+                                             uint64_t *s_full, uint64_t *p_full, uint64_t *o_done,
+                                             uint64_t *o_final, volatile int *abort_flag) {
+    const int t = DB ? 0 : (warp - 4) >> 2, lg = warp & 3;
+    const int r = lg * 32 + lane;
+    const int qi = qbase + 128 * t + r;
+    const bool valid_row = qi < A.Qu;
+    const int rr = qi % A.nq;
+    const int nvis = (valid_row && rr < A.w && A.window_causal) ? A.n - A.w + rr + 1 : A.n;
+    const int vend = min(t1, nvis);
+    const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
+    const uint32_t o_col = tmem + lane_off + 256 + t * 128;
+    float m_used = kNoMax, l = 0.f;  // finite sentinel: exp2(x - kNoMax) = 0
+    float m_np = kNoMax;             // true maximum over visible non-protected tokens
+    bool ok = true;
+    for (int i = 0; i < ntl; ++i) {
+        const int sb = DB ? (i & 1) : t;  // S buffer (TMEM columns 128 sb) and its barriers
+        const uint32_t s_col = tmem + lane_off + sb * 128;
+        if (!tc::mbar_wait_warp(&s_full[sb], DB ? ((i >> 1) & 1) : (i & 1), abort_flag,
+                                A.err)) {
+            ok = false;
+            break;
+        }
+        tc::fence_after_sync();
+        float s[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_col + c * 32, s[c]);
+        tc::tmem_wait_ld();
+        const int nv_tile = vend - (t0 + i * 128);  // valid columns of this row in the tile
+        float mt = -INFINITY;
+        if (nv_tile < 128) {  // the tile crosses the end of the split, the unit or a causal window row
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (c * 32 + e >= nv_tile) s[c][e] = -INFINITY;
+        }
+        {
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) m4[c] = tc::max3(m4[c], s[c][e], s[c][e + 1]);
+            mt = tc::max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
+        }
+        {
+            // the largest a over non-protected tokens flags queries with peaked pairs; only
+            // the tiles holding sink or window tokens (CTA-uniform) need a masked maximum
+            const int tbase = t0 + i * 128;
+            float mnp = mt;
+            if (tbase < A.sink || tbase + 128 > A.n - A.w) {
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int tok = tbase + c * 32 + e;
+                        if (tok >= A.sink && tok < A.n - A.w) m4[c] = fmaxf(m4[c], s[c][e]);
+                    }
+                mnp = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            }
+            m_np = fmaxf(m_np, mnp * A.k1);
+        }
+        const float m_new = fmaxf(m_used, mt * A.k1);
+        // O is rescaled only when the row maximum grew by more than 2^8 (and O holds data)
+        const bool rescale = m_new > m_used + kRescaleLog2;
+        const float f = (rescale && i > 0) ? tc::ex2_approx(m_used - m_new) : 1.f;
+        if (rescale) m_used = m_new;
+        const float neg_m = -m_used;
+        // p = exp2(s log2e/sqrt(d) - m), packed at once as bf16 pairs: column j of P holds
+        // tokens 2j, 2j+1
+        const uint64_t k1_2 = tc::pk2(A.k1, A.k1), negm_2 = tc::pk2(neg_m, neg_m);
+        uint64_t lsum2[4] = {0, 0, 0, 0};  // bit pattern 0 = (0.f, 0.f)
+        float pk[2][32];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+            float t0, t1;
+            tc::upk2(tc::fma2(tc::pk2(s[j >> 4][(2 * j) & 31], s[j >> 4][(2 * j + 1) & 31]),
+                              k1_2, negm_2),
+                     t0, t1);
+            const float p0 = tc::ex2_approx(t0), p1 = tc::ex2_approx(t1);
+            lsum2[j & 3] = tc::add2(lsum2[j & 3], tc::pk2(p0, p1));
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+            pk[j >> 5][j & 31] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&h2));
+        }
+        float lsum;
+        {
+            float a[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) tc::upk2(lsum2[k], a[2 * k], a[2 * k + 1]);
+            lsum = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+        }
+        l = fmaf(l, f, lsum);
+        // tcgen05.ld/st are warp-collective (.sync.aligned): the rescale branch is taken by the
+        // whole warp when any of its rows needs it (f = 1 leaves the other rows unchanged)
+        if (__any_sync(0xffffffffu, f != 1.f)) {
+            // O must hold the previous product before it is rescaled
+            if (!tc::mbar_wait_warp(&o_done[t], (i - 1) & 1, abort_flag, A.err)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float o[32];
+                tc::tmem_ld32(o_col + c * 32, o);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] *= f;
+                tc::tmem_st32(o_col + c * 32, o);
+            }
+        }
+        // P row -> TMEM over the first 64 columns of S_t (S_t is in registers; the previous
+        // P_t V product completed before S_t(i) was written)
+        tc::tmem_st32(s_col, pk[0]);
+        tc::tmem_st32(s_col + 32, pk[1]);
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        tc::mbar_arrive(&p_full[sb]);
+    }
+    // warp-uniform condition before the warp-collective TMEM loads
+    if (__all_sync(0xffffffffu,
+                   ok && (DB ? tc::mbar_wait(o_final, 0, abort_flag, A.err)
+                             : tc::mbar_wait(&o_done[t], (ntl - 1) & 1, abort_flag,
+                                             A.err)))) {
+        tc::fence_after_sync();
+        const size_t rowi = ((size_t)unit * A.nsplit + sp) * A.Qu + qi;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float o[32];
+            tc::tmem_ld32(o_col + c * 32, o);
+            tc::tmem_wait_ld();
+            if (valid_row) {
+                float4 *dst = reinterpret_cast<float4 *>(A.part_o + rowi * 128 + c * 32);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+            }
+        }
+        if (valid_row) {
+            A.part_ml[rowi] = make_float2(m_used, l);
+            A.part_mx[rowi] = m_np;
+        }
+    }
+}
+
 // 12 warps: three share a sub-partition's 16K registers, so at most 168 registers a thread.
 __global__ void __launch_bounds__(kAtThreads, 1)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -681,9 +881,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + AT_BAR);
     uint64_t *q_full = bars + 0, *rfull = bars + 1, *rempty = bars + 1 + AT_SLOTS,
              *s_full = bars + 1 + 2 * AT_SLOTS, *p_full = bars + 3 + 2 * AT_SLOTS,
-             *o_done = bars + 5 + 2 * AT_SLOTS, *drain = bars + 7 + 2 * AT_SLOTS;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 8 + 2 * AT_SLOTS);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 9 + 2 * AT_SLOTS);
+             *o_done = bars + 5 + 2 * AT_SLOTS, *drain = bars + 7 + 2 * AT_SLOTS,
+             *o_final = bars + 8 + 2 * AT_SLOTS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 9 + 2 * AT_SLOTS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 10 + 2 * AT_SLOTS);
 
     if (threadIdx.x == 0) {
         tc::mbar_init(q_full, 1);
@@ -697,6 +898,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             tc::mbar_init(&o_done[t], 1);
         }
         tc::mbar_init(drain, 1);
+        tc::mbar_init(o_final, 1);
         *abort_flag = 0;
         tc::mbar_fence_init();
     }
@@ -741,9 +943,20 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         if (lane == 0 && tc::mbar_wait(q_full, 0, abort_flag, A.err)) {
             const uint32_t base = tc::smem_u32(sm);
             bool ok = true;
-            for (int t = 0; ok && t < nqt; ++t)
+            if (nqt == 1) {  // one query tile, S double-buffered
+                for (int i = 0; ok && i < 2 && i < ntl; ++i)
+                    ok = attn_db_issue_s(base, tmem, i, rfull, rempty, s_full, abort_flag, A.err);
+                for (int i = 0; ok && i < ntl; ++i) {
+                    ok = attn_db_issue_pv(base, tmem, i, ntl, rfull, rempty, p_full, o_done,
+                                          o_final, abort_flag, A.err);
+                    if (ok && i + 2 < ntl)
+                        ok = attn_db_issue_s(base, tmem, i + 2, rfull, rempty, s_full, abort_flag,
+                                             A.err);
+                }
+            }
+            for (int t = 0; ok && nqt == 2 && t < nqt; ++t)
                 ok = attn_issue_s(base, tmem, t, 0, nqt, rfull, rempty, s_full, abort_flag, A.err);
-            for (int i = 0; ok && i < ntl; ++i) {
+            for (int i = 0; ok && nqt == 2 && i < ntl; ++i) {
                 for (int t = 0; ok && t < nqt; ++t) {
                     ok = attn_issue_pv(base, tmem, t, i, nqt, rfull, rempty, p_full, o_done,
                                        abort_flag, A.err);
@@ -758,144 +971,12 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             tc::mbar_drain(drain, 0);
         }
     } else if (warp >= 4 && ((warp - 4) >> 2) < nqt) {
-        // ---- softmax groups: warps 4-7 own query tile 0, 8-11 tile 1 ----
-        const int t = (warp - 4) >> 2, lg = warp & 3;
-        const int r = lg * 32 + lane;
-        const int qi = qbase + 128 * t + r;
-        const bool valid_row = qi < A.Qu;
-        const int rr = qi % A.nq;
-        const int nvis = (valid_row && rr < A.w && A.window_causal) ? A.n - A.w + rr + 1 : A.n;
-        const int vend = min(t1, nvis);
-        const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
-        const uint32_t s_col = tmem + lane_off + t * 128;
-        const uint32_t o_col = tmem + lane_off + 256 + t * 128;
-        float m_used = kNoMax, l = 0.f;  // finite sentinel: exp2(x - kNoMax) = 0
-        float m_np = kNoMax;             // true maximum over visible non-protected tokens
-        bool ok = true;
-        for (int i = 0; i < ntl; ++i) {
-            if (!tc::mbar_wait_warp(&s_full[t], i & 1, abort_flag, A.err)) {
-                ok = false;
-                break;
-            }
-            tc::fence_after_sync();
-            float s[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_col + c * 32, s[c]);
-            tc::tmem_wait_ld();
-            const int nv_tile = vend - (t0 + i * 128);  // valid columns of this row in the tile
-            float mt = -INFINITY;
-            if (nv_tile < 128) {  // the tile crosses the end of the split, the unit or a causal window row
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (c * 32 + e >= nv_tile) s[c][e] = -INFINITY;
-            }
-            {
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) m4[c] = tc::max3(m4[c], s[c][e], s[c][e + 1]);
-                mt = tc::max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
-            }
-            {
-                // the largest a over non-protected tokens flags queries with peaked pairs; only
-                // the tiles holding sink or window tokens (CTA-uniform) need a masked maximum
-                const int tbase = t0 + i * 128;
-                float mnp = mt;
-                if (tbase < A.sink || tbase + 128 > A.n - A.w) {
-                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int tok = tbase + c * 32 + e;
-                            if (tok >= A.sink && tok < A.n - A.w) m4[c] = fmaxf(m4[c], s[c][e]);
-                        }
-                    mnp = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-                }
-                m_np = fmaxf(m_np, mnp * A.k1);
-            }
-            const float m_new = fmaxf(m_used, mt * A.k1);
-            // O is rescaled only when the row maximum grew by more than 2^8 (and O holds data)
-            const bool rescale = m_new > m_used + kRescaleLog2;
-            const float f = (rescale && i > 0) ? tc::ex2_approx(m_used - m_new) : 1.f;
-            if (rescale) m_used = m_new;
-            const float neg_m = -m_used;
-            // p = exp2(s log2e/sqrt(d) - m), packed at once as bf16 pairs: column j of P holds
-            // tokens 2j, 2j+1
-            const uint64_t k1_2 = tc::pk2(A.k1, A.k1), negm_2 = tc::pk2(neg_m, neg_m);
-            uint64_t lsum2[4] = {0, 0, 0, 0};  // bit pattern 0 = (0.f, 0.f)
-            float pk[2][32];
-#pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                float t0, t1;
-                tc::upk2(tc::fma2(tc::pk2(s[j >> 4][(2 * j) & 31], s[j >> 4][(2 * j + 1) & 31]),
-                                  k1_2, negm_2),
-                         t0, t1);
-                const float p0 = tc::ex2_approx(t0), p1 = tc::ex2_approx(t1);
-                lsum2[j & 3] = tc::add2(lsum2[j & 3], tc::pk2(p0, p1));
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-                pk[j >> 5][j & 31] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&h2));
-            }
-            float lsum;
-            {
-                float a[8];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) tc::upk2(lsum2[k], a[2 * k], a[2 * k + 1]);
-                lsum = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
-            }
-            l = fmaf(l, f, lsum);
-            // tcgen05.ld/st are warp-collective (.sync.aligned): the rescale branch is taken by the
-            // whole warp when any of its rows needs it (f = 1 leaves the other rows unchanged)
-            if (__any_sync(0xffffffffu, f != 1.f)) {
-                // O must hold the previous product before it is rescaled
-                if (!tc::mbar_wait_warp(&o_done[t], (i - 1) & 1, abort_flag, A.err)) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after_sync();
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float o[32];
-                    tc::tmem_ld32(o_col + c * 32, o);
-                    tc::tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] *= f;
-                    tc::tmem_st32(o_col + c * 32, o);
-                }
-            }
-            // P row -> TMEM over the first 64 columns of S_t (S_t is in registers; the previous
-            // P_t V product completed before S_t(i) was written)
-            tc::tmem_st32(s_col, pk[0]);
-            tc::tmem_st32(s_col + 32, pk[1]);
-            tc::tmem_wait_st();
-            tc::fence_before_sync();
-            tc::mbar_arrive(&p_full[t]);
-        }
-        // warp-uniform condition before the warp-collective TMEM loads
-        if (__all_sync(0xffffffffu,
-                       ok && tc::mbar_wait(&o_done[t], (ntl - 1) & 1, abort_flag, A.err))) {
-            tc::fence_after_sync();
-            const size_t rowi = ((size_t)unit * A.nsplit + sp) * A.Qu + qi;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float o[32];
-                tc::tmem_ld32(o_col + c * 32, o);
-                tc::tmem_wait_ld();
-                if (valid_row) {
-                    float4 *dst = reinterpret_cast<float4 *>(A.part_o + rowi * 128 + c * 32);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
-                }
-            }
-            if (valid_row) {
-                A.part_ml[rowi] = make_float2(m_used, l);
-                A.part_mx[rowi] = m_np;
-            }
-        }
+        if (nqt == 1)
+            attn_softmax<true>(A, tmem, warp, lane, qbase, t0, t1, ntl, unit, sp, s_full, p_full,
+                               o_done, o_final, abort_flag);
+        else
+            attn_softmax<false>(A, tmem, warp, lane, qbase, t0, t1, ntl, unit, sp, s_full, p_full,
+                                o_done, o_final, abort_flag);
     }
     __syncthreads();
     if (warp == 1) {
