@@ -38,6 +38,12 @@ SMALL = {
 MULTITILE = CFG("bf16_multitile", "bf16", S=1, L=10, Hq=32, Hkv=8, d=128, d_model=512, n=2048,
                 vocab=1000)
 MULTITILE_UNITS = [(0, 0, 0), (0, 4, 3), (0, 9, 7)]
+# GQA 5: 320 queries per KV head, so each unit's second attention CTA holds one valid query tile
+# (rows 256-319) and double-buffers S; 2048 tokens in two 8-tile ranges per CTA
+MULTITILE_G5 = CFG("bf16_multitile_g5", "bf16", S=1, L=4, Hq=40, Hkv=8, d=128, d_model=512,
+                   n=2048, vocab=1000)
+MULTITILE_G5_UNITS = [(0, 0, 0), (0, 2, 5), (0, 3, 7)]
+MULTITILE_CASES = {"gqa4": (MULTITILE, MULTITILE_UNITS), "gqa5": (MULTITILE_G5, MULTITILE_G5_UNITS)}
 
 
 def _dev():
@@ -241,10 +247,12 @@ def _check_units(cfg, inp, run, units, what):
                             B=cfg.B, rtol=SCORE_RTOL[cfg.dtype], what=f"{what} unit {ui}")
 
 
-def test_multitile_ranges_match_oracle():
+@pytest.mark.parametrize("case", list(MULTITILE_CASES))
+def test_multitile_ranges_match_oracle(case):
     """Attention statistics and the whole pass when every attention CTA walks several K/V tiles
-    (double-buffered S, ring wrap-around, per-half partial merge)."""
-    cfg = MULTITILE
+    (ring wrap-around, per-half partial merge; at GQA 5 also the single-tile CTAs' alternating S
+    buffers)."""
+    cfg, units = MULTITILE_CASES[case]
     inp = synth.lorekv_inputs(cfg, "cpu")
     g = {k: v.to(_dev()) for k, v in inp.items()}
     pb = api.LorekvProblem.from_config(cfg)
@@ -255,7 +263,7 @@ def test_multitile_ranges_match_oracle():
     api.lorekv_attention_stats(pb, g["K"], g["V"], g["Q_W"], g["Q_look"], lse, o, ws)
     api.kve_check_device()
     lse, o = lse.double().cpu().numpy(), o.double().cpu().numpy()
-    for (s, l, kh) in MULTITILE_UNITS:
+    for (s, l, kh) in units:
         u = synth.unit_slice(cfg, inp, s, l, kh)
         eye = np.stack([np.eye(cfg.d)] * cfg.g)
         r = oracle.lorekv_unit(u["K"], u["V"], u["Q_W"], u["Q_look"], eye, np.ones(cfg.M) / cfg.M,
@@ -272,15 +280,16 @@ def test_multitile_ranges_match_oracle():
         bound = 4.0 * sigma + 1e-5 * np.linalg.norm(o_ref, axis=1) + 1e-6
         assert np.all(err <= bound), (ui, float((err / bound).max()))
     run = _run_pass(cfg, g)
-    _check_units(cfg, inp, run, MULTITILE_UNITS, "multitile")
+    _check_units(cfg, inp, run, units, "multitile")
 
 
-def test_eviction_pass_rising_scores():
+@pytest.mark.parametrize("case", list(MULTITILE_CASES))
+def test_eviction_pass_rising_scores(case):
     """The second half of every unit's keys is shifted by 30 along the unit's mean query direction:
     nearly every query's running maximum rises by more than 2^8 (in exp2 units) half-way through
     the cache, which takes the attention pass's lazy-rescale path inside multi-tile ranges, while
     attention stays spread over the shifted half (largest probability about 0.2)."""
-    cfg = MULTITILE
+    cfg, units = MULTITILE_CASES[case]
     inp = synth.lorekv_inputs(cfg, "cpu")
     K = inp["K"].float()
     for s in range(cfg.S):
@@ -294,7 +303,7 @@ def test_eviction_pass_rising_scores():
     inp["K"] = K.to(inp["K"].dtype)
     g = {k: v.to(_dev()) for k, v in inp.items()}
     run = _run_pass(cfg, g)
-    _check_units(cfg, inp, run, MULTITILE_UNITS, "rising")
+    _check_units(cfg, inp, run, units, "rising")
 
 
 def test_layer_chunks_match_whole_pass():
