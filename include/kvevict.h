@@ -88,7 +88,10 @@ typedef struct {
 int lorekv_prepare_wo(const KveShape *shape, const void *W_O, float *L_out, float *G_out,
                       void *stream);
 
-/* Bytes of workspace lorekv_score() needs for this shape and parameters. 0 on invalid input. */
+/* Bytes of workspace lorekv_score() needs for this shape and parameters. 0 on invalid input.
+ * Size limits of every LORE-KV call (KVE_EINVAL beyond them): units = n_seq * n_layers *
+ * n_kv_heads at most 65535; units * n_tokens and units * (n_q_heads / n_kv_heads) * (w + M*T)
+ * below 2^31. */
 size_t lorekv_workspace_size(const KveShape *shape, const KveLorekvParams *params);
 
 /* Scores every cached token (LORE-KV page, Method, Eqs. 2-7).
@@ -182,7 +185,9 @@ typedef struct KveH2O KveH2O;
  * up to max_len tokens (prompt + decode steps), budget_frac in (0, 1]. Slot capacity per unit is
  * floor(budget_frac*max_len) + 1. dtype KVE_F16 or KVE_BF16. *out receives the handle. The state
  * also holds the prefill's scratch (two fp32 partial column sums per unit and prompt token, sized
- * for a prompt of max_len), so h2o_prefill and h2o_decode_step allocate nothing. */
+ * for a prompt of max_len), so h2o_prefill and h2o_decode_step allocate nothing. KVE_EINVAL for
+ * d_head other than 64 or 128, a slot capacity above 4096, or batch * n_layers * n_heads * max_len
+ * of 2^31 or more (checked before anything is allocated). */
 int h2o_state_create(KveH2O **out, int batch, int n_layers, int n_heads, int d_head, int max_len,
                      float budget_frac, int dtype);
 
@@ -226,7 +231,8 @@ void h2o_state_destroy(KveH2O *st);
  * h / (n_q_heads/n_kv_heads); sink = leading system-prompt slots that are never scored or evicted
  * (design choice 4); keep_J = tokens kept per sequence (Algorithm 3, J). dtype is the element type
  * of K, V, Q_fresh, H_last, W_O and W_U: KVE_F32 or KVE_BF16. d_head is 32, 64 or 128;
- * 0 <= sink <= n_tokens; 1 <= keep_J <= n_tokens. */
+ * 0 <= sink <= n_tokens; 1 <= keep_J <= n_tokens; n_seq and n_q_heads at most 65535, d_model at
+ * most 2^22, n_seq * n_q_heads * n_tokens below 2^31 (KVE_EINVAL otherwise). */
 typedef struct {
     int n_seq, n_q_heads, n_kv_heads, d_head, d_model, n_tokens, vocab, dtype, sink, keep_J;
 } KveCcShape;

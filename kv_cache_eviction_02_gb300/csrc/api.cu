@@ -176,6 +176,13 @@ bool lorekv_dims(const KveShape *sh, const KveLorekvParams *p, LorekvDims *D, co
     if (!(p->eps >= 0.f) || !std::isfinite(p->eps) || !std::isfinite(p->lambda_L) ||
         !std::isfinite(p->beta) || !std::isfinite(p->gamma) || !std::isfinite(p->lambda_D))
         return (*why = "parameters must be finite, eps >= 0"), false;
+    // the kernels' grids carry the units in gridDim.y (at most 65535), and K/V rows (unit, token)
+    // and query rows (unit, query) are addressed with 32-bit indices and TMA coordinates
+    const long long units = (long long)sh->n_seq * sh->n_layers * sh->n_kv_heads;
+    const long long qu = (long long)(sh->n_q_heads / sh->n_kv_heads) * (p->w + p->M * p->T);
+    if (units > 65535) return (*why = "n_seq * n_layers * n_kv_heads must be at most 65535"), false;
+    if (units * sh->n_tokens >= (1LL << 31) || units * qu >= (1LL << 31))
+        return (*why = "units * n_tokens and units * queries per unit must be below 2^31"), false;
     D->S = sh->n_seq;
     D->L = sh->n_layers;
     D->Hq = sh->n_q_heads;
@@ -515,6 +522,9 @@ static int cc_dims(const char *fn, const KveCcShape *sh, CcDims *D) {
     // launch-grid limits: y = query heads / column tiles, z = sequences
     if (sh->n_seq > 65535 || sh->n_q_heads > 65535 || sh->d_model > (1 << 22))
         return fail(KVE_EINVAL, "%s: n_seq, n_q_heads or d_model too large", fn);
+    // query rows (sequence, head, token) are addressed with 32-bit indices and TMA coordinates
+    if ((long long)sh->n_seq * sh->n_q_heads * sh->n_tokens >= (1LL << 31))
+        return fail(KVE_EINVAL, "%s: n_seq * n_q_heads * n_tokens must be below 2^31", fn);
     *D = CcDims{sh->n_seq, sh->n_q_heads, sh->n_kv_heads, sh->d_head, sh->d_model, sh->n_tokens,
                 sh->vocab, sh->dtype, sh->sink, sh->keep_J, sh->n_tokens};
     return KVE_OK;
@@ -843,6 +853,9 @@ int h2o_state_create(KveH2O **out, int batch, int n_layers, int n_heads, int d_h
         return fail(KVE_EINVAL, "h2o_state_create: budget_frac must be in (0, 1]");
     const int cap = (int)floor((double)budget_frac * (double)max_len) + 1;
     if (cap > 4096) return fail(KVE_EINVAL, "h2o_state_create: slot capacity %d > 4096", cap);
+    // prompt rows (unit, position) are addressed with 32-bit indices and TMA coordinates
+    if ((long long)batch * n_layers * n_heads * max_len >= (1LL << 31))
+        return fail(KVE_EINVAL, "h2o_state_create: batch * n_layers * n_heads * max_len must be below 2^31");
     KveH2O *h = new KveH2O();
     H2OState &s = h->s;
     s.batch = batch;

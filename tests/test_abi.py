@@ -67,6 +67,8 @@ def test_workspace_size_and_capacity(api):
     dict(d_head=96),                # unsupported head size
     dict(n_tokens=20),              # fewer tokens than sink + w
     dict(M=40),                     # too many trajectories
+    dict(n_seq=16385),              # 65540 units: beyond the launch grids' y extent
+    dict(n_tokens=1 << 29),         # 4 units x 2^29 K/V rows: beyond 32-bit row indices
 ])
 def test_invalid_shapes_are_rejected_without_a_gpu(api, bad):
     pb = _pb(api, **bad)
@@ -126,6 +128,7 @@ def test_cc_workspace_size_covers_the_attention_outputs(api):
     dict(sink=-1), dict(sink=513),
     dict(dtype=2),                 # f16 not supported here
     dict(vocab=0),
+    dict(n_seq=4096, n_tokens=1 << 16, keep_J=512),  # query rows beyond 32-bit indices
 ])
 def test_cc_invalid_shapes_are_rejected_without_a_gpu(api, bad):
     pb = _cc(api, **bad)
@@ -157,6 +160,9 @@ def test_h2o_create_validates_arguments(api):
     assert L.h2o_state_create(ctypes.byref(h), 1, 1, 2, 64, 100, 1.5, api.KVE_F16) == api.KVE_EINVAL
     assert L.h2o_state_create(ctypes.byref(h), 1, 1, 2, 64, 100, 0.2, api.KVE_F32) == api.KVE_EDTYPE
     assert L.h2o_state_create(ctypes.byref(h), 1, 1, 2, 64, 100000, 0.2, api.KVE_F16) == api.KVE_EINVAL
+    # 2^21 units x 1024 positions: prompt rows beyond 32-bit indices (checked before allocating)
+    assert L.h2o_state_create(ctypes.byref(h), 1 << 11, 32, 32, 64, 1024, 0.2,
+                              api.KVE_F16) == api.KVE_EINVAL
     assert not h.value
     assert L.h2o_decode_step(None, None, None, None, None, None) == api.KVE_EINVAL
 
