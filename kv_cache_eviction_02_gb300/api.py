@@ -126,6 +126,25 @@ def _ptr(t):
     return t.data_ptr()
 
 
+_TORCH_DTYPE = {KVE_F32: torch.float32, KVE_BF16: torch.bfloat16, KVE_F16: torch.float16}
+
+
+def _sized(t, name, dtype, numel):
+    """_ptr of a tensor argument after checking it against the declared shape: its element type
+    and at least the number of elements the call reads or writes through it (a short buffer
+    would otherwise be read or written past its end on the device). Integer addresses pass
+    unchecked."""
+    if t is None or isinstance(t, int):
+        return _ptr(t)
+    if isinstance(dtype, int):
+        dtype = _TORCH_DTYPE[dtype]
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, the shape declares {dtype}")
+    if t.numel() < numel:
+        raise ValueError(f"{name}: {t.numel()} elements, the shape needs {numel}")
+    return _ptr(t)
+
+
 def _stream(stream):
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -177,11 +196,34 @@ class LorekvProblem:
     def units(self) -> int:
         return self.n_seq * self.n_layers * self.n_kv_heads
 
+    def _inputs(self, K, V, Q_W, Q_look):
+        """Checked pointers of the cache and query tensors (layouts of lorekv_score)."""
+        rows = self.n_seq * self.n_layers
+        return (_sized(K, "K", self.dtype, self.units * self.n_tokens * self.d_head),
+                _sized(V, "V", self.dtype, self.units * self.n_tokens * self.d_head),
+                _sized(Q_W, "Q_W", self.dtype, rows * self.n_q_heads * self.w * self.d_head),
+                _sized(Q_look, "Q_look", self.dtype,
+                       rows * self.n_q_heads * self.M * self.T * self.d_head))
+
+    def _factors(self, L, G):
+        f = self.n_layers * self.n_q_heads * self.d_head * self.d_head
+        return _sized(L, "L", torch.float32, f), _sized(G, "G", torch.float32, f)
+
+    def _outputs(self, logits, sampled, scores_out, omega_out):
+        mt = self.n_seq * self.M * self.T
+        return (_sized(logits, "logits", torch.float32, mt * self.vocab),
+                _sized(sampled, "sampled", torch.int32, mt),
+                _sized(scores_out, "scores_out", torch.float32, self.units * self.n_tokens),
+                _sized(omega_out, "omega_out", torch.float32, self.n_seq * self.M))
+
 
 def lorekv_prepare_wo(pb: LorekvProblem, W_O, L_out, G_out, stream=None):
     sh = pb.shape()
-    _check(lib().lorekv_prepare_wo(ctypes.byref(sh), _ptr(W_O), _ptr(L_out), _ptr(G_out),
-                                   _stream(stream)))
+    f = pb.n_layers * pb.n_q_heads * pb.d_head * pb.d_head
+    _check(lib().lorekv_prepare_wo(
+        ctypes.byref(sh), _sized(W_O, "W_O", pb.dtype, f // pb.d_head * pb.d_model),
+        _sized(L_out, "L_out", torch.float32, f), _sized(G_out, "G_out", torch.float32, f),
+        _stream(stream)))
 
 
 def lorekv_workspace_size(pb: LorekvProblem) -> int:
@@ -201,10 +243,10 @@ def lorekv_score(pb, K, V, Q_W, Q_look, L, G, logits, sampled, scores_out, omega
                  stream=None):
     sh, pr = pb.shape(), pb.params()
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(lib().lorekv_score(ctypes.byref(sh), ctypes.byref(pr), _ptr(K), _ptr(V), _ptr(Q_W),
-                              _ptr(Q_look), _ptr(L), _ptr(G), _ptr(logits), _ptr(sampled),
-                              _ptr(scores_out), _ptr(omega_out), _ptr(workspace), ws_bytes,
-                              _stream(stream)))
+    _check(lib().lorekv_score(ctypes.byref(sh), ctypes.byref(pr), *pb._inputs(K, V, Q_W, Q_look),
+                              *pb._factors(L, G), *pb._outputs(logits, sampled, scores_out,
+                                                               omega_out),
+                              _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def lorekv_score_noalloc(pb, K, V, Q_W, Q_look, L, G, logits, sampled, scores_out, omega_out,
@@ -212,17 +254,20 @@ def lorekv_score_noalloc(pb, K, V, Q_W, Q_look, L, G, logits, sampled, scores_ou
     """lorekv_score with the library's fixed scratch array instead of a workspace (allocates
     nothing; shapes needing more than 64 MiB of scratch are rejected)."""
     sh, pr = pb.shape(), pb.params()
-    _check(lib().lorekv_score_noalloc(ctypes.byref(sh), ctypes.byref(pr), _ptr(K), _ptr(V),
-                                      _ptr(Q_W), _ptr(Q_look), _ptr(L), _ptr(G), _ptr(logits),
-                                      _ptr(sampled), _ptr(scores_out), _ptr(omega_out),
+    _check(lib().lorekv_score_noalloc(ctypes.byref(sh), ctypes.byref(pr),
+                                      *pb._inputs(K, V, Q_W, Q_look), *pb._factors(L, G),
+                                      *pb._outputs(logits, sampled, scores_out, omega_out),
                                       _stream(stream)))
 
 
 def lorekv_attention_stats(pb, K, V, Q_W, Q_look, lse_out, o_out, workspace, stream=None):
     sh, pr = pb.shape(), pb.params()
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(lib().lorekv_attention_stats(ctypes.byref(sh), ctypes.byref(pr), _ptr(K), _ptr(V),
-                                        _ptr(Q_W), _ptr(Q_look), _ptr(lse_out), _ptr(o_out),
+    rows = pb.units * (pb.n_q_heads // pb.n_kv_heads) * (pb.w + pb.M * pb.T)
+    _check(lib().lorekv_attention_stats(ctypes.byref(sh), ctypes.byref(pr),
+                                        *pb._inputs(K, V, Q_W, Q_look),
+                                        _sized(lse_out, "lse_out", torch.float32, rows),
+                                        _sized(o_out, "o_out", torch.float32, rows * pb.d_head),
                                         _ptr(workspace), ws_bytes, _stream(stream)))
 
 
@@ -236,9 +281,17 @@ def lorekv_select_compact(pb, scores, K, V, kept_idx, kept_len, K_out, V_out, wo
                           stream=None):
     sh, pr = pb.shape(), pb.params()
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(lib().lorekv_select_compact(ctypes.byref(sh), ctypes.byref(pr), _ptr(scores), _ptr(K),
-                                       _ptr(V), _ptr(kept_idx), _ptr(kept_len), _ptr(K_out),
-                                       _ptr(V_out), _ptr(workspace), ws_bytes, _stream(stream)))
+    cap = lorekv_kept_capacity(pb)
+    kv = pb.units * pb.n_tokens * pb.d_head
+    _check(lib().lorekv_select_compact(
+        ctypes.byref(sh), ctypes.byref(pr),
+        _sized(scores, "scores", torch.float32, pb.units * pb.n_tokens),
+        _sized(K, "K", pb.dtype, kv), _sized(V, "V", pb.dtype, kv),
+        _sized(kept_idx, "kept_idx", torch.int32, pb.units * cap),
+        _sized(kept_len, "kept_len", torch.int32, pb.units),
+        _sized(K_out, "K_out", pb.dtype, pb.units * cap * pb.d_head),
+        _sized(V_out, "V_out", pb.dtype, pb.units * cap * pb.d_head),
+        _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 @dataclass
@@ -259,6 +312,20 @@ class CcProblem:
         return KveCcShape(self.n_seq, self.n_q_heads, self.n_kv_heads, self.d_head, self.d_model,
                           self.n_tokens, self.vocab, self.dtype, self.sink, self.keep_J)
 
+    def _rows(self, K, V, Q, H, tokens, m):
+        """Checked pointers (K, V, Q, H, tokens) of m token rows per sequence: K, V
+        [n_seq][n_kv_heads][m][d_head], Q [n_seq][n_q_heads][m][d_head], H [n_seq][m][d_model],
+        tokens [n_seq][m] int32."""
+        kv = self.n_seq * self.n_kv_heads * m * self.d_head
+        return (_sized(K, "K", self.dtype, kv), _sized(V, "V", self.dtype, kv),
+                _sized(Q, "Q", self.dtype, self.n_seq * self.n_q_heads * m * self.d_head),
+                _sized(H, "H", self.dtype, self.n_seq * m * self.d_model),
+                _sized(tokens, "tokens", torch.int32, self.n_seq * m))
+
+    def _weights(self, W_O, W_U):
+        return (_sized(W_O, "W_O", self.dtype, self.d_model * self.n_q_heads * self.d_head),
+                _sized(W_U, "W_U", self.dtype, self.vocab * self.d_model))
+
 
 def cc_workspace_size(pb: CcProblem) -> int:
     sh = pb.shape()
@@ -269,17 +336,23 @@ def cc_surprise(pb: CcProblem, K, V, Q_fresh, H_last, W_O, W_U, tokens, surprise
                 stream=None):
     sh = pb.shape()
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(lib().cc_surprise(ctypes.byref(sh), _ptr(K), _ptr(V), _ptr(Q_fresh), _ptr(H_last),
-                             _ptr(W_O), _ptr(W_U), _ptr(tokens), _ptr(surprise_out),
+    k, v, q, h, t = pb._rows(K, V, Q_fresh, H_last, tokens, pb.n_tokens)
+    _check(lib().cc_surprise(ctypes.byref(sh), k, v, q, h, *pb._weights(W_O, W_U), t,
+                             _sized(surprise_out, "surprise_out", torch.float32,
+                                    pb.n_seq * pb.n_tokens),
                              _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def cc_select_compact(pb: CcProblem, surprise, K, V, tokens, kept_idx, K_out, V_out, tokens_out,
                       stream=None):
     sh = pb.shape()
-    _check(lib().cc_select_compact(ctypes.byref(sh), _ptr(surprise), _ptr(K), _ptr(V),
-                                   _ptr(tokens), _ptr(kept_idx), _ptr(K_out), _ptr(V_out),
-                                   _ptr(tokens_out), _stream(stream)))
+    k, v, _, _, t = pb._rows(K, V, None, None, tokens, pb.n_tokens)
+    ko, vo, _, _, to = pb._rows(K_out, V_out, None, None, tokens_out, pb.keep_J)
+    _check(lib().cc_select_compact(ctypes.byref(sh),
+                                   _sized(surprise, "surprise", torch.float32,
+                                          pb.n_seq * pb.n_tokens), k, v, t,
+                                   _sized(kept_idx, "kept_idx", torch.int32, pb.n_seq * pb.keep_J),
+                                   ko, vo, to, _stream(stream)))
 
 
 class CcCache:
@@ -302,17 +375,21 @@ class CcCache:
         return lib().cc_cache_seen(self.h)
 
     def append(self, K_new, V_new, Q_new, H_new, tokens_new, stream=None):
-        _check(lib().cc_cache_append(self.h, _ptr(K_new), _ptr(V_new), _ptr(Q_new), _ptr(H_new),
-                                     _ptr(tokens_new), int(K_new.shape[-2]), _stream(stream)))
+        m = int(K_new.shape[-2])
+        _check(lib().cc_cache_append(self.h, *self.pb._rows(K_new, V_new, Q_new, H_new,
+                                                            tokens_new, m),
+                                     m, _stream(stream)))
 
     def refresh(self, W_O, W_U, stream=None):
-        _check(lib().cc_cache_refresh(self.h, _ptr(W_O), _ptr(W_U), _stream(stream)))
+        _check(lib().cc_cache_refresh(self.h, *self.pb._weights(W_O, W_U), _stream(stream)))
 
     def step(self, K_new, V_new, Q_new, H_new, tokens_new, W_O, W_U, stream=None) -> bool:
         r = ctypes.c_int(0)
-        _check(lib().cc_cache_step(self.h, _ptr(K_new), _ptr(V_new), _ptr(Q_new), _ptr(H_new),
-                                   _ptr(tokens_new), int(K_new.shape[-2]), _ptr(W_O), _ptr(W_U),
-                                   ctypes.byref(r), _stream(stream)))
+        m = int(K_new.shape[-2])
+        _check(lib().cc_cache_step(self.h, *self.pb._rows(K_new, V_new, Q_new, H_new, tokens_new,
+                                                          m),
+                                   m, *self.pb._weights(W_O, W_U), ctypes.byref(r),
+                                   _stream(stream)))
         return bool(r.value)
 
     def export(self, stream=None) -> dict:
@@ -394,11 +471,17 @@ class H2OState:
         return lib().h2o_length(self.h)
 
     def prefill(self, K, V, Q, stream=None):
-        _check(lib().h2o_prefill(self.h, _ptr(K), _ptr(V), _ptr(Q), K.shape[-2], _stream(stream)))
+        P = int(K.shape[-2])
+        n = self.units * P * self.d  # [batch][n_layers][n_heads][P][d_head] each
+        _check(lib().h2o_prefill(self.h, _sized(K, "K", self.dtype, n), _sized(V, "V", self.dtype, n),
+                                 _sized(Q, "Q", self.dtype, n), P, _stream(stream)))
 
     def decode_step(self, q, k_new, v_new, attn_out, stream=None):
-        _check(lib().h2o_decode_step(self.h, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(attn_out),
-                                     _stream(stream)))
+        n = self.units * self.d  # [batch][n_layers][n_heads][d_head] each
+        _check(lib().h2o_decode_step(self.h, _sized(q, "q", self.dtype, n),
+                                     _sized(k_new, "k_new", self.dtype, n),
+                                     _sized(v_new, "v_new", self.dtype, n),
+                                     _sized(attn_out, "attn_out", self.dtype, n), _stream(stream)))
 
     def export(self, stream=None):
         cap, dev = self.capacity, torch.device("cuda")

@@ -198,3 +198,27 @@ def test_cc_cache_create_validates_arguments(api):
     assert L.cc_cache_append(None, fake, fake, fake, fake, fake, 1, None) == api.KVE_EINVAL
     assert L.cc_cache_refresh(None, fake, fake, None) == api.KVE_EINVAL
     assert L.cc_cache_length(None) == -api.KVE_EINVAL
+
+
+def test_binding_checks_tensors_against_the_shape(api):
+    """A tensor of another element type, or shorter than the declared shape needs, is refused
+    in the binding before its address reaches the library."""
+    import torch
+    pb = _pb(api)  # bf16, 4 units x 1000 tokens x d 128
+    kv = pb.units * pb.n_tokens * pb.d_head
+    K = torch.zeros(kv, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="dtype"):
+        api.lorekv_score(pb, K.float(), None, None, None, None, None, None, None, None, None, None)
+    with pytest.raises(ValueError, match="elements"):
+        api.lorekv_score(pb, K[:-1], None, None, None, None, None, None, None, None, None, None)
+    with pytest.raises(ValueError, match="elements"):
+        api.lorekv_attention_stats(pb, None, None, None, None, torch.zeros(10), None,
+                                   torch.zeros(1, dtype=torch.uint8))
+    cap = api.lorekv_kept_capacity(pb)
+    with pytest.raises(ValueError, match="kept_idx"):
+        api.lorekv_select_compact(pb, None, None, None,
+                                  torch.zeros(pb.units * cap - 1, dtype=torch.int32), None, None,
+                                  None)
+    # every size right: the binding goes on to the device check (CPU tensors are refused there)
+    with pytest.raises(ValueError, match="CUDA"):
+        api.lorekv_score(pb, K, K, None, None, None, None, None, None, None, None, None)
