@@ -51,6 +51,92 @@ __device__ __forceinline__ void load_half(uint32_t taddr, float (&v)[64]) {
     tc::tmem_wait_ld();
 }
 
+// How the 32 columns of one half of a lane owner's 64-column block slice are treated, decided
+// per warp from the causal and prompt limits of its 32 rows: every column visible to every row,
+// visibility decided per element, or no column visible to any row.
+enum : int { kColAll = 0, kColMask = 1, kColNone = 2 };
+
+// Phase 1 on one block: the row's running maximum m and sum l (log2 domain) take the visible
+// key columns c <= lim of v; H0 and H1 are the modes of columns 0-31 and 32-63. Every mode
+// gives the values of the per-element test (skipped columns add the maximum's identity and +0).
+template <int H0, int H1>
+__device__ __forceinline__ void p1_block(const float (&v)[64], int lim, float k1, uint64_t k1_2,
+                                         float &m, float &l) {
+    float m4[4] = {kNoMax, kNoMax, kNoMax, kNoMax};
+#pragma unroll
+    for (int c = 0; c < 64; c += 2) {
+        const int mode = c < 32 ? H0 : H1;
+        if (mode == kColNone) continue;
+        const float a = (mode == kColAll || c <= lim) ? v[c] : kNoMax;
+        const float b = (mode == kColAll || c + 1 <= lim) ? v[c + 1] : kNoMax;
+        m4[(c >> 1) & 3] = tc::max3(m4[(c >> 1) & 3], a, b);
+    }
+    const float mx = tc::max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
+    const float mn = fmaxf(m, mx);
+    const float nmk = -mn * k1;
+    const uint64_t nmk_2 = tc::pk2(nmk, nmk);
+    uint64_t s2[4] = {0, 0, 0, 0};  // bit pattern 0 = (0.f, 0.f)
+#pragma unroll
+    for (int c = 0; c < 64; c += 2) {
+        const int mode = c < 32 ? H0 : H1;
+        if (mode == kColNone) continue;
+        float ta, tb;
+        tc::upk2(tc::fma2(tc::pk2(v[c], v[c + 1]), k1_2, nmk_2), ta, tb);
+        float ea = tc::ex2_approx(ta), eb = tc::ex2_approx(tb);
+        if (mode == kColMask) {
+            ea = c <= lim ? ea : 0.f;
+            eb = c + 1 <= lim ? eb : 0.f;
+        }
+        s2[(c >> 1) & 3] = tc::add2(s2[(c >> 1) & 3], tc::pk2(ea, eb));
+    }
+    float bs = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float a, bb;
+        tc::upk2(s2[k], a, bb);
+        bs += a + bb;
+    }
+    // a half may see no valid column yet (m stays kNoMax, l 0): the merge of the halves
+    // weights it by 2^(-huge) = 0
+    l = l * tc::ex2_approx((m - mn) * k1) + bs;
+    m = mn;
+}
+
+// Phase 2 on one block: the key row's sum of 2^(s k1 - lse2) over the visible query columns
+// lo <= c <= qmax of v (-lse2 of column c in nlse4); H0, H1 as in p1_block.
+template <int H0, int H1>
+__device__ __forceinline__ float p2_block(const float (&v)[64], const float4 *nlse4, int lo,
+                                          int qmax, uint64_t k1_2) {
+    uint64_t s2[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int c = 0; c < 64; c += 4) {
+        const int mode = c < 32 ? H0 : H1;
+        if (mode == kColNone) continue;
+        const float4 nl = nlse4[c >> 2];
+        float ta, tb, tc_, td;
+        tc::upk2(tc::fma2(tc::pk2(v[c], v[c + 1]), k1_2, tc::pk2(nl.x, nl.y)), ta, tb);
+        tc::upk2(tc::fma2(tc::pk2(v[c + 2], v[c + 3]), k1_2, tc::pk2(nl.z, nl.w)), tc_, td);
+        float ea = tc::ex2_approx(ta), eb = tc::ex2_approx(tb);
+        float ec = tc::ex2_approx(tc_), ed = tc::ex2_approx(td);
+        if (mode == kColMask) {
+            ea = (c >= lo && c <= qmax) ? ea : 0.f;
+            eb = (c + 1 >= lo && c + 1 <= qmax) ? eb : 0.f;
+            ec = (c + 2 >= lo && c + 2 <= qmax) ? ec : 0.f;
+            ed = (c + 3 >= lo && c + 3 <= qmax) ? ed : 0.f;
+        }
+        s2[(c >> 2) & 1] = tc::add2(s2[(c >> 2) & 1], tc::pk2(ea, eb));
+        s2[2 + ((c >> 2) & 1)] = tc::add2(s2[2 + ((c >> 2) & 1)], tc::pk2(ec, ed));
+    }
+    float bs = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float a, bb;
+        tc::upk2(s2[k], a, bb);
+        bs += a + bb;
+    }
+    return bs;
+}
+
 __global__ void __launch_bounds__(kHpThreads, 1)
     h2o_colsum_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_q, ColsumArgs A) {
@@ -227,64 +313,31 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                         break;
                     }
                     tc::fence_after_sync();
+                    // key column c of this half valid iff c <= lim; the warp's rows 32 lg .. +31
+                    // span lim_lo .. lim_hi (warp-uniform)
+                    const int lim = min(q - 128 * b, A.P - 1 - 128 * b) - 64 * hf;
+                    const int qb = 128 * (r - b) + (warp & 3) * 32, plim = A.P - 1 - 128 * b;
+                    const int lim_lo = min(qb, plim) - 64 * hf, lim_hi = min(qb + 31, plim) - 64 * hf;
+                    if (lim_hi < 0) {  // no column of this half is visible to the warp's rows
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&tempty[ts]);
+                        ++tcn;
+                        continue;
+                    }
                     float v[64];
                     load_half(tmem + tcol + ts * 128, v);
                     tc::fence_before_sync();
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(&tempty[ts]);
                     ++tcn;
-                    const bool full = b < r && 128 * (b + 1) <= A.P;  // warp-uniform
-                    // key column c of this half valid iff c <= lim
-                    const int lim = min(q - 128 * b, A.P - 1 - 128 * b) - 64 * hf;
-                    float mx;
-                    {
-                        float m4[4] = {kNoMax, kNoMax, kNoMax, kNoMax};
-                        if (full) {
-#pragma unroll
-                            for (int c = 0; c < 64; c += 2)
-                                m4[(c >> 1) & 3] = tc::max3(m4[(c >> 1) & 3], v[c], v[c + 1]);
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < 64; c += 2)
-                                m4[(c >> 1) & 3] =
-                                    tc::max3(m4[(c >> 1) & 3], c <= lim ? v[c] : kNoMax,
-                                             c + 1 <= lim ? v[c + 1] : kNoMax);
-                        }
-                        mx = tc::max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
-                    }
-                    const float mn = fmaxf(m, mx);
-                    const float nmk = -mn * k1;
-                    const uint64_t nmk_2 = tc::pk2(nmk, nmk);
-                    uint64_t s2[4] = {0, 0, 0, 0};  // bit pattern 0 = (0.f, 0.f)
-                    if (full) {
-#pragma unroll
-                        for (int c = 0; c < 64; c += 2) {
-                            float ta, tb;
-                            tc::upk2(tc::fma2(tc::pk2(v[c], v[c + 1]), k1_2, nmk_2), ta, tb);
-                            s2[(c >> 1) & 3] = tc::add2(
-                                s2[(c >> 1) & 3], tc::pk2(tc::ex2_approx(ta), tc::ex2_approx(tb)));
-                        }
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 64; c += 2) {
-                            float ta, tb;
-                            tc::upk2(tc::fma2(tc::pk2(v[c], v[c + 1]), k1_2, nmk_2), ta, tb);
-                            const float ea = c <= lim ? tc::ex2_approx(ta) : 0.f;
-                            const float eb = c + 1 <= lim ? tc::ex2_approx(tb) : 0.f;
-                            s2[(c >> 1) & 3] = tc::add2(s2[(c >> 1) & 3], tc::pk2(ea, eb));
-                        }
-                    }
-                    float bs = 0.f;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        float a, bb;
-                        tc::upk2(s2[k], a, bb);
-                        bs += a + bb;
-                    }
-                    // a half may see no valid column yet (m stays kNoMax, l 0): the merge below
-                    // weights it by 2^(-huge) = 0
-                    l = l * tc::ex2_approx((m - mn) * k1) + bs;
-                    m = mn;
+                    if (lim_lo >= 63)
+                        p1_block<kColAll, kColAll>(v, lim, k1, k1_2, m, l);
+                    else if (lim_lo == 0 && lim_hi == 31)
+                        p1_block<kColMask, kColNone>(v, lim, k1, k1_2, m, l);
+                    else if (lim_lo == 32 && lim_hi == 63)
+                        p1_block<kColAll, kColMask>(v, lim, k1, k1_2, m, l);
+                    else
+                        p1_block<kColMask, kColMask>(v, lim, k1, k1_2, m, l);
                 }
                 if (!ok) break;
                 // merge the halves: half 1 hands (m, l) over, half 0 writes lse2 of the row
@@ -322,41 +375,30 @@ __global__ void __launch_bounds__(kHpThreads, 1)
                         continue;
                     }
                     tc::fence_after_sync();
-                    float v[64];
-                    load_half(tmem + tcol + ts * 128, v);
-                    tc::fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&tempty[ts]);
-                    ++tcn;
                     const int j = 128 * b + row;
-                    const bool full = b < r && qmax >= 63;  // warp-uniform
-                    const int lo = j - 128 * r - 64 * hf;   // query column c valid iff c >= lo
-                    uint64_t s2[4] = {0, 0, 0, 0};
-#pragma unroll
-                    for (int c = 0; c < 64; c += 4) {
-                        const float4 nl = nlse4[c >> 2];
-                        float ta, tb, tc_, td;
-                        tc::upk2(tc::fma2(tc::pk2(v[c], v[c + 1]), k1_2, tc::pk2(nl.x, nl.y)), ta,
-                                 tb);
-                        tc::upk2(tc::fma2(tc::pk2(v[c + 2], v[c + 3]), k1_2, tc::pk2(nl.z, nl.w)),
-                                 tc_, td);
-                        float ea = tc::ex2_approx(ta), eb = tc::ex2_approx(tb);
-                        float ec = tc::ex2_approx(tc_), ed = tc::ex2_approx(td);
-                        if (!full) {
-                            ea = (c >= lo && c <= qmax) ? ea : 0.f;
-                            eb = (c + 1 >= lo && c + 1 <= qmax) ? eb : 0.f;
-                            ec = (c + 2 >= lo && c + 2 <= qmax) ? ec : 0.f;
-                            ed = (c + 3 >= lo && c + 3 <= qmax) ? ed : 0.f;
-                        }
-                        s2[(c >> 2) & 1] = tc::add2(s2[(c >> 2) & 1], tc::pk2(ea, eb));
-                        s2[2 + ((c >> 2) & 1)] = tc::add2(s2[2 + ((c >> 2) & 1)], tc::pk2(ec, ed));
-                    }
+                    const int lo = j - 128 * r - 64 * hf;  // query column c valid iff c >= lo
+                    // the warp's rows span lo_lo .. lo_lo + 31 (warp-uniform)
+                    const int lo_lo = 128 * (b - r) + (warp & 3) * 32 - 64 * hf;
                     float bs = 0.f;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        float a, bb;
-                        tc::upk2(s2[k], a, bb);
-                        bs += a + bb;
+                    if (qmax < 0 || lo_lo > min(63, qmax)) {  // no column visible to the warp
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&tempty[ts]);
+                        ++tcn;
+                    } else {
+                        float v[64];
+                        load_half(tmem + tcol + ts * 128, v);
+                        tc::fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&tempty[ts]);
+                        ++tcn;
+                        if (lo_lo + 31 <= 0 && qmax >= 63)
+                            bs = p2_block<kColAll, kColAll>(v, nlse4, lo, qmax, k1_2);
+                        else if (lo_lo == 0 && qmax >= 63)
+                            bs = p2_block<kColMask, kColAll>(v, nlse4, lo, qmax, k1_2);
+                        else if (lo_lo == 32 && qmax >= 63)
+                            bs = p2_block<kColNone, kColMask>(v, nlse4, lo, qmax, k1_2);
+                        else
+                            bs = p2_block<kColMask, kColMask>(v, nlse4, lo, qmax, k1_2);
                     }
                     accb[b] = (r == nt - 1 ? 0.f : accb[b]) + bs;
                     if (b == r && j < A.P) accu[j] = accb[b];
