@@ -347,14 +347,16 @@ def run_reference(args):
     steps_total = max(1, args.steps + args.warmup)
     cal = cpu_baseline(cfg, steps=1, warmup=0, one_core=False, n_tokens=4096)
     per_token_s = cal["seconds_per_step"] / 4096
-    n_s = int(min(cfg.n, max(4096, (100.0 / steps_total) / per_token_s)) // 4096 * 4096)
+    n_s = int(min(cfg.n, max(4096, (100.0 / steps_total) / per_token_s)))
+    if n_s < cfg.n:  # a sample shorter than the workload: whole 4096-token blocks
+        n_s = n_s // 4096 * 4096
     cb = cpu_baseline(cfg, steps=args.steps, warmup=args.warmup, one_core=False, n_tokens=n_s)
     line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": cb["seconds_per_step"] * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": f"{cfg.name}: 1 seq x {cfg.L} layers x {cfg.Hq}/{cfg.Hkv} "
-                                   f"heads, d_head {cfg.d}, n {cfg.n}, bf16 inputs",
+                                   f"heads, d_head {cfg.d}, n {cfg.n}, {cfg.dtype} inputs",
                        "sample": cb["sample"]},
             "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample",
                                                 "cpu_model")},
