@@ -225,6 +225,7 @@ bool lorekv_dims(const KveShape *sh, const KveLorekvParams *p, LorekvDims *D, co
     split_len = (split_len + 127) / 128 * 128;
     D->split_len = (int)split_len;
     D->nsplit = (int)((D->n + split_len - 1) / split_len);
+    D->at_qt = 2;
     if (tc_supported(*D)) tc_plan(D);
     long rs = (304 + (long)D->S * D->MT - 1) / ((long)D->S * D->MT);
     const long rs_max = (D->vocab + 2047) / 2048;

@@ -71,6 +71,7 @@ struct LorekvDims {
     float lambda_L, beta, gamma, lambda_D, eps;
     int nsplit;                // token splits of the attention-statistics pass
     int split_len;             // tokens per split (multiple of 128)
+    int at_qt;                 // 128-query tiles per attention CTA on the tensor cores (1 or 2)
     int rel_splits;            // CTAs per logits row in the reliability pass
 };
 

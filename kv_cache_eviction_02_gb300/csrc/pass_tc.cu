@@ -75,7 +75,11 @@ static int balance_parts(long items, long tiles, int max_parts, long setup = 0) 
 
 void tc_plan(LorekvDims *D) {
     const long ntiles = (D->n + 127) / 128;
-    const long nqp = (D->Qu + 255) / 256;
+    // attention CTAs hold two 128-query tiles when the unit's queries fill whole pairs (one
+    // K/V stream serves 256 queries); otherwise one tile each, with S double-buffered and a
+    // deeper K/V ring (the CTAs of a unit share the stream through L2)
+    D->at_qt = D->Qu % 256 == 0 ? 2 : 1;
+    const long nqp = (D->Qu + 128 * D->at_qt - 1) / (128 * D->at_qt);
     // Each split writes and the combine re-reads a 256-query partial (o, m, l: ~128 KB), about
     // the DRAM traffic of two 128-token K/V tiles; count that next to the per-SM tile load.
     const long items = (long)D->units * nqp;
@@ -604,10 +608,17 @@ struct AttnArgs {
 };
 
 constexpr int kAtThreads = 384;  // TMA, MMA issuer, 2 idle, 2 softmax groups
-constexpr int AT_SLOTS = 5;
-constexpr uint32_t AT_Q = 0, AT_RING = 65536;  // Q0, Q1 | 5 x 32 KB ring (K_0, V_0, K_1, ...)
-constexpr uint32_t AT_BAR = AT_RING + AT_SLOTS * 32768;
-constexpr size_t AT_SMEM = AT_BAR + 256 + 1024;
+// Shared memory of a CTA holding QT query tiles: the Q tiles (32 KB each), then the K/V ring of
+// 32 KB items (K_0, V_0, K_1, ...: 5 slots next to two Q tiles, 6 next to one), then barriers.
+template <int QT>
+struct AtLayout {
+    static constexpr int SLOTS = QT == 2 ? 5 : 6;
+    static constexpr uint32_t Q = 0, RING = QT * 32768;
+    static constexpr uint32_t BAR = RING + SLOTS * 32768;
+    static constexpr size_t SMEM = BAR + 256 + 1024;
+};
+constexpr int AT_SLOTS = AtLayout<2>::SLOTS;  // the two-tile issue helpers below
+constexpr uint32_t AT_Q = AtLayout<2>::Q, AT_RING = AtLayout<2>::RING;
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when a row maximum grows by > 2^8
 constexpr float kNoMax = -1e30f;     // running maximum before any visible token
 
@@ -662,16 +673,18 @@ __device__ __forceinline__ bool attn_issue_pv(uint32_t base, uint32_t tmem, int 
 // columns the two tiles use otherwise, so S(i + 1) is computed while the softmax of S(i) runs.
 // S(i) goes to buffer i % 2 (TMEM columns 128 (i % 2)); it is issued right after P(i - 2) V,
 // which read its P from the same columns (MMAs execute in issue order).
+template <int QT>
 __device__ __forceinline__ bool attn_db_issue_s(uint32_t base, uint32_t tmem, int i,
                                                 uint64_t *rfull, uint64_t *rempty,
                                                 uint64_t *s_full, volatile int *abort_flag,
                                                 unsigned *err) {
     constexpr uint32_t id_s = tc::idesc_bf16(128, 128, 0);
-    const int c = 2 * i, slot = c % AT_SLOTS, b = i & 1;
-    if (!tc::mbar_wait(&rfull[slot], (c / AT_SLOTS) & 1, abort_flag, err)) return false;
+    using L = AtLayout<QT>;
+    const int c = 2 * i, slot = c % L::SLOTS, b = i & 1;
+    if (!tc::mbar_wait(&rfull[slot], (c / L::SLOTS) & 1, abort_flag, err)) return false;
     tc::fence_after_sync();
-    const uint32_t q_addr = base + AT_Q;
-    const uint32_t k_addr = base + AT_RING + slot * 32768;
+    const uint32_t q_addr = base + L::Q;
+    const uint32_t k_addr = base + L::RING + slot * 32768;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const uint32_t o = (k >> 2) * 16384 + (k & 3) * 32;
@@ -685,17 +698,19 @@ __device__ __forceinline__ bool attn_db_issue_s(uint32_t base, uint32_t tmem, in
 // O += P(i) V_i with P(i) in buffer i % 2; the last product also completes the single-use
 // o_final barrier (o_done alone can be two phases behind the softmax here: S(i + 1) is issued
 // before P(i) V).
+template <int QT>
 __device__ __forceinline__ bool attn_db_issue_pv(uint32_t base, uint32_t tmem, int i, int ntl,
                                                  uint64_t *rfull, uint64_t *rempty,
                                                  uint64_t *p_full, uint64_t *o_done,
                                                  uint64_t *o_final, volatile int *abort_flag,
                                                  unsigned *err) {
     constexpr uint32_t id_pv = tc::idesc_bf16(128, 128, 1);
-    const int c = 2 * i + 1, slot = c % AT_SLOTS, b = i & 1;
-    if (!tc::mbar_wait(&rfull[slot], (c / AT_SLOTS) & 1, abort_flag, err)) return false;
+    using L = AtLayout<QT>;
+    const int c = 2 * i + 1, slot = c % L::SLOTS, b = i & 1;
+    if (!tc::mbar_wait(&rfull[slot], (c / L::SLOTS) & 1, abort_flag, err)) return false;
     if (!tc::mbar_wait(&p_full[b], (i >> 1) & 1, abort_flag, err)) return false;
     tc::fence_after_sync();
-    const uint32_t v_addr = base + AT_RING + slot * 32768;
+    const uint32_t v_addr = base + L::RING + slot * 32768;
 #pragma unroll
     for (int k = 0; k < 8; ++k)
         tc::mma_bf16_ts(tmem + 256, tmem + b * 128 + 8 * k,
@@ -859,6 +874,8 @@ __device__ __forceinline__ void attn_softmax(const AttnArgs &A, uint32_t tmem, i
 }
 
 // 12 warps: three share a sub-partition's 16K registers, so at most 168 registers a thread.
+// QT: 128-query tiles per CTA (2: one K/V stream for 256 queries; 1: S double-buffered).
+template <int QT>
 __global__ void __launch_bounds__(kAtThreads, 1)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
@@ -867,28 +884,31 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int sp = blockIdx.x % A.nsplit;
-    const int qp = (blockIdx.x / A.nsplit) % A.nqp;
+    using L = AtLayout<QT>;
+    // with one tile per CTA, the CTAs of a (unit, split) are adjacent, so they stream its K/V
+    // tiles together and meet in L2
+    const int sp = QT == 2 ? blockIdx.x % A.nsplit : (blockIdx.x / A.nqp) % A.nsplit;
+    const int qp = QT == 2 ? (blockIdx.x / A.nsplit) % A.nqp : blockIdx.x % A.nqp;
     const int unit = blockIdx.x / (A.nsplit * A.nqp);
     const int t0 = sp * A.split_len, t1 = min(A.n, t0 + A.split_len);
     const int ntl = (t1 - t0 + 127) / 128;
     if (ntl <= 0) return;
-    const int qbase = qp * 256;
+    const int qbase = qp * 128 * QT;
     // query tiles with a valid row: the last CTA of a unit may hold only one (e.g. 320 queries
     // per KV head at GQA 5: rows 256-319); an empty second tile is neither computed nor waited on
-    const int nqt = qbase + 128 < A.Qu ? 2 : 1;
+    const int nqt = QT == 2 && qbase + 128 < A.Qu ? 2 : 1;
 
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + AT_BAR);
-    uint64_t *q_full = bars + 0, *rfull = bars + 1, *rempty = bars + 1 + AT_SLOTS,
-             *s_full = bars + 1 + 2 * AT_SLOTS, *p_full = bars + 3 + 2 * AT_SLOTS,
-             *o_done = bars + 5 + 2 * AT_SLOTS, *drain = bars + 7 + 2 * AT_SLOTS,
-             *o_final = bars + 8 + 2 * AT_SLOTS;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 9 + 2 * AT_SLOTS);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 10 + 2 * AT_SLOTS);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::BAR);
+    uint64_t *q_full = bars + 0, *rfull = bars + 1, *rempty = bars + 1 + L::SLOTS,
+             *s_full = bars + 1 + 2 * L::SLOTS, *p_full = bars + 3 + 2 * L::SLOTS,
+             *o_done = bars + 5 + 2 * L::SLOTS, *drain = bars + 7 + 2 * L::SLOTS,
+             *o_final = bars + 8 + 2 * L::SLOTS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 9 + 2 * L::SLOTS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 10 + 2 * L::SLOTS);
 
     if (threadIdx.x == 0) {
         tc::mbar_init(q_full, 1);
-        for (int s = 0; s < AT_SLOTS; ++s) {
+        for (int s = 0; s < L::SLOTS; ++s) {
             tc::mbar_init(&rfull[s], 1);
             tc::mbar_init(&rempty[s], 1);
         }
@@ -915,26 +935,26 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             const int qrow = unit * A.Qu + qbase;
             tc::mbar_expect_tx(q_full, 32768u * nqt);
             for (int t = 0; t < nqt; ++t) {
-                tc::tma_load_2d(sm + AT_Q + t * 32768, &tm_q, 0, qrow + 128 * t, q_full);
-                tc::tma_load_2d(sm + AT_Q + t * 32768 + 16384, &tm_q, 64, qrow + 128 * t, q_full);
+                tc::tma_load_2d(sm + L::Q + t * 32768, &tm_q, 0, qrow + 128 * t, q_full);
+                tc::tma_load_2d(sm + L::Q + t * 32768 + 16384, &tm_q, 64, qrow + 128 * t, q_full);
             }
             int issued = 0;
             for (int c = 0; c < 2 * ntl; ++c) {
-                const int slot = c % AT_SLOTS;
-                const uint32_t ph = (c / AT_SLOTS) & 1;
+                const int slot = c % L::SLOTS;
+                const uint32_t ph = (c / L::SLOTS) & 1;
                 if (!tc::mbar_wait(&rempty[slot], ph ^ 1, abort_flag, A.err)) break;
                 tc::mbar_expect_tx(&rfull[slot], 32768);
                 const int row = unit * A.n + t0 + (c >> 1) * 128;
                 const CUtensorMap *map = (c & 1) ? &tm_v : &tm_k;
-                uint8_t *dst = sm + AT_RING + slot * 32768;
+                uint8_t *dst = sm + L::RING + slot * 32768;
                 tc::tma_load_2d(dst, map, 0, row, &rfull[slot]);
                 tc::tma_load_2d(dst + 16384, map, 64, row, &rfull[slot]);
                 issued = c + 1;
             }
             // copies still in flight land before the CTA exits (immediate on the normal path)
             tc::mbar_drain(q_full, 0);
-            for (int c = issued - AT_SLOTS < 0 ? 0 : issued - AT_SLOTS; c < issued; ++c)
-                tc::mbar_drain(&rfull[c % AT_SLOTS], (c / AT_SLOTS) & 1);
+            for (int c = issued - L::SLOTS < 0 ? 0 : issued - L::SLOTS; c < issued; ++c)
+                tc::mbar_drain(&rfull[c % L::SLOTS], (c / L::SLOTS) & 1);
         }
     } else if (warp == 1) {
         // ---- MMA issuer. Per K/V tile it submits [P_0 V, S_0 next] then [P_1 V, S_1 next] as
@@ -945,13 +965,14 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             bool ok = true;
             if (nqt == 1) {  // one query tile, S double-buffered
                 for (int i = 0; ok && i < 2 && i < ntl; ++i)
-                    ok = attn_db_issue_s(base, tmem, i, rfull, rempty, s_full, abort_flag, A.err);
-                for (int i = 0; ok && i < ntl; ++i) {
-                    ok = attn_db_issue_pv(base, tmem, i, ntl, rfull, rempty, p_full, o_done,
-                                          o_final, abort_flag, A.err);
-                    if (ok && i + 2 < ntl)
-                        ok = attn_db_issue_s(base, tmem, i + 2, rfull, rempty, s_full, abort_flag,
+                    ok = attn_db_issue_s<QT>(base, tmem, i, rfull, rempty, s_full, abort_flag,
                                              A.err);
+                for (int i = 0; ok && i < ntl; ++i) {
+                    ok = attn_db_issue_pv<QT>(base, tmem, i, ntl, rfull, rempty, p_full, o_done,
+                                              o_final, abort_flag, A.err);
+                    if (ok && i + 2 < ntl)
+                        ok = attn_db_issue_s<QT>(base, tmem, i + 2, rfull, rempty, s_full,
+                                                 abort_flag, A.err);
                 }
             }
             for (int t = 0; ok && nqt == 2 && t < nqt; ++t)
@@ -1033,16 +1054,19 @@ cudaError_t launch_attention_tc(const LorekvDims &D, const void *K, const void *
     A.window_causal = D.window_causal;
     A.nsplit = D.nsplit;
     A.split_len = D.split_len;
-    A.nqp = (D.Qu + 255) / 256;
+    const int qt = D.at_qt == 1 ? 1 : 2;
+    A.nqp = (D.Qu + 128 * qt - 1) / (128 * qt);
     A.k1 = kLog2e / sqrtf((float)D.d);
     A.part_ml = reinterpret_cast<float2 *>(b + W.part_ml);
     A.part_o = reinterpret_cast<float *>(b + W.part_o);
     A.part_mx = reinterpret_cast<float *>(b + W.part_mx);
     A.err = err;
-    cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AT_SMEM);
+    auto kern = qt == 1 ? attention_tc_kernel<1> : attention_tc_kernel<2>;
+    const size_t smem = qt == 1 ? AtLayout<1>::SMEM : AtLayout<2>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return e;
-    attention_tc_kernel<<<D.units * A.nqp * D.nsplit, kAtThreads, AT_SMEM, st>>>(tk, tv, tq, A);
+    kern<<<D.units * A.nqp * D.nsplit, kAtThreads, smem, st>>>(tk, tv, tq, A);
     return cudaGetLastError();
 }
 
