@@ -607,7 +607,9 @@ struct AttnArgs {
     unsigned *err;
 };
 
-constexpr int kAtThreads = 384;  // TMA, MMA issuer, 2 idle, 2 softmax groups
+// TMA, MMA issuer, 2 idle, one softmax group of 4 warps per query tile
+template <int QT>
+constexpr int at_threads() { return (4 + 4 * QT) * 32; }
 // Shared memory of a CTA holding QT query tiles: the Q tiles (32 KB each), then the K/V ring of
 // 32 KB items (K_0, V_0, K_1, ...: 5 slots next to two Q tiles, 6 next to one), then barriers.
 template <int QT>
@@ -873,10 +875,10 @@ __device__ __forceinline__ void attn_softmax(const AttnArgs &A, uint32_t tmem, i
     }
 }
 
-// 12 warps: three share a sub-partition's 16K registers, so at most 168 registers a thread.
-// QT: 128-query tiles per CTA (2: one K/V stream for 256 queries; 1: S double-buffered).
+// QT: 128-query tiles per CTA (2: one K/V stream for 256 queries; 1: S double-buffered). With 12
+// warps three share a sub-partition's 16K registers (at most 168 a thread), with 8 two (255).
 template <int QT>
-__global__ void __launch_bounds__(kAtThreads, 1)
+__global__ void __launch_bounds__(at_threads<QT>(), 1)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_q, AttnArgs A) {
@@ -1066,7 +1068,8 @@ cudaError_t launch_attention_tc(const LorekvDims &D, const void *K, const void *
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<D.units * A.nqp * D.nsplit, kAtThreads, smem, st>>>(tk, tv, tq, A);
+    kern<<<D.units * A.nqp * D.nsplit, qt == 1 ? at_threads<1>() : at_threads<2>(), smem, st>>>(
+        tk, tv, tq, A);
     return cudaGetLastError();
 }
 
