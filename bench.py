@@ -41,7 +41,7 @@ WORKLOAD = "llama"        # the 128K-context configuration the metric is quoted 
 # kernel's source file at capture time; a changed source reports null until re-captured.
 # scores_tc_kernel: 17.245 GB read + 0.535 GB written in one launch at the 128K workload (ncu
 # --metrics dram__bytes_read.sum,dram__bytes_write.sum, one pass); K and V are 17.18 GB.
-NCU_TRAFFIC = {"scores": (17244652288 + 535189248, "e06434e55aa640ea")}
+NCU_TRAFFIC = {"scores": (17244990976 + 534989312, "3467fa20b356fd90")}
 # h2o_step_kernel on the OPT-30B shape at batch 8 (ncu, decode steps 21-23 after the 512-token
 # prompt): 1.2094 GB read + 0.0268 GB written per launch against 1.2189 GB of algorithmic bytes
 # (retained K/V rows, accumulated scores and positions, q/k/v/out): DRAM traffic is 1.014 x the
