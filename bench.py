@@ -37,11 +37,15 @@ METRIC = "KV tokens scored+compacted/sec (eviction pass, 128K ctx); % of HBM roo
 UNIT = "tokens/s"
 WORKLOAD = "llama"        # the 128K-context configuration the metric is quoted on
 
-# DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by the sha256 of the
-# kernel's source file at capture time; a changed source reports null until re-captured.
-# scores_tc_kernel: 17.245 GB read + 0.535 GB written in one launch at the 128K workload (ncu
-# --metrics dram__bytes_read.sum,dram__bytes_write.sum, one pass); K and V are 17.18 GB.
-NCU_TRAFFIC = {"scores": (17244990976 + 534989312, "3467fa20b356fd90")}
+# DRAM bytes per launch of the dominant kernel from an ncu capture (--metrics
+# dram__bytes_read.sum,dram__bytes_write.sum, one pass, full size), by (kernel, workload), with
+# the sha256 of the kernel's source file at capture time; a changed source reports null until
+# re-captured. scores_tc_kernel: 128K workload 17.245 GB read + 0.535 GB written (K and V are
+# 17.18 GB); Mistral-16K 2.207 + 0.065 GB (K + V 2.15 GB); Qwen 4 x 32K 26.445 + 1.005 GB
+# (K + V 25.77 GB).
+NCU_TRAFFIC = {("scores", "llama"): (17244990976 + 534989312, "3467fa20b356fd90"),
+               ("scores", "mistral"): (2207325952 + 64619776, "3467fa20b356fd90"),
+               ("scores", "qwen"): (26445185280 + 1004733696, "3467fa20b356fd90")}
 # h2o_step_kernel on the OPT-30B shape at batch 8 (ncu, decode steps 21-23 after the 512-token
 # prompt): 1.2094 GB read + 0.0268 GB written per launch against 1.2189 GB of algorithmic bytes
 # (retained K/V rows, accumulated scores and positions, q/k/v/out): DRAM traffic is 1.014 x the
@@ -439,8 +443,9 @@ def measure_pass(cfg, g, dev, stream, pg, world, steps, warmup, pk, sample_clock
     src = ("kv_cache_eviction_02_gb300/csrc/pass_tc.cu" if tensor
            else "kv_cache_eviction_02_gb300/csrc/pass_simt.cu")
     traffic = None
-    if cfg.name == WORKLOAD and dom in NCU_TRAFFIC and NCU_TRAFFIC[dom][1] == src_hash(src):
-        traffic = NCU_TRAFFIC[dom][0]
+    key = (dom, cfg.name)
+    if key in NCU_TRAFFIC and NCU_TRAFFIC[key][1] == src_hash(src):
+        traffic = NCU_TRAFFIC[key][0]
     if flops is not None and tensor:
         # a step timed for well under a second: the burst bf16 figure applies
         ach = flops / (dom_ms / 1e3) / 1e12
