@@ -40,12 +40,12 @@ WORKLOAD = "llama"        # the 128K-context configuration the metric is quoted 
 # DRAM bytes per launch of the dominant kernel from an ncu capture (--metrics
 # dram__bytes_read.sum,dram__bytes_write.sum, one pass, full size), by (kernel, workload), with
 # the sha256 of the kernel's source file at capture time; a changed source reports null until
-# re-captured. scores_tc_kernel: 128K workload 17.245 GB read + 0.535 GB written (K and V are
-# 17.18 GB); Mistral-16K 2.207 + 0.065 GB (K + V 2.15 GB); Qwen 4 x 32K 26.445 + 1.005 GB
+# re-captured. scores_tc_kernel: 128K workload 17.244 GB read + 0.535 GB written (K and V are
+# 17.18 GB); Mistral-16K 2.207 + 0.065 GB (K + V 2.15 GB); Qwen 4 x 32K 26.492 + 1.004 GB
 # (K + V 25.77 GB).
-NCU_TRAFFIC = {("scores", "llama"): (17244990976 + 534989312, "3467fa20b356fd90"),
-               ("scores", "mistral"): (2207325952 + 64619776, "3467fa20b356fd90"),
-               ("scores", "qwen"): (26445185280 + 1004733696, "3467fa20b356fd90")}
+NCU_TRAFFIC = {("scores", "llama"): (17244091904 + 534949632, "2184dae91a476dc3"),
+               ("scores", "mistral"): (2207387904 + 64717568, "2184dae91a476dc3"),
+               ("scores", "qwen"): (26491987456 + 1004316416, "2184dae91a476dc3")}
 # h2o_step_kernel on the OPT-30B shape at batch 8 (ncu, decode steps 21-23 after the 512-token
 # prompt): 1.2094 GB read + 0.0268 GB written per launch against 1.2189 GB of algorithmic bytes
 # (retained K/V rows, accumulated scores and positions, q/k/v/out): DRAM traffic is 1.014 x the

@@ -80,14 +80,15 @@ void tc_plan(LorekvDims *D) {
     // deeper K/V ring (the CTAs of a unit share the stream through L2)
     D->at_qt = D->Qu % 256 == 0 ? 2 : 1;
     const long nqp = (D->Qu + 128 * D->at_qt - 1) / (128 * D->at_qt);
-    // Each split writes and the combine re-reads a 256-query partial (o, m, l: ~128 KB), about
-    // the DRAM traffic of two 128-token K/V tiles; count that next to the per-SM tile load.
+    // Each split writes and the combine re-reads a 256-query partial (o, m, l: ~128 KB, the DRAM
+    // traffic of two 128-token K/V tiles) and pays a CTA's set-up; counted as four tiles next to
+    // the per-SM tile load (at 128K this picks 7 splits, measured faster than 13 or 16).
     const long items = (long)D->units * nqp;
     int ns = 1;
     long best = -1;
     for (int p = 1; p <= 64 && p <= ntiles; ++p) {
         const long waves = (items * p + kSms - 1) / kSms;
-        const long cost = waves * ((ntiles + p - 1) / p) + 2 * ((items * p + kSms - 1) / kSms);
+        const long cost = waves * ((ntiles + p - 1) / p) + 4 * waves;
         if (best < 0 || cost < best) {
             best = cost;
             ns = p;

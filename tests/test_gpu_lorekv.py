@@ -33,13 +33,13 @@ SMALL = {
 }
 
 
-# 80 units: enough (unit, query tile) pairs that the attention pass splits the 2048 tokens into a
-# few multi-tile ranges (the small configurations above plan one 128-token tile per range)
+# 80 units: enough (unit, query tile) pairs that the attention pass plans ranges of several
+# 128-token tiles per CTA (the small configurations above plan one tile per range)
 MULTITILE = CFG("bf16_multitile", "bf16", S=1, L=10, Hq=32, Hkv=8, d=128, d_model=512, n=2048,
                 vocab=1000)
 MULTITILE_UNITS = [(0, 0, 0), (0, 4, 3), (0, 9, 7)]
-# GQA 5: 320 queries per KV head, so each unit's second attention CTA holds one valid query tile
-# (rows 256-319) and double-buffers S; 2048 tokens in two 8-tile ranges per CTA
+# GQA 5: 320 queries per KV head, so the attention CTAs hold one query tile each (rows 0-127,
+# 128-255, 256-319) and double-buffer S over multi-tile ranges
 MULTITILE_G5 = CFG("bf16_multitile_g5", "bf16", S=1, L=4, Hq=40, Hkv=8, d=128, d_model=512,
                    n=2048, vocab=1000)
 MULTITILE_G5_UNITS = [(0, 0, 0), (0, 2, 5), (0, 3, 7)]
