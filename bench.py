@@ -39,22 +39,22 @@ WORKLOAD = "llama"        # the 128K-context configuration the metric is quoted 
 
 # DRAM bytes per launch of the dominant kernel from an ncu capture (--metrics
 # dram__bytes_read.sum,dram__bytes_write.sum, one pass, full size), by (kernel, workload), with
-# the sha256 of the kernel's source file at capture time; a changed source reports null until
-# re-captured. scores_tc_kernel: 128K workload 17.244 GB read + 0.535 GB written (K and V are
-# 17.18 GB); Mistral-16K 2.207 + 0.065 GB (K + V 2.15 GB); Qwen 4 x 32K 26.492 + 1.004 GB
-# (K + V 25.77 GB).
-NCU_TRAFFIC = {("scores", "llama"): (17244091904 + 534949632, "2184dae91a476dc3"),
-               ("scores", "mistral"): (2207387904 + 64717568, "2184dae91a476dc3"),
-               ("scores", "qwen"): (26491987456 + 1004316416, "2184dae91a476dc3")}
+# the hash of the kernel source file's code at capture time (src_hash: comments and whitespace
+# left out); changed code reports null until re-captured. scores_tc_kernel: 128K workload
+# 17.244 GB read + 0.535 GB written (K and V are 17.18 GB); Mistral-16K 2.207 + 0.065 GB
+# (K + V 2.15 GB); Qwen 4 x 32K 26.492 + 1.004 GB (K + V 25.77 GB).
+NCU_TRAFFIC = {("scores", "llama"): (17244091904 + 534949632, "a9ef66bf1aca8d1f"),
+               ("scores", "mistral"): (2207387904 + 64717568, "a9ef66bf1aca8d1f"),
+               ("scores", "qwen"): (26491987456 + 1004316416, "a9ef66bf1aca8d1f")}
 # h2o_step_kernel on the OPT-30B shape at batch 8 (ncu, decode steps 21-23 after the 512-token
 # prompt): 1.2094 GB read + 0.0268 GB written per launch against 1.2189 GB of algorithmic bytes
 # (retained K/V rows, accumulated scores and positions, q/k/v/out): DRAM traffic is 1.014 x the
 # algorithmic bytes, a ratio that holds at any batch and length (every term grows with the units
 # and the retained rows), applied to the batch-64 launches.
-NCU_TRAFFIC_H2O = (1.0146, "93a5caf6cc381a20")
+NCU_TRAFFIC_H2O = (1.0146, "46dd9151c168d74b")
 # cc_attn_tc_kernel on the n = 4096 counter-causal workload (ncu --set full, one launch):
 # 37.807 MB read + 0.233 MB written
-NCU_TRAFFIC_CC = {("cc_attention", "qwen7b_4096"): (37.80736e6 + 0.23296e6, "741c9d25cbda615d")}
+NCU_TRAFFIC_CC = {("cc_attention", "qwen7b_4096"): (37.80736e6 + 0.23296e6, "84e8ed792716cff5")}
 
 
 def parse():
@@ -229,8 +229,15 @@ FP32_ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 def src_hash(rel):
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256 prefix of a source file's code: comments removed and whitespace collapsed, so an ncu
+    figure stays tied to the code it was taken on and survives edits to comments only."""
+    import re
+    with open(os.path.join(ROOT, rel)) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    text = re.sub(r"\s+", " ", text).strip()
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
 
 
 # ---------------------------------------------------------------------------------------------

@@ -2,21 +2,21 @@
 // accumulators, TMA-staged 128-byte-swizzled operand tiles.
 //
 // Attention statistics (LORE-KV page, Method: a_{q,i} = softmax_i(q.k_i/sqrt d), o_q =
-// sum_i a_{q,i} v_i), one CTA per (unit, 256 queries, token split):
-//   S_t = Q_t K^T (M = 128 queries, N = 128 tokens) for the two query tiles t = 0, 1 of the CTA,
-//   an online softmax per query row in a 4-warp group per tile (rows = TMEM lanes), P written as
-//   bf16 into shared memory, O_t += P_t V (V as the MN-major B operand). O stays in TMEM; it is
-//   rescaled only when a row's running maximum grows by more than 2^8, so the common step needs no
-//   TMEM round trip. The MMA issuer ping-pongs the two tiles so the tensor pipe computes one tile's
-//   S while the other tile's softmax runs.
+// sum_i a_{q,i} v_i), one CTA per (unit, 256 or 128 queries, token split):
+//   S_t = Q_t K^T (M = 128 queries, N = 128 tokens) per query tile t, an online softmax per query
+//   row in a 4-warp group per tile (rows = TMEM lanes), P written back into TMEM as bf16 pairs
+//   and O_t += P_t V issued with P read from TMEM (V as the MN-major B operand). O stays in TMEM;
+//   it is rescaled only when a row's running maximum grows by more than 2^8. A CTA with two query
+//   tiles alternates them on the tensor pipe (one tile's S is computed while the other tile's
+//   softmax runs); a CTA with one tile double-buffers S instead.
 //
-// Projected deletion scores (Eqs. 5-7), one CTA per (unit, query head, token range), tokens on M:
-//   S^T = K Q_h^T, X = V U_h^T (u_q = G_h o_q) and Y = V L_h (||L_h^T v||^2 = ||row of Y||^2,
-//   the upper-right 64x64 block of L_h^T is zero and skipped) for 128 tokens per tile, into one of
-//   two 256-column TMEM buffers; two 4-warp epilogue groups take alternate tiles and evaluate
-//   e = a/(1-a+eps) sqrt(||L^T v||^2 - 2 v.u + c) with a = exp2(s log2e/sqrt(d) - lse2) for the
-//   head's 64 queries, weighted by psi = mean per set. Per-head partial sums go to the workspace and
-//   a small kernel adds the g heads in a fixed order.
+// Projected deletion scores (Eqs. 5-7), one CTA per (unit, pair of query heads, token range),
+// tokens on M: S = K [Q_h0; Q_h1]^T, X = V [U_h0; U_h1]^T (U holds -2 G_h o_q) and Y = V L_h
+// (||L_h^T v||^2 = ||row of Y||^2; the zero upper-right block of L_h^T is skipped) for 128 tokens
+// per tile, one extra K step adding the per-query constants inside the MMAs; two 4-warp epilogue
+// groups (one per head) evaluate e = a/(1-a+eps) sqrt(||L^T v||^2 - 2 v.u + c) with
+// a = exp2(s log2e/sqrt(d) - lse2) for the head's 64 queries, weighted per query set. Per-head
+// partial sums go to the workspace and a small kernel adds the g heads in a fixed order.
 #include <cudaTypedefs.h>
 
 #include "tc_common.cuh"
