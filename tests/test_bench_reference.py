@@ -27,3 +27,19 @@ def test_reference_arm_prints_its_json_line_on_the_host():
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_source_hash_follows_code_not_comments(tmp_path, monkeypatch):
+    """The key that ties an ncu figure to its kernel: unchanged by edits to comments or layout,
+    changed by any edit to the code."""
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    src = tmp_path / "k.cu"
+    src.write_text("// header\n__global__ void k(int *p) { p[0] = 1; }  // store\n/* block\n note */\n")
+    h0 = bench.src_hash("k.cu")
+    src.write_text("// a longer header\n// over two lines\n__global__ void k(int *p) {\n"
+                   "    p[0] = 1;\n}\n")
+    assert bench.src_hash("k.cu") == h0
+    src.write_text("__global__ void k(int *p) { p[0] = 2; }\n")
+    assert bench.src_hash("k.cu") != h0
