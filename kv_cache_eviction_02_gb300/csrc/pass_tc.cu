@@ -897,8 +897,9 @@ __global__ void __launch_bounds__(at_threads<QT>(), 1)
     const int ntl = (t1 - t0 + 127) / 128;
     if (ntl <= 0) return;
     const int qbase = qp * 128 * QT;
-    // query tiles with a valid row: the last CTA of a unit may hold only one (e.g. 320 queries
-    // per KV head at GQA 5: rows 256-319); an empty second tile is neither computed nor waited on
+    // query tiles with a valid row: with two tiles per CTA, the last CTA of a unit whose queries
+    // are not a multiple of 256 holds only one (the planner gives such units one-tile CTAs, but
+    // the case is handled); an empty second tile is neither computed nor waited on
     const int nqt = QT == 2 && qbase + 128 < A.Qu ? 2 : 1;
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::BAR);
