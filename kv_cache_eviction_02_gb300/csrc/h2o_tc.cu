@@ -12,8 +12,11 @@
 // The unit's K tiles stay in shared memory while its query tiles run in descending order, so key
 // tile r is last used by query tile r and the next unit's K tiles stream into the slots as they
 // are released; Q tiles are double-buffered. One persistent CTA per SM walks the units.
-// Roles: warp 0 TMA producer, warp 1 MMA issuer (one thread), warps 2-5 the 128 threads that own
-// the TMEM lanes. TMEM: four 128-column slots, one 128 x 128 block each.
+// Roles: warp 0 TMA producer, warp 1 MMA issuer (one thread), warps 2-9 the lane owners: warp w
+// reads TMEM lanes 32 (w % 4) .. +31, warps 2-5 columns 0-63 and warps 6-9 columns 64-127 of every
+// block (the two halves' row statistics are merged between the phases). Causal and prompt masks
+// are decided per warp and 32-column half (every column visible, none, or per element). TMEM:
+// four 128-column slots, one 128 x 128 block each.
 #include "tc_common.cuh"
 
 namespace kve {
